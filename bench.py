@@ -1,0 +1,392 @@
+"""Benchmark of the MoE layer forward path (one step = gating -> align -> grouped FFN -> combine).
+
+Default workload: Mixtral-shaped prefill, bf16 (T=4096, H=4096, I=14336, E=8,
+top_k=2, norm_topk_prob=True), synthetic seeded inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (no data-path collective);
+`value` is the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_inputs import WORKLOADS  # noqa: E402
+
+METRIC = "MoE layer tokens/sec; grouped-FFN TFLOPS & routing GB/s as % of GB300 peak"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral", choices=list(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d.get("hbm_gbs", 6800.0), bf16_tflops=d.get("bf16_tflops", 1900.0),
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", 1700.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_device_inputs(wl, device, seed=0):
+    """Seeded synthetic inputs drawn on the device (same recipes as moe_inputs, torch RNG)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    T, H, I, E = wl.T, wl.H, wl.I, wl.E
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    hidden = torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(dt)
+    logits = torch.randn((T, E), generator=g, device=device, dtype=torch.float32)
+    if wl.logits == "jitter":
+        logits += 1e-3 * torch.arange(E, device=device, dtype=torch.float32)
+    elif wl.logits == "zipf":
+        r = torch.arange(1, E + 1, dtype=torch.float64)
+        p = r ** -1.2
+        bias = (2.0 * torch.log(p / p.sum())).float()
+        perm = torch.randperm(E, generator=torch.Generator().manual_seed(seed))
+        b = torch.empty(E)
+        b[perm] = bias
+        logits += b.to(device)
+    w13 = torch.empty((E, 2 * I, H), device=device, dtype=dt)
+    w2 = torch.empty((E, H, I), device=device, dtype=dt)
+    for e in range(E):   # one expert at a time keeps the fp32 temporaries small
+        w13[e] = (torch.randn((2 * I, H), generator=g, device=device) / H ** 0.5).to(dt)
+        w2[e] = (torch.randn((H, I), generator=g, device=device) / I ** 0.5).to(dt)
+    return hidden, logits, w13, w2
+
+
+def cpu_baseline(wl, hidden, logits, w13, w2, budget_s=20.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of tokens."""
+    from oracle import ffn, gating
+    import torch
+    t0 = time.perf_counter()
+    lg = logits.cpu().numpy()
+    wts, idx = gating.softmax_topk(lg, wl.k, wl.norm_topk_prob)
+    used = set(np.unique(idx[: min(wl.T, 64)]).tolist())
+
+    def host(t):
+        a = t.contiguous().cpu()
+        return a.view(torch.int16).numpy().view(np.uint16) if a.dtype == torch.bfloat16 else a.numpy()
+
+    hid = host(hidden)
+    w13h = {e: host(w13[e]) for e in used}
+    w2h = {e: host(w2[e]) for e in used}
+
+    class Lazy:
+        def __init__(self, d):
+            self.d = d
+
+        def __getitem__(self, e):
+            return self.d[int(e)]
+
+        def __len__(self):
+            return wl.E
+
+    copy_s = time.perf_counter() - t0
+    n, tot, done = 8, 0.0, 0
+    start = time.perf_counter()
+    while done < min(wl.T, 64):
+        tok = np.arange(done, min(done + n, wl.T, 64))
+        t1 = time.perf_counter()
+        ffn.layer_rows(hid, Lazy(w13h), Lazy(w2h), wl.dtype, wts, idx, tok)
+        tot += time.perf_counter() - t1
+        done += len(tok)
+        if time.perf_counter() - start > budget_s:
+            break
+    # routing over the whole batch is part of every token's cost
+    t2 = time.perf_counter()
+    wts, idx = gating.softmax_topk(lg, wl.k, wl.norm_topk_prob)
+    route_s = time.perf_counter() - t2
+    per_tok = tot / max(done, 1) + route_s / wl.T
+    return {"value": 1.0 / per_tok, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"numpy float64 oracle: routing over all {wl.T} tokens + FFN/combine of the "
+                      f"first {done} tokens (host copy of {len(used)} experts' weights, {copy_s:.1f}s, "
+                      f"not counted); BLAS threads = all host cores"}
+
+
+def run_reference(args, wl, rank, world):
+    """--impl reference: the oracle on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return
+    import torch
+    from oracle import ffn, gating
+    import moe_inputs as mi
+    d = mi.make_layer_inputs(wl, with_weights=False)
+    n_tok = 8
+    tok = np.arange(n_tok)
+    w, i = gating.softmax_topk(d["logits"], wl.k, wl.norm_topk_prob)
+    used = sorted(set(np.unique(i[:n_tok]).tolist()))
+    # weights only for the experts the sample touches (same distribution, per-expert seeds)
+    w13 = {e: mi.gen_normal(np.random.SeedSequence([wl.seed, 13, e]), (2 * wl.I, wl.H), 1 / np.sqrt(wl.H), wl.dtype)
+           for e in used}
+    w2 = {e: mi.gen_normal(np.random.SeedSequence([wl.seed, 2, e]), (wl.H, wl.I), 1 / np.sqrt(wl.I), wl.dtype)
+          for e in used}
+
+    class Lazy:
+        def __init__(self, dd):
+            self.d = dd
+
+        def __getitem__(self, e):
+            return self.d[int(e)]
+
+        def __len__(self):
+            return wl.E
+
+    def step():
+        ww, ii = gating.softmax_topk(d["logits"], wl.k, wl.norm_topk_prob)
+        ffn.layer_rows(d["hidden"], Lazy(w13), Lazy(w2), wl.dtype, ww, ii, tok)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    # one step = routing of all T tokens + FFN of n_tok tokens; scale FFN to the whole batch
+    t1 = time.perf_counter()
+    gating.softmax_topk(d["logits"], wl.k, wl.norm_topk_prob)
+    route = time.perf_counter() - t1
+    per_tok = (dt - route) / n_tok + route / wl.T
+    value = 1.0 / per_tok
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                                            "k": wl.k, "norm_topk_prob": wl.norm_topk_prob},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"each step: oracle routing of all {wl.T} tokens + FFN of {n_tok} tokens; "
+                                       "tokens/s extrapolated per token"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    wl = WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    import torch
+    import mixture_experts_routing_token_gb300 as moe
+    from mixture_experts_routing_token_gb300.build import build
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        build()
+    if world > 1:
+        dist.barrier()
+    moe.lib()
+
+    hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=rank)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    dcode = moe.MOE_BF16 if wl.dtype == "bf16" else moe.MOE_F32
+    ws = torch.empty(moe.moe_layer_workspace_size(dcode, T, H, I, E, k), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H), dtype=hidden.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        moe.moe_layer_forward(hidden, logits, w13, w2, k, wl.norm_topk_prob, out=out, workspace=ws,
+                              stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device events on the launching stream, per-kernel events
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    moe.profiler_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    moe.profiler_enable(False)
+    kern = moe.profiler_report()
+    clocks = clk.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms = ms_total / args.steps
+    value = T * world * args.steps / (ms_total / 1e3)
+
+    # ---- end to end through the public call: pinned host inputs in, output back to host
+    e2e = None
+    if not args.no_e2e:
+        h_hidden = hidden.cpu().pin_memory()
+        h_logits = logits.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d_hidden = torch.empty_like(hidden)
+        d_logits = torch.empty_like(logits)
+
+        def e2e_step():
+            d_hidden.copy_(h_hidden, non_blocking=True)
+            d_logits.copy_(h_logits, non_blocking=True)
+            moe.moe_layer_forward(d_hidden, d_logits, w13, w2, k, wl.norm_topk_prob, out=out, workspace=ws,
+                                  stream=stream)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": T * world * args.steps / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size() + h_logits.numel() * 4,
+               "d2h_bytes_per_step": h_out.numel() * h_out.element_size()}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peaks = measured_peaks()
+    S = T * k
+    launches = sum(v["launches"] for v in kern.values()) / args.steps
+    fc1 = kern.get("ffn_fc1_tc") or kern.get("ffn_fc1_simt")
+    roofline = None
+    if fc1 and fc1["launches"]:
+        fc1_ms = fc1["total_ms"] / fc1["launches"]
+        flops = 2.0 * S * H * (2 * I)          # FC1: S routed rows x H x 2I
+        ach = flops / (fc1_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "ffn_fc1_tc", "achieved": ach,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                    "traffic": None, "peak_source": peaks["source"] + " (burst bf16, cuBLAS)",
+                    "algorithmic_flops_per_launch": flops, "avg_launch_ms": fc1_ms}
+    per_kernel = {n: {"launches_per_step": v["launches"] / args.steps, "avg_ms": v["total_ms"] / max(v["launches"], 1),
+                      "share": v["total_ms"] / max(sum(x["total_ms"] for x in kern.values()), 1e-12)}
+                  for n, v in kern.items()}
+    ffn_flops = 6.0 * S * H * I
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
+                       "norm_topk_prob": wl.norm_topk_prob, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (weights %.2f GB read per step)" % (
+                           (w13.numel() + w2.numel()) * w13.element_size() / 1e9),
+                       "inputs": "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)))"},
+            "layer_tflops": ffn_flops / (ms / 1e3) / 1e12,
+            "roofline": roofline, "kernels": per_kernel, "gpu_launches": launches * args.steps,
+            "gpu_launches_per_step": launches, "clocks": clocks, "e2e": e2e, "lib": moe.version()}
+    if not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline(wl, hidden, logits, w13, w2)
+        except Exception as ex:   # the baseline is reported, never required
+            line["cpu_baseline"] = {"error": repr(ex)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

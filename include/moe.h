@@ -1,0 +1,200 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) Mixture-of-Experts layer forward path.
+ *
+ * The path, in order: gating softmax-top-k over router logits; the
+ * indices <-> multihot routing map with its position map; grouping of the
+ * routed slots by expert (counts, offsets, sorted token ids and weights,
+ * reverse slot ids); per-expert FC1 (w13) -> silu_and_mul -> FC2 (w2); the
+ * weighted sum of each token's k expert outputs.
+ *
+ * Sources of the semantics (web pages):
+ *   [mlc]  mlc-llm, python/mlc_llm/op/moe_misc.py, "Mixture of Experts operators":
+ *          gating_topk, gating_softmax_topk, moe_cumsum, get_indices,
+ *          get_indptr, scatter_output, moe_sum.
+ *   [mgt]  Megatron-LM, megatron/core/fusions/fused_indices_converter.py:
+ *          _indices_to_multihot_kernel, _multihot_to_indices_kernel,
+ *          IndicesToMultihot.
+ *   [p6]   project_6, ex_engine/csrc/moe_expert_gemm.cpp:
+ *          moe_decode_experts, moe_prefill_experts.
+ *
+ * Conventions for every entry point:
+ *   - Tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *     row-major, at least 16-byte aligned (256-byte for the workspace). Outputs
+ *     are preallocated by the caller; the library never allocates device memory.
+ *     Scratch comes from a caller-provided workspace sized by the matching
+ *     *_workspace_size() function.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream and performs no host
+ *     synchronisation.
+ *   - Return value: MOE_OK, or an MOE_ERR_* code when the host-side argument
+ *     check fails (nothing is launched) or a launch fails. moe_last_error()
+ *     gives a message for the calling thread's last failure.
+ *   - Problems found on the device (an expert index outside [0, E), a bounded
+ *     wait that gave up) are OR-ed as MOE_STATUS_* bits into the optional
+ *     caller word `status` (device int32, zeroed by the caller). Kernels never
+ *     trap.
+ *   - Index tensors are int32; T*k must be below 2^31.
+ *   - dtype is MOE_F32 or MOE_BF16 for hidden, w13, w2, out (and the FFN's
+ *     intermediate activation). Router logits, routing weights and probs are
+ *     float32.
+ *   - Logits must be finite. Rows of `indices` must name distinct experts.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* return codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1   /* null pointer, bad size, misalignment, k > E ... */
+#define MOE_ERR_UNSUPPORTED 2   /* a dtype/shape combination this build does not run */
+#define MOE_ERR_CUDA 3          /* a CUDA runtime or launch error */
+#define MOE_ERR_WORKSPACE 4     /* workspace pointer null/misaligned or too small */
+
+/* dtypes */
+#define MOE_F32 0
+#define MOE_BF16 1
+
+/* device status bits */
+#define MOE_STATUS_BAD_INDEX 1  /* a routed expert index was outside [0, E); the slot was dropped */
+#define MOE_STATUS_TIMEOUT 2    /* a bounded on-device wait gave up; outputs are invalid */
+
+/* Limits: 1 <= k <= 32, k <= E <= 1024. */
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_EXPERTS 1024
+
+/*
+ * Gating softmax-top-k.  [mlc] gating_topk / gating_softmax_topk.
+ *   logits   [T, E] float32 (finite).
+ *   weights  [T, k] float32 out: norm_topk_prob != 0: softmax over the k
+ *            selected logits; == 0: the full-row softmax probability of each
+ *            selected expert.
+ *   indices  [T, k] int32 out: the k experts with the largest logits in
+ *            descending order; of equal logits the lower expert index comes
+ *            first (the page keeps a value only when a candidate is strictly
+ *            greater).
+ * Selection is made on the logits in both modes: softmax is strictly
+ * increasing, so this equals ranking the probabilities. T may be 0.
+ */
+MOE_API int moe_gating_softmax_topk(const float* logits, int T, int E, int k, int norm_topk_prob,
+                                    float* weights, int32_t* indices, void* stream);
+
+/*
+ * Indices -> multihot routing map.  [mgt] _indices_to_multihot_kernel.
+ *   indices            [T, k] int32; an entry outside [0, E) (e.g. -1) is not routed.
+ *   probs              [T, k] float32.
+ *   multihot           [T, E] uint8 out: 1 where routed, else 0.
+ *   probs_in_multihot  [T, E] float32 out: probs[t, j] at expert indices[t, j], else 0.
+ *   position_map       [T, E] int32 out: j at expert indices[t, j], else -1.
+ * Every output element is written exactly once. If a row names an expert twice
+ * the lowest j is recorded.
+ */
+MOE_API int moe_indices_to_multihot(const int32_t* indices, const float* probs, int T, int k, int E,
+                                    uint8_t* multihot, float* probs_in_multihot,
+                                    int32_t* position_map, void* stream);
+
+/*
+ * Multihot -> indices (the inverse map).  [mgt] _multihot_to_indices_kernel.
+ *   probs_in_multihot  [T, E] float32, position_map [T, E] int32 (j or -1).
+ *   probs              [T, k] float32 out: probs[t, pos[t, e]] = probs_in_multihot[t, e];
+ *                      slots no expert maps to are 0.
+ *   indices_or_null    [T, k] int32 out (optional): the expert of each slot, -1 if none.
+ * Positions outside [0, k) are ignored; two experts of one row must not share a slot.
+ */
+MOE_API int moe_multihot_to_indices(const float* probs_in_multihot, const int32_t* position_map,
+                                    int T, int E, int k, float* probs, int32_t* indices_or_null,
+                                    void* stream);
+
+/*
+ * Align by expert.  [mlc] moe_cumsum + get_indptr (exclusive) + get_indices;
+ * [p6] moe_prefill_experts (counts, sorted_token_ids, sorted_weights).
+ *   indices  [T, k] int32, weights [T, k] float32 (the routing of each slot).
+ *   counts            [E]   int32 out: routed slots per expert.
+ *   offsets           [E+1] int32 out: exclusive prefix of counts, offsets[E] = routed slots.
+ *   sorted_token_ids  [T*k] int32 out: token of each sorted position.
+ *   sorted_weights    [T*k] float32 out: routing weight of each sorted position.
+ *   reverse_indices   [T*k] int32 out: flat slot t*k + j of each sorted position.
+ * Sorted position of slot (t, j) with expert e: offsets[e] + (number of tokens
+ * t' < t routed to e) — expert-major, ascending token, exactly the page's
+ * mask-cumsum order. A slot whose expert lies outside [0, E) is dropped and
+ * sets MOE_STATUS_BAD_INDEX; positions >= offsets[E] are then left unwritten.
+ *   ws / ws_bytes: workspace of at least moe_align_workspace_size(T, k, E) bytes.
+ */
+MOE_API size_t moe_align_workspace_size(int T, int k, int E);
+MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, int T, int k, int E,
+                                int32_t* counts, int32_t* offsets, int32_t* sorted_token_ids,
+                                float* sorted_weights, int32_t* reverse_indices, void* ws,
+                                size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * Grouped expert FFN and weighted combine.  [p6] moe_prefill_experts /
+ * moe_decode_experts; [mlc] scatter_output, moe_sum.
+ *   hidden  [T, H]      dtype.
+ *   w13     [E, 2I, H]  dtype; rows 0..I-1 of w13[e] are the gate projection,
+ *                       rows I..2I-1 the up projection; used as x @ w13[e]^T.
+ *   w2      [E, H, I]   dtype; used as act @ w2[e]^T.
+ *   counts, offsets, sorted_token_ids, sorted_weights, reverse_indices: as
+ *                       produced by moe_align_by_expert.
+ *   out     [T, H]      dtype out:
+ *     out[t] = sum_{j<k} w[t,j] * FC2_e(silu(FC1g_e(x_t)) * FC1u_e(x_t)),  e = expert of slot (t, j),
+ *     with float32 accumulation; for bf16 the activation is rounded to bf16
+ *     before FC2 and the output once at the end. Slots that were dropped by
+ *     the align step contribute nothing.
+ *   ws / ws_bytes: at least moe_grouped_ffn_workspace_size(...) bytes.
+ * bf16 with H % 64 == 0 and I % 64 == 0 runs on the tcgen05 tensor cores;
+ * other shapes and float32 run on a CUDA-core path.
+ */
+MOE_API size_t moe_grouped_ffn_workspace_size(int dtype, int T, int H, int I, int E, int k);
+MOE_API int moe_grouped_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int T,
+                            int H, int I, int E, int k, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* sorted_token_ids,
+                            const float* sorted_weights, const int32_t* reverse_indices,
+                            void* out, void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * Whole layer: gating -> align -> grouped FFN -> combine, in one call, on one
+ * stream, without host synchronisation.
+ *   hidden [T, H] dtype, router_logits [T, E] float32, w13, w2 as above.
+ *   out [T, H] dtype out.
+ *   topk_weights_or_null [T, k] float32 / topk_indices_or_null [T, k] int32:
+ *     optional copies of the gating result.
+ *   ws / ws_bytes: at least moe_layer_workspace_size(...) bytes.
+ */
+MOE_API size_t moe_layer_workspace_size(int dtype, int T, int H, int I, int E, int k);
+MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, const void* w13,
+                              const void* w2, int dtype, int T, int H, int I, int E, int k,
+                              int norm_topk_prob, void* out, float* topk_weights_or_null,
+                              int32_t* topk_indices_or_null, void* ws, size_t ws_bytes,
+                              int32_t* status, void* stream);
+
+/*
+ * Kernel timing.  moe_profiler_enable(1) makes every launch of this library
+ * record a CUDA event pair on its stream; moe_profiler_report() synchronises
+ * on those events, writes a JSON object {"kernel": {"launches": n,
+ * "total_ms": t}, ...} into buf (NUL-terminated, truncated to len) and clears
+ * the record. Returns the number of bytes needed (excluding the NUL).
+ * Not for use inside CUDA graph capture.
+ */
+MOE_API int moe_profiler_enable(int on);
+MOE_API int moe_profiler_report(char* buf, size_t len);
+
+/* Message for the calling thread's last failed call ("" if none). */
+MOE_API const char* moe_last_error(void);
+/* Build identification string. */
+MOE_API const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) Mixture-of-Experts layer forward path.
+
+The compute lives in ``libmoe_gb300.so`` (hand-written CUDA for sm_103a behind
+the C ABI of ``include/moe.h``); this package is its thin Python binding with
+the same entry-point names. Build the library with :func:`build`.
+"""
+from ._binding import (  # noqa: F401
+    MOE_BF16, MOE_F32, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_STATUS_BAD_INDEX, MOE_STATUS_TIMEOUT,
+    MoeError, SIGNATURES, LIB_PATH, lib, moe_align_by_expert, moe_align_workspace_size,
+    moe_gating_softmax_topk, moe_grouped_ffn, moe_grouped_ffn_workspace_size,
+    moe_indices_to_multihot, moe_layer_forward, moe_layer_workspace_size, moe_multihot_to_indices,
+    profiler_enable, profiler_report, version,
+)
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a) and return its path."""
+    from .build import build as _build
+    return _build(force=force)

@@ -1,0 +1,384 @@
+// C ABI: argument checks, workspace layout, launch sequencing, timing hooks.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace moe {
+
+static thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// ---- kernel timing -------------------------------------------------------------
+
+namespace {
+struct ProfRec {
+  std::string name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t pool_get() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+ProfScope::ProfScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ProfRec r{name, pool_get(), pool_get()};
+  cudaEventRecord(r.a, s);
+  g_prof.push_back(r);
+  slot = (int)g_prof.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (slot < (int)g_prof.size()) cudaEventRecord(g_prof[slot].b, stream);
+}
+
+// ---- argument checks ---------------------------------------------------------------
+
+namespace {
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+#define REQUIRE(cond, ...)                                   \
+  do {                                                       \
+    if (!(cond)) return fail(MOE_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+// A tensor argument: non-null, 16-byte aligned, device memory (when it holds data).
+int check_tensor(const void* p, long count, const char* name) {
+  if (count <= 0) return MOE_OK;
+  REQUIRE(p != nullptr, "%s is null", name);
+  REQUIRE(aligned(p, 16), "%s is not 16-byte aligned", name);
+  REQUIRE(is_device_ptr(p), "%s is not device memory", name);
+  return MOE_OK;
+}
+
+int check_routing_dims(int T, int E, int k) {
+  REQUIRE(T >= 0, "T must be >= 0 (got %d)", T);
+  REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "E must be in [1, %d] (got %d)", MOE_MAX_EXPERTS, E);
+  REQUIRE(k >= 1 && k <= MOE_MAX_TOPK && k <= E, "k must be in [1, min(E, %d)] (got k=%d, E=%d)",
+          MOE_MAX_TOPK, k, E);
+  REQUIRE((long)T * k < (1L << 31), "T*k must be below 2^31");
+  REQUIRE((long)T * E < (1L << 40), "T*E too large");
+  return MOE_OK;
+}
+
+int check_ffn_dims(int dtype, int H, int I) {
+  REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, "dtype must be MOE_F32 or MOE_BF16 (got %d)", dtype);
+  REQUIRE(H >= 1 && I >= 1, "H and I must be >= 1 (got H=%d, I=%d)", H, I);
+  return MOE_OK;
+}
+
+struct FfnWs {
+  void* act;
+  float* staging;
+  void* xs;
+};
+
+size_t dsize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+
+FfnWs carve_ffn(Carver& c, int dtype, long S, int H, int I) {
+  FfnWs w;
+  w.act = c.take<char>((size_t)S * I * dsize(dtype));
+  w.staging = c.take<float>((size_t)S * H);
+  const size_t xs = ffn_uses_tensor_cores(dtype, H, I) ? ffn_tc_extra_bytes(S, H) : 0;
+  w.xs = xs ? c.take<char>(xs) : nullptr;
+  return w;
+}
+
+struct AlignWs {
+  int32_t *counts, *offsets, *sorted_ids, *reverse;
+  float* sorted_w;
+  void* scratch;
+};
+
+AlignWs carve_align(Carver& c, long S, int E) {
+  AlignWs w;
+  w.counts = c.take<int32_t>(E);
+  w.offsets = c.take<int32_t>(E + 1);
+  w.sorted_ids = c.take<int32_t>(S);
+  w.sorted_w = c.take<float>(S);
+  w.reverse = c.take<int32_t>(S);
+  const size_t sb = align_scratch_bytes((int)S, E);
+  w.scratch = c.take<char>(sb ? sb : 1);
+  return w;
+}
+
+int check_ws(void* ws, size_t have, size_t need) {
+  if (need == 0) return MOE_OK;
+  if (ws == nullptr || !aligned(ws, 256))
+    return fail(MOE_ERR_WORKSPACE, "workspace is null or not 256-byte aligned");
+  if (have < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", have, need);
+  if (!is_device_ptr(ws)) return fail(MOE_ERR_WORKSPACE, "workspace is not device memory");
+  return MOE_OK;
+}
+
+int run_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int T, int H, int I,
+            int E, int k, const int32_t* counts, const int32_t* offsets, const int32_t* ids,
+            const float* sw, const int32_t* rev, void* out, const FfnWs& w, int32_t* status,
+            cudaStream_t s) {
+  FfnArgs a{hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, ids, sw, rev,
+            out, w.act, w.staging, w.xs, status};
+  return ffn_uses_tensor_cores(dtype, H, I) ? launch_ffn_tc(a, s) : launch_ffn_simt(a, s);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+MOE_API const char* moe_last_error(void) { return g_err; }
+
+MOE_API const char* moe_version(void) { return "moe-gb300 0.1 (sm_103a, tcgen05 grouped FFN)"; }
+
+MOE_API int moe_gating_softmax_topk(const float* logits, int T, int E, int k, int norm_topk_prob,
+                                    float* weights, int32_t* indices, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_tensor(logits, (long)T * E, "logits"))) return rc;
+  if ((rc = check_tensor(weights, (long)T * k, "weights"))) return rc;
+  if ((rc = check_tensor(indices, (long)T * k, "indices"))) return rc;
+  return launch_gating(logits, T, E, k, norm_topk_prob != 0, weights, indices, (cudaStream_t)stream);
+}
+
+MOE_API int moe_indices_to_multihot(const int32_t* indices, const float* probs, int T, int k, int E,
+                                    uint8_t* multihot, float* probs_in_multihot,
+                                    int32_t* position_map, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_tensor(indices, (long)T * k, "indices"))) return rc;
+  if ((rc = check_tensor(probs, (long)T * k, "probs"))) return rc;
+  if ((rc = check_tensor(multihot, (long)T * E, "multihot"))) return rc;
+  if ((rc = check_tensor(probs_in_multihot, (long)T * E, "probs_in_multihot"))) return rc;
+  if ((rc = check_tensor(position_map, (long)T * E, "position_map"))) return rc;
+  return launch_indices_to_multihot(indices, probs, T, k, E, multihot, probs_in_multihot, position_map,
+                                    (cudaStream_t)stream);
+}
+
+MOE_API int moe_multihot_to_indices(const float* probs_in_multihot, const int32_t* position_map,
+                                    int T, int E, int k, float* probs, int32_t* indices_or_null,
+                                    void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_tensor(probs_in_multihot, (long)T * E, "probs_in_multihot"))) return rc;
+  if ((rc = check_tensor(position_map, (long)T * E, "position_map"))) return rc;
+  if ((rc = check_tensor(probs, (long)T * k, "probs"))) return rc;
+  if (indices_or_null && (rc = check_tensor(indices_or_null, (long)T * k, "indices"))) return rc;
+  return launch_multihot_to_indices(probs_in_multihot, position_map, T, E, k, probs, indices_or_null,
+                                    (cudaStream_t)stream);
+}
+
+MOE_API size_t moe_align_workspace_size(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return align_up(align_scratch_bytes(T * k, E), 256);
+}
+
+MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, int T, int k, int E,
+                                int32_t* counts, int32_t* offsets, int32_t* sorted_token_ids,
+                                float* sorted_weights, int32_t* reverse_indices, void* ws,
+                                size_t ws_bytes, int32_t* status, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  const long S = (long)T * k;
+  if ((rc = check_tensor(indices, S, "indices"))) return rc;
+  if ((rc = check_tensor(weights, S, "weights"))) return rc;
+  if ((rc = check_tensor(counts, E, "counts"))) return rc;
+  if ((rc = check_tensor(offsets, E + 1, "offsets"))) return rc;
+  if ((rc = check_tensor(sorted_token_ids, S, "sorted_token_ids"))) return rc;
+  if ((rc = check_tensor(sorted_weights, S, "sorted_weights"))) return rc;
+  if ((rc = check_tensor(reverse_indices, S, "reverse_indices"))) return rc;
+  if (status && (rc = check_tensor(status, 1, "status"))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, align_scratch_bytes((int)S, E)))) return rc;
+  return launch_align(indices, weights, T, k, E, counts, offsets, sorted_token_ids, sorted_weights,
+                      reverse_indices, ws, status, (cudaStream_t)stream);
+}
+
+MOE_API size_t moe_grouped_ffn_workspace_size(int dtype, int T, int H, int I, int E, int k) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  Carver c(nullptr);
+  carve_ffn(c, dtype, (long)T * k, H, I);
+  return align_up(c.used, 256);
+}
+
+MOE_API int moe_grouped_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int T,
+                            int H, int I, int E, int k, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* sorted_token_ids,
+                            const float* sorted_weights, const int32_t* reverse_indices,
+                            void* out, void* ws, size_t ws_bytes, int32_t* status, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_ffn_dims(dtype, H, I))) return rc;
+  const long S = (long)T * k;
+  if ((rc = check_tensor(hidden, (long)T * H, "hidden"))) return rc;
+  if ((rc = check_tensor(w13, (long)E * 2 * I * H, "w13"))) return rc;
+  if ((rc = check_tensor(w2, (long)E * H * I, "w2"))) return rc;
+  if ((rc = check_tensor(counts, E, "counts"))) return rc;
+  if ((rc = check_tensor(offsets, E + 1, "offsets"))) return rc;
+  if ((rc = check_tensor(sorted_token_ids, S, "sorted_token_ids"))) return rc;
+  if ((rc = check_tensor(sorted_weights, S, "sorted_weights"))) return rc;
+  if ((rc = check_tensor(reverse_indices, S, "reverse_indices"))) return rc;
+  if ((rc = check_tensor(out, (long)T * H, "out"))) return rc;
+  if (status && (rc = check_tensor(status, 1, "status"))) return rc;
+  const size_t need = moe_grouped_ffn_workspace_size(dtype, T, H, I, E, k);
+  if ((rc = check_ws(ws, ws_bytes, need))) return rc;
+  Carver c(ws);
+  const FfnWs w = carve_ffn(c, dtype, S, H, I);
+  return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, sorted_token_ids,
+                 sorted_weights, reverse_indices, out, w, status, (cudaStream_t)stream);
+}
+
+MOE_API size_t moe_layer_workspace_size(int dtype, int T, int H, int I, int E, int k) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  const long S = (long)T * k;
+  Carver c(nullptr);
+  c.take<float>(S);
+  c.take<int32_t>(S);
+  carve_align(c, S, E);
+  carve_ffn(c, dtype, S, H, I);
+  return align_up(c.used, 256);
+}
+
+MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, const void* w13,
+                              const void* w2, int dtype, int T, int H, int I, int E, int k,
+                              int norm_topk_prob, void* out, float* topk_weights_or_null,
+                              int32_t* topk_indices_or_null, void* ws, size_t ws_bytes,
+                              int32_t* status, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_ffn_dims(dtype, H, I))) return rc;
+  const long S = (long)T * k;
+  if ((rc = check_tensor(hidden, (long)T * H, "hidden"))) return rc;
+  if ((rc = check_tensor(router_logits, (long)T * E, "router_logits"))) return rc;
+  if ((rc = check_tensor(w13, (long)E * 2 * I * H, "w13"))) return rc;
+  if ((rc = check_tensor(w2, (long)E * H * I, "w2"))) return rc;
+  if ((rc = check_tensor(out, (long)T * H, "out"))) return rc;
+  if (topk_weights_or_null && (rc = check_tensor(topk_weights_or_null, S, "topk_weights"))) return rc;
+  if (topk_indices_or_null && (rc = check_tensor(topk_indices_or_null, S, "topk_indices"))) return rc;
+  if (status && (rc = check_tensor(status, 1, "status"))) return rc;
+  const size_t need = moe_layer_workspace_size(dtype, T, H, I, E, k);
+  if ((rc = check_ws(ws, ws_bytes, need))) return rc;
+  if (T == 0) return MOE_OK;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  Carver c(ws);
+  float* tw = c.take<float>(S);
+  int32_t* ti = c.take<int32_t>(S);
+  if (topk_weights_or_null) tw = topk_weights_or_null;
+  if (topk_indices_or_null) ti = topk_indices_or_null;
+  const AlignWs al = carve_align(c, S, E);
+  const FfnWs fw = carve_ffn(c, dtype, S, H, I);
+
+  if ((rc = launch_gating(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, s))) return rc;
+  if ((rc = launch_align(ti, tw, T, k, E, al.counts, al.offsets, al.sorted_ids, al.sorted_w,
+                         al.reverse, al.scratch, status, s)))
+    return rc;
+  return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, al.counts, al.offsets, al.sorted_ids,
+                 al.sorted_w, al.reverse, out, fw, status, s);
+}
+
+MOE_API int moe_profiler_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+MOE_API int moe_profiler_report(char* buf, size_t len) {
+  std::map<std::string, std::pair<long, double>> agg;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& r : g_prof) {
+      float ms = 0.f;
+      cudaEventSynchronize(r.b);
+      if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+        cudaGetLastError();
+        ms = 0.f;
+      }
+      auto& a = agg[r.name];
+      a.first += 1;
+      a.second += ms;
+      g_pool.push_back(r.a);
+      g_pool.push_back(r.b);
+    }
+    g_prof.clear();
+  }
+  std::string js = "{";
+  bool first = true;
+  for (auto& kv : agg) {
+    char tmp[256];
+    snprintf(tmp, sizeof(tmp), "%s\"%s\": {\"launches\": %ld, \"total_ms\": %.6f}", first ? "" : ", ",
+             kv.first.c_str(), kv.second.first, kv.second.second);
+    js += tmp;
+    first = false;
+  }
+  js += "}";
+  if (buf && len) {
+    const size_t n = js.size() < len - 1 ? js.size() : len - 1;
+    memcpy(buf, js.data(), n);
+    buf[n] = 0;
+  }
+  return (int)js.size();
+}
+
+}  // extern "C"

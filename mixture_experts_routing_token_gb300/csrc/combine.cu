@@ -1,0 +1,82 @@
+// Weighted combine: out[t] = sum_{j<k} staging[t*k + j], j ascending, fp32,
+// one rounding to the output dtype.
+// mlc-llm moe_misc.py moe_sum (sum of the [T, k, H] expert outputs over k);
+// the routing weight was already applied by the FC2 epilogue.
+// HBM-bound streaming kernel: 16-byte loads, one thread per 4 output columns.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+template <class OutT>
+struct Out4;
+template <>
+struct Out4<float> {
+  static __device__ __forceinline__ void store(float* o, float4 v) {
+    *reinterpret_cast<float4*>(o) = v;
+  }
+};
+template <>
+struct Out4<__nv_bfloat16> {
+  static __device__ __forceinline__ void store(__nv_bfloat16* o, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(o) = u;
+  }
+};
+
+template <class OutT>
+__global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restrict__ staging, long T,
+                                                          int k, int H4, OutT* __restrict__ out) {
+  const long n = T * H4;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const long t = i / H4;
+    const int c = (int)(i - t * H4);
+    const float4* src = staging + t * k * H4 + c;
+    float4 acc = __ldcs(src);
+    for (int j = 1; j < k; ++j) {
+      const float4 v = __ldcs(src + (long)j * H4);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    Out4<OutT>::store(out + i * 4, acc);
+  }
+}
+
+template <class OutT>
+__global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __restrict__ staging, long T,
+                                                             int k, int H, OutT* __restrict__ out) {
+  const long n = T * H;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const long t = i / H;
+    const int h = (int)(i - t * H);
+    float acc = staging[t * k * H + h];
+    for (int j = 1; j < k; ++j) acc += staging[(t * k + j) * H + h];
+    out[i] = from_float<OutT>(acc);
+  }
+}
+
+template <class OutT>
+int launch_t(const float* staging, int T, int k, int H, OutT* out, cudaStream_t s) {
+  ProfScope ps("combine", s);
+  const int grid = num_sms() * 8;
+  if (H % 4 == 0)
+    combine_vec_kernel<OutT><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(staging), T, k, H / 4, out);
+  else
+    combine_scalar_kernel<OutT><<<grid, 256, 0, s>>>(staging, T, k, H, out);
+  return check_launch("combine");
+}
+
+}  // namespace
+
+int launch_combine(const float* staging, int T, int k, int H, int dtype, void* out, cudaStream_t s) {
+  if ((long)T * H == 0) return MOE_OK;
+  return dtype == MOE_F32 ? launch_t<float>(staging, T, k, H, static_cast<float*>(out), s)
+                          : launch_t<__nv_bfloat16>(staging, T, k, H, static_cast<__nv_bfloat16*>(out), s);
+}
+
+}  // namespace moe

@@ -1,0 +1,102 @@
+// Internal helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- host side -------------------------------------------------------------
+
+// Records a message for moe_last_error() and returns `code`.
+int fail(int code, const char* fmt, ...);
+// Turns the last CUDA launch error into MOE_ERR_CUDA (or MOE_OK).
+int check_launch(const char* what);
+// Multiprocessor count of the current device (cached per device).
+int num_sms();
+
+// Kernel timing hooks (no-ops unless moe_profiler_enable(1)).
+struct ProfScope {
+  ProfScope(const char* name, cudaStream_t s);
+  ~ProfScope();
+  int slot;
+  cudaStream_t stream;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Bump allocator over a caller workspace; every carve is 256-byte aligned.
+struct Carver {
+  char* base;
+  size_t used;
+  explicit Carver(void* b) : base(static_cast<char*>(b)), used(0) {}
+  template <class T>
+  T* take(size_t count) {
+    used = align_up(used, 256);
+    T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
+    used += count * sizeof(T);
+    return p;
+  }
+};
+
+// ---- launchers (one per translation unit) -------------------------------
+
+int launch_gating(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                  cudaStream_t s);
+int launch_indices_to_multihot(const int32_t* idx, const float* probs, int T, int k, int E,
+                               uint8_t* mh, float* pm, int32_t* pos, cudaStream_t s);
+int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E, int k,
+                               float* probs, int32_t* idx, cudaStream_t s);
+
+size_t align_scratch_bytes(int S, int E);
+int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
+                 int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
+                 void* scratch, int32_t* status, cudaStream_t s);
+
+struct FfnArgs {
+  const void* hidden;
+  const void* w13;
+  const void* w2;
+  int dtype, T, H, I, E, k;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* sorted_ids;
+  const float* sorted_w;
+  const int32_t* reverse;
+  void* out;
+  void* act;        // [S, I] dtype
+  float* staging;   // [S, H] float32
+  void* xs;         // [S, H] dtype: expert-sorted copy of hidden (only without the TMA gather)
+  int32_t* status;
+};
+
+bool ffn_uses_tensor_cores(int dtype, int H, int I);
+size_t ffn_tc_extra_bytes(long S, int H);
+int launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
+int launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
+int launch_combine(const float* staging, int T, int k, int H, int dtype, void* out,
+                   cudaStream_t s);
+
+// ---- device side -----------------------------------------------------------
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <class T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// silu(z) = z / (1 + e^-z); e^-z overflows to +inf for very negative z, giving -0.
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+}  // namespace moe

@@ -139,7 +139,7 @@ def layer_rows(hidden, w13, w2, dtype: str, topk_weights, topk_indices, tokens) 
     tokens = np.asarray(tokens, dtype=np.int64)
     idx = np.asarray(topk_indices)[tokens]
     wts = np.asarray(topk_weights)[tokens]
-    E = np.asarray(w13).shape[0]
+    E = len(w13)          # w13 / w2 may be any per-expert indexable (array or mapping)
     al = _align.align_by_expert(idx, wts, E)
     k = idx.shape[1]
     return grouped_ffn(np.asarray(hidden)[tokens], w13, w2, dtype, k, al["counts"],

@@ -1,0 +1,138 @@
+"""GPU parity of the grouped FFN and of the whole layer against the oracle, through the C ABI.
+
+Tolerance: max|err| <= 2e-2 * max|ref| for bf16 inputs with fp32
+accumulation, 1e-4 for float32. Full-size workloads are compared on a
+seeded sample of tokens (plus every token of the least-loaded experts), each
+row computed independently by the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import DEV, assert_close_rel_max, layer_tolerance, need_gpu, to_dev, to_np64
+from moe_inputs import WORKLOADS, make_layer_inputs
+from oracle import align, ffn, gating
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(moe, d, status=None):
+    dt = d["dtype"]
+    tw = torch.empty((d["T"], d["k"]), dtype=torch.float32, device=DEV)
+    ti = torch.empty((d["T"], d["k"]), dtype=torch.int32, device=DEV)
+    out = moe.moe_layer_forward(to_dev(d["hidden"], dt), torch.from_numpy(d["logits"]).to(DEV),
+                                to_dev(d["w13"], dt), to_dev(d["w2"], dt), d["k"], d["norm_topk_prob"],
+                                topk_weights=tw, topk_indices=ti, status=status)
+    torch.cuda.synchronize()
+    return out, tw, ti
+
+
+def _full_check(moe, d):
+    out, tw, ti = _layer(moe, d)
+    ref = ffn.layer_forward(d["logits"], d["hidden"], d["w13"], d["w2"], d["k"], d["norm_topk_prob"],
+                            d["dtype"])
+    np.testing.assert_array_equal(ti.cpu().numpy(), ref["topk_indices"])
+    assert_close_rel_max(to_np64(out), ref["out"], layer_tolerance(d["dtype"]), "layer out")
+
+
+def test_tiny_f32_workload_full():
+    moe = need_gpu()
+    _full_check(moe, make_layer_inputs("tiny"))
+
+
+@pytest.mark.parametrize("name", ["decode1", "decode8", "decode64"])
+def test_decode_workloads_full(name):
+    moe = need_gpu()
+    _full_check(moe, make_layer_inputs(name))
+
+
+# tensor-core path: H, I multiples of 64; ragged expert counts, several tiles, a tail
+@pytest.mark.parametrize("T,H,I,E,k,norm", [
+    (1, 64, 64, 4, 1, True),
+    (5, 128, 192, 8, 2, True),          # I % 128 == 64: half-empty last gate/up tile
+    (300, 256, 256, 8, 2, True),        # counts ~75 per expert, one ragged M tile each
+    (700, 512, 384, 8, 2, False),
+    (1000, 256, 128, 16, 4, True),      # several M tiles per expert + tail
+    (513, 320, 640, 5, 3, True),        # H % 256 == 64: partial FC2 N tile
+    (2048, 1024, 512, 64, 8, False),
+    (257, 128, 128, 128, 8, True),      # many empty experts
+])
+def test_layer_tensor_core_shapes(T, H, I, E, k, norm):
+    moe = need_gpu()
+    _full_check(moe, make_layer_inputs(T=T, H=H, I=I, E=E, k=k, norm_topk_prob=norm, dtype="bf16",
+                                       logits="distinct", seed=T + H))
+
+
+# CUDA-core path: float32, and bf16 shapes the tensor path does not take
+@pytest.mark.parametrize("T,H,I,E,k,dtype", [
+    (64, 128, 256, 8, 2, "f32"),
+    (33, 40, 24, 3, 2, "f32"),
+    (100, 72, 56, 6, 3, "bf16"),
+    (1, 8, 8, 2, 2, "f32"),
+])
+def test_layer_cuda_core_shapes(T, H, I, E, k, dtype):
+    moe = need_gpu()
+    _full_check(moe, make_layer_inputs(T=T, H=H, I=I, E=E, k=k, norm_topk_prob=True, dtype=dtype,
+                                       logits="distinct", seed=T))
+
+
+def test_grouped_ffn_entry_point_with_oracle_routing():
+    """moe_grouped_ffn fed the oracle's own align outputs."""
+    moe = need_gpu()
+    d = make_layer_inputs(T=400, H=256, I=320, E=12, k=3, norm_topk_prob=True, dtype="bf16",
+                          logits="zipf", seed=5)
+    w, i = gating.softmax_topk(d["logits"], 3, True)
+    al = align.align_by_expert(i, w, 12)
+    t = {k_: torch.from_numpy(np.ascontiguousarray(al[k_])).to(DEV)
+         for k_ in ("counts", "offsets", "sorted_token_ids", "sorted_weights", "reverse_indices")}
+    out = moe.moe_grouped_ffn(to_dev(d["hidden"], "bf16"), to_dev(d["w13"], "bf16"), to_dev(d["w2"], "bf16"),
+                              3, t["counts"], t["offsets"], t["sorted_token_ids"], t["sorted_weights"],
+                              t["reverse_indices"])
+    torch.cuda.synchronize()
+    ref = ffn.grouped_ffn(d["hidden"], d["w13"], d["w2"], "bf16", 3, al["counts"], al["offsets"],
+                          al["sorted_token_ids"], al["sorted_weights"], al["reverse_indices"])
+    assert_close_rel_max(to_np64(out), ref, 2e-2, "grouped ffn")
+
+
+def test_layer_repeated_calls_are_identical():
+    moe = need_gpu()
+    d = make_layer_inputs(T=600, H=256, I=256, E=8, k=2, dtype="bf16", logits="distinct", seed=9)
+    a, _, _ = _layer(moe, d)
+    b, _, _ = _layer(moe, d)
+    assert torch.equal(a, b)
+
+
+def test_layer_status_stays_clear():
+    moe = need_gpu()
+    d = make_layer_inputs(T=300, H=128, I=128, E=8, k=2, dtype="bf16", logits="distinct", seed=2)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _layer(moe, d, status=st)
+    assert int(st.item()) == 0
+
+
+def _sample_tokens(ti_np, T, E, n, seed):
+    rng = np.random.default_rng(seed)
+    tok = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    counts = np.bincount(ti_np.reshape(-1), minlength=E)
+    light = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0][:8]
+    for e in light:
+        rows = np.nonzero((ti_np == e).any(axis=1))[0][:64]
+        tok.update(rows.tolist())
+    return np.array(sorted(tok), dtype=np.int64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n", [("mixtral", 512), ("fine", 512), ("skew", 384)])
+def test_full_size_workload_sampled(name, n):
+    moe = need_gpu()
+    d = make_layer_inputs(name)
+    out, tw, ti = _layer(moe, d)
+    w_ref, i_ref = gating.softmax_topk(d["logits"], d["k"], d["norm_topk_prob"])
+    ti_np = ti.cpu().numpy()
+    np.testing.assert_array_equal(ti_np, i_ref)
+    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=1e-6, atol=0)
+    tok = _sample_tokens(ti_np, d["T"], d["E"], n, seed=1)
+    ref = ffn.layer_rows(d["hidden"], d["w13"], d["w2"], d["dtype"], w_ref, i_ref, tok)
+    got = to_np64(out[torch.from_numpy(tok).to(DEV)])
+    assert_close_rel_max(got, ref, 2e-2, f"{name} sampled rows")
+    assert np.isfinite(to_np64(out)).all()

@@ -1,0 +1,165 @@
+"""GPU parity of the routing steps against the oracle, through the C ABI.
+
+Bit-exact: indices, multihot, position maps, counts, offsets, sorted ids,
+reverse ids, sorted weights (a copy of routing weights). Routing weights:
+within 1e-6 relative of the oracle's float64 value rounded to float32.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import DEV, need_gpu
+from moe_inputs import WORKLOADS, gen_logits
+from oracle import align, gating, multihot
+
+pytestmark = pytest.mark.gpu
+
+W_RTOL = 1e-6
+
+
+def _gating_case(moe, x, k, norm):
+    w_ref, i_ref = gating.softmax_topk(x, k, norm)
+    w, i = moe.moe_gating_softmax_topk(torch.from_numpy(x).to(DEV), k, norm)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(i.cpu().numpy(), i_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=W_RTOL, atol=0)
+    return w, i, w_ref, i_ref
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_gating_on_workload_logits(name):
+    moe = need_gpu()
+    wl = WORKLOADS[name]
+    x = gen_logits(np.random.SeedSequence(wl.seed).spawn(5)[0], wl.T, wl.E, wl.logits,
+                   np.random.SeedSequence(wl.seed).spawn(5)[4])
+    _gating_case(moe, x, wl.k, wl.norm_topk_prob)
+    _gating_case(moe, x, wl.k, not wl.norm_topk_prob)
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (2, 1), (3, 2), (5, 5), (7, 3), (8, 8), (16, 4), (31, 1),
+                                 (32, 32), (33, 8), (100, 6), (128, 1), (200, 16), (256, 8),
+                                 (1000, 32), (1024, 2)])
+@pytest.mark.parametrize("norm", [True, False])
+def test_gating_shapes(E, k, norm):
+    moe = need_gpu()
+    x = gen_logits(np.random.SeedSequence(E * 1000 + k), 257, E, "distinct")
+    _gating_case(moe, x, k, norm)
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 8), (6, 6), (40, 5)])
+def test_gating_ties_go_to_lower_index(E, k):
+    moe = need_gpu()
+    rng = np.random.default_rng(E)
+    x = (rng.integers(-2, 3, size=(300, E)) * 0.5).astype(np.float32)
+    x[0] = 1.0  # a row of all-equal values
+    _gating_case(moe, x, k, True)
+    _gating_case(moe, x, k, False)
+
+
+def test_gating_empty_and_single():
+    moe = need_gpu()
+    w, i = moe.moe_gating_softmax_topk(torch.zeros((0, 8), device=DEV), 2)
+    assert w.shape == (0, 2)
+    _gating_case(moe, np.array([[0.5, -1.0, 3.0]], np.float32), 2, True)
+
+
+@pytest.mark.parametrize("T,E,k", [(16384, 64, 8), (37, 5, 2), (3, 1024, 32), (1000, 128, 8), (1, 4, 4)])
+def test_multihot_round_trip(T, E, k):
+    moe = need_gpu()
+    x = gen_logits(np.random.SeedSequence(T + E), T, E, "distinct")
+    w_ref, i_ref = gating.softmax_topk(x, k, True)
+    mh_r, pm_r, pos_r = multihot.indices_to_multihot(i_ref, w_ref, E)
+    mh, pm, pos = moe.moe_indices_to_multihot(torch.from_numpy(i_ref).to(DEV),
+                                              torch.from_numpy(w_ref).to(DEV), E)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(mh.cpu().numpy(), mh_r)
+    np.testing.assert_array_equal(pm.cpu().numpy(), pm_r)
+    np.testing.assert_array_equal(pos.cpu().numpy(), pos_r)
+    p2, i2 = moe.moe_multihot_to_indices(pm, pos, k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(p2.cpu().numpy(), w_ref)
+    np.testing.assert_array_equal(i2.cpu().numpy(), i_ref)
+
+
+def test_multihot_page_examples(gold):
+    moe = need_gpu()
+    g = gold("indices_to_multihot")
+    mh, pm, pos = moe.moe_indices_to_multihot(torch.tensor(g["indices"], dtype=torch.int32, device=DEV),
+                                              torch.tensor(g["probs"], dtype=torch.float32, device=DEV), g["E"])
+    assert mh.cpu().tolist() == g["multihot"]
+    assert pos.cpu().tolist() == g["position_map"]
+    np.testing.assert_array_equal(pm.cpu().numpy(), np.array(g["probs_in_multihot"], np.float32))
+    g = gold("multihot_to_indices")
+    p, _ = moe.moe_multihot_to_indices(torch.tensor(g["probs_in_multihot"], dtype=torch.float32, device=DEV),
+                                       torch.tensor(g["position_map"], dtype=torch.int32, device=DEV), g["k"])
+    np.testing.assert_array_equal(p.cpu().numpy(), np.array(g["probs"], np.float32))
+
+
+def test_multihot_invalid_and_duplicate_indices():
+    moe = need_gpu()
+    idx = np.array([[-1, 2], [5, -7], [1, 1], [3, 0]], np.int32)
+    pr = np.array([[0.5, 0.25], [0.1, 0.2], [0.3, 0.4], [0.6, 0.7]], np.float32)
+    for E in (4, 5):   # vector and scalar store paths
+        ref = multihot.indices_to_multihot(idx, pr, E)
+        got = moe.moe_indices_to_multihot(torch.from_numpy(idx).to(DEV), torch.from_numpy(pr).to(DEV), E)
+        for r, g_ in zip(ref, got):
+            np.testing.assert_array_equal(g_.cpu().numpy(), r)
+        rp, ri = multihot.multihot_to_indices(ref[1], ref[2], 2)
+        gp, gi = moe.moe_multihot_to_indices(got[1], got[2], 2)
+        np.testing.assert_array_equal(gp.cpu().numpy(), rp)
+        np.testing.assert_array_equal(gi.cpu().numpy(), ri)
+
+
+def _align_case(moe, i_np, w_np, E):
+    ref = align.align_by_expert(i_np, w_np, E)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = moe.moe_align_by_expert(torch.from_numpy(i_np).to(DEV), torch.from_numpy(w_np).to(DEV), E,
+                                  status=status)
+    torch.cuda.synchronize()
+    n = ref["valid_slots"]
+    np.testing.assert_array_equal(got["counts"].cpu().numpy(), ref["counts"])
+    np.testing.assert_array_equal(got["offsets"].cpu().numpy(), ref["offsets"])
+    for key in ("sorted_token_ids", "sorted_weights", "reverse_indices"):
+        np.testing.assert_array_equal(got[key].cpu().numpy()[:n], ref[key][:n], err_msg=key)
+    return int(status.item())
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_align_on_workload_routing(name):
+    moe = need_gpu()
+    wl = WORKLOADS[name]
+    ss = np.random.SeedSequence(wl.seed).spawn(5)
+    x = gen_logits(ss[0], wl.T, wl.E, wl.logits, ss[4])
+    w, i = gating.softmax_topk(x, wl.k, wl.norm_topk_prob)
+    assert _align_case(moe, i, w, wl.E) == 0
+    if name == "skew":
+        assert (np.bincount(i.reshape(-1), minlength=wl.E) == 0).any()   # empty experts exercised
+
+
+@pytest.mark.parametrize("T,E,k", [(0, 8, 2), (1, 8, 8), (4095, 3, 1), (4096, 7, 2), (4097, 64, 8),
+                                   (9000, 1024, 4), (50000, 16, 2), (3, 1, 1)])
+def test_align_shapes(T, E, k):
+    moe = need_gpu()
+    x = gen_logits(np.random.SeedSequence(T * 3 + E), T, E, "distinct")
+    w, i = gating.softmax_topk(x, k, True) if T else (np.zeros((0, k), np.float32), np.zeros((0, k), np.int32))
+    assert _align_case(moe, i, w, E) == 0
+
+
+def test_align_all_to_one_expert_and_page_example(gold):
+    moe = need_gpu()
+    T, E = 10000, 16
+    i = np.zeros((T, 1), np.int32) + 11
+    w = np.random.default_rng(0).random((T, 1)).astype(np.float32)
+    assert _align_case(moe, i, w, E) == 0
+    g = gold("moe_cumsum")
+    i = np.array(g["indices"], np.int32)
+    assert _align_case(moe, i, np.ones(i.shape, np.float32), g["E"]) == 0
+
+
+def test_align_invalid_index_sets_status_and_drops_slot():
+    moe = need_gpu()
+    for T in (3, 6000):    # single-chunk and multi-chunk launches
+        i = np.tile(np.array([[0, 9], [-1, 1], [1, 0]], np.int32), (T // 3, 1))
+        w = np.ones(i.shape, np.float32)
+        st = _align_case(moe, i, w, 3)
+        assert st & moe.MOE_STATUS_BAD_INDEX
