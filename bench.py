@@ -141,6 +141,24 @@ def make_device_inputs(wl, device, seed=0):
     return hidden, logits, w13, w2
 
 
+def kernel_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture, or None when the
+    capture is for another workload or the kernel sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec["bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
+
+
 def cpu_baseline(wl, hidden, logits, w13, w2, budget_s=20.0):
     """The oracle as it stands, on the host cores, over a bounded sample of tokens."""
     from oracle import ffn, gating
@@ -360,7 +378,7 @@ def main():
         ach = flops / (fc1_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "kernel": "ffn_fc1_tc", "achieved": ach,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                    "traffic": None, "peak_source": peaks["source"] + " (burst bf16, cuBLAS)",
+                    "traffic": kernel_traffic("ffn_fc1_tc", wl.name), "peak_source": peaks["source"] + " (burst bf16, cuBLAS)",
                     "algorithmic_flops_per_launch": flops, "avg_launch_ms": fc1_ms}
     per_kernel = {n: {"launches_per_step": v["launches"] / args.steps, "avg_ms": v["total_ms"] / max(v["launches"], 1),
                       "share": v["total_ms"] / max(sum(x["total_ms"] for x in kern.values()), 1e-12)}

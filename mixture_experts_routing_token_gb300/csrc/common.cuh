@@ -1,6 +1,7 @@
 // Internal helpers shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -74,6 +75,13 @@ struct FfnArgs {
   void* xs;         // [S, H] dtype: expert-sorted copy of hidden (only without the TMA gather)
   int32_t* status;
 };
+
+// bf16 matrix [rows, cols] row-major as a TMA tensor map: box = box_rows x 64
+// columns, 128-byte swizzle, zero fill out of bounds.
+int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// Token-count threshold at or below which the weight-streaming decode kernels run.
+constexpr int kDecodeMaxTokens = 64;
+int launch_ffn_decode(const FfnArgs& a, cudaStream_t s);
 
 bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);

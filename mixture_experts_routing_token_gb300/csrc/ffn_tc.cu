@@ -12,8 +12,10 @@
 //
 // CTA = 6 warps, one CTA per SM:
 //   warp 0      TMA producer: A tile (128 x 64 bf16) and B tile (256 x 64 bf16)
-//               per k-step into a 4-stage ring. FC1's A rows are the expert's
-//               tokens, fetched straight from `hidden` by 4-row TMA gathers.
+//               per k-step into a 4-stage ring. FC1's A operand is the
+//               expert-sorted copy of the token rows written by
+//               gather_rows_kernel (one tiled TMA load per stage; a fused
+//               4-row TMA gather per stage measured 3.4x slower on GB300).
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16) per k-step into
 //               one of two TMEM accumulators (2 x 256 columns), so the
 //               epilogue of tile i overlaps the main loop of tile i+1.
@@ -26,8 +28,6 @@
 // Every wait is bounded; on expiry the CTA drains, frees TMEM, and reports
 // MOE_STATUS_TIMEOUT.
 #include <cuda.h>
-#include <stdio.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "sm100_ptx.cuh"
@@ -89,7 +89,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int MODE, bool GATHER>
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const TcParams P) {
@@ -156,10 +156,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     const int KB = P.K / BK;
-    if (GATHER || lane == 0) {
+    if (lane == 0) {
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
         const TileInfo ti = decode_tile(t, tile_start, P.E, P.NT);
-        const int cnt = __ldg(P.counts + ti.e);
         const int a_row0 = __ldg(P.offsets + ti.e) + ti.m_tile * BM;
         int b_row0, b_row1;
         if (MODE == MODE_FC1) {
@@ -169,46 +168,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           b_row0 = ti.e * P.b_rows + ti.n_tile * BN;
           b_row1 = b_row0 + 128;
         }
-        int rid[4] = {0, 0, 0, 0};
-        if (GATHER) {
-          const int valid_rows = min(BM, cnt - ti.m_tile * BM);
-          const int first = __ldg(P.sorted_ids + a_row0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = lane * 4 + i;
-            rid[i] = r < valid_rows ? __ldg(P.sorted_ids + a_row0 + r) : first;
-          }
-        }
         for (int kb = 0; kb < KB; ++kb) {
-          int ok = 1;
-          if (lane == 0) ok = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p,
-                                             WAIT_LIMIT_NS);
-          if (GATHER) ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) goto producer_done;
+          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, WAIT_LIMIT_NS))
+            goto producer_done;
           const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            ptx::tma_load_2d(sB(stage), &tmB, kb * BK, b_row0, fb);
-            ptx::tma_load_2d(sB(stage) + 128 * 128, &tmB, kb * BK, b_row1, fb);
-            if (!GATHER) ptx::tma_load_2d(sA(stage), &tmA, kb * BK, a_row0, fb);
-          }
-          if (GATHER) {
-            __syncwarp();
-            ptx::tma_gather4(sA(stage) + lane * 512, &tmA, kb * BK, rid[0], rid[1], rid[2], rid[3], fb);
-          }
+          ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          ptx::tma_load_2d(sA(stage), &tmA, kb * BK, a_row0, fb);
+          ptx::tma_load_2d(sB(stage), &tmB, kb * BK, b_row0, fb);
+          ptx::tma_load_2d(sB(stage) + 128 * 128, &tmB, kb * BK, b_row1, fb);
           issued_parity[stage] = (int)ph;
           if (++stage == STAGES) { stage = 0; ph ^= 1u; }
         }
       }
     producer_done:
       // wait until every copy this thread issued has landed
-      if (lane == 0) {
-        int dummy = 0;
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0)
-            ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (uint32_t)issued_parity[s], &dummy,
-                           WAIT_LIMIT_NS);
-      }
+      int dummy = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0)
+          ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (uint32_t)issued_parity[s], &dummy, WAIT_LIMIT_NS);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -318,8 +295,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (tid == 0 && abort_flag && P.status) atomicOr(P.status, MOE_STATUS_TIMEOUT);
 }
 
-// Copies the expert-sorted token rows of `hidden` into x_sorted (used when the
-// 4-row TMA gather is switched off).
+// Copies the expert-sorted token rows of `hidden` into x_sorted, the FC1 A operand
+// (16-byte vectors; rows p < offsets[E]).
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
                                    const int32_t* __restrict__ offsets, int E, int H16,
                                    uint4* __restrict__ xs) {
@@ -352,6 +329,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // bf16 matrix [rows, cols] row-major; box = box_rows x 64 columns, 128-byte swizzle.
 int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -367,14 +346,16 @@ int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return MOE_OK;
 }
 
-template <int MODE, bool GATHER>
+namespace {
+
+template <int MODE>
 int launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, long S, cudaStream_t s,
               const char* name) {
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(ffn_tc_kernel<MODE, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(ffn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DSMEM_BYTES) != cudaSuccess)
       return check_launch(name);
     attr[dev] = true;
@@ -383,17 +364,8 @@ int launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, lon
   const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
   if (grid <= 0) return MOE_OK;
   ProfScope ps(name, s);
-  ffn_tc_kernel<MODE, GATHER><<<grid, THREADS, DSMEM_BYTES, s>>>(a, b, p);
+  ffn_tc_kernel<MODE><<<grid, THREADS, DSMEM_BYTES, s>>>(a, b, p);
   return check_launch(name);
-}
-
-bool fc1_gather_enabled() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MOE_FC1_GATHER4");
-    v = (e && e[0] == '0') ? 0 : 1;
-  }
-  return v == 1;
 }
 
 }  // namespace
@@ -402,41 +374,31 @@ bool ffn_uses_tensor_cores(int dtype, int H, int I) {
   return dtype == MOE_BF16 && H % 64 == 0 && I % 64 == 0 && H > 0 && I > 0;
 }
 
-size_t ffn_tc_extra_bytes(long S, int H) {
-  return fc1_gather_enabled() ? 0 : (size_t)S * H * 2;
-}
+size_t ffn_tc_extra_bytes(long S, int H) { return (size_t)S * H * 2; }
 
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   const long S = (long)a.T * a.k;
   if (S == 0) return MOE_OK;
-  const bool gather = fc1_gather_enabled();
+  if (a.T <= kDecodeMaxTokens) return launch_ffn_decode(a, s);
   CUtensorMap tA1, tB1, tA2, tB2;
   int rc;
-  if (gather) {
-    rc = make_tmap(&tA1, a.hidden, (uint64_t)a.T, (uint64_t)a.H, 1);
-  } else {
-    const int H16 = a.H / 8;
+  {
     ProfScope ps("gather_rows", s);
     gather_rows_kernel<<<num_sms() * 4, 256, 0, s>>>(static_cast<const uint4*>(a.hidden), a.sorted_ids,
-                                                     a.offsets, a.E, H16, static_cast<uint4*>(a.xs));
-    rc = check_launch("gather_rows");
-    if (rc) return rc;
-    rc = make_tmap(&tA1, a.xs, (uint64_t)S, (uint64_t)a.H, BM);
+                                                     a.offsets, a.E, a.H / 8, static_cast<uint4*>(a.xs));
+    if ((rc = check_launch("gather_rows"))) return rc;
   }
-  if (rc) return rc;
+  if ((rc = make_tmap(&tA1, a.xs, (uint64_t)S, (uint64_t)a.H, BM))) return rc;
   if ((rc = make_tmap(&tB1, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, 128))) return rc;
   if ((rc = make_tmap(&tA2, a.act, (uint64_t)S, (uint64_t)a.I, BM))) return rc;
   if ((rc = make_tmap(&tB2, a.w2, (uint64_t)a.E * a.H, (uint64_t)a.I, 128))) return rc;
 
   TcParams p1{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.H, a.I,
               (a.I + 127) / 128, 2 * a.I, a.act, a.status};
-  rc = gather ? launch_tc<MODE_FC1, true>(tA1, tB1, p1, S, s, "ffn_fc1_tc")
-              : launch_tc<MODE_FC1, false>(tA1, tB1, p1, S, s, "ffn_fc1_tc");
-  if (rc) return rc;
+  if ((rc = launch_tc<MODE_FC1>(tA1, tB1, p1, S, s, "ffn_fc1_tc"))) return rc;
   TcParams p2{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H,
               (a.H + BN - 1) / BN, a.H, a.staging, a.status};
-  rc = launch_tc<MODE_FC2, false>(tA2, tB2, p2, S, s, "ffn_fc2_tc");
-  if (rc) return rc;
+  if ((rc = launch_tc<MODE_FC2>(tA2, tB2, p2, S, s, "ffn_fc2_tc"))) return rc;
   return launch_combine(a.staging, a.T, a.k, a.H, a.dtype, a.out, s);
 }
 

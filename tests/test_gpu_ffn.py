@@ -63,6 +63,17 @@ def test_layer_tensor_core_shapes(T, H, I, E, k, norm):
                                        logits="distinct", seed=T + H))
 
 
+# decode (weight-streaming, T <= 64) kernels at every token-chunk width and around the threshold
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 256, 128, 8, 2), (3, 128, 192, 16, 4), (16, 256, 256, 64, 8), (17, 128, 384, 32, 8),
+    (33, 192, 320, 64, 8), (64, 256, 128, 8, 2), (64, 128, 256, 64, 8), (65, 128, 256, 64, 8),
+])
+def test_layer_decode_shapes(T, H, I, E, k):
+    moe = need_gpu()
+    _full_check(moe, make_layer_inputs(T=T, H=H, I=I, E=E, k=k, norm_topk_prob=True, dtype="bf16",
+                                       logits="distinct", seed=T * 7))
+
+
 # CUDA-core path: float32, and bf16 shapes the tensor path does not take
 @pytest.mark.parametrize("T,H,I,E,k,dtype", [
     (64, 128, 256, 8, 2, "f32"),
