@@ -138,6 +138,31 @@ MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, in
                                 size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * Align by expert without a workspace. The source pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory when
+ * they call in (host code handed tensors by a framework whose allocator it
+ * cannot reach, or a runtime whose device memory is fixed at start-up), so
+ * they cannot supply `ws`. Same arguments and results as moe_align_by_expert,
+ * minus the workspace; it allocates nothing.
+ *   - Its scratch is a fixed device array inside the library of
+ *     MOE_ALIGN_NOALLOC_SCRATCH_INTS int32 (256 KiB), present on every GPU that
+ *     loads the library until the process exits. Sizes needing more,
+ *     ceil(T*k / 4096) * E > MOE_ALIGN_NOALLOC_SCRATCH_INTS, are rejected with
+ *     MOE_ERR_UNSUPPORTED and a message from moe_last_error(); nothing is
+ *     launched. (E = 128 allows T*k up to 2,097,152; E = 1024 up to 262,144.)
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the array: calls whose work overlaps on the GPU (other
+ *     streams, other host threads) race and must be serialised by the caller.
+ */
+#define MOE_ALIGN_NOALLOC_SCRATCH_INTS 65536
+MOE_API int moe_align_by_expert_noalloc(const int32_t* indices, const float* weights, int T, int k,
+                                        int E, int32_t* counts, int32_t* offsets,
+                                        int32_t* sorted_token_ids, float* sorted_weights,
+                                        int32_t* reverse_indices, int32_t* status, void* stream);
+
+/*
  * Grouped expert FFN and weighted combine.  [p6] moe_prefill_experts /
  * moe_decode_experts; [mlc] scatter_output, moe_sum.
  *   hidden  [T, H]      dtype.

@@ -21,6 +21,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPAC
 MOE_F32, MOE_BF16 = 0, 1
 MOE_STATUS_BAD_INDEX, MOE_STATUS_TIMEOUT = 1, 2
 MOE_MAX_TOPK, MOE_MAX_EXPERTS = 32, 1024
+MOE_ALIGN_NOALLOC_SCRATCH_INTS = 65536
 
 _p, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 
@@ -31,6 +32,7 @@ SIGNATURES = {
     "moe_multihot_to_indices": (_i, [_p, _p, _i, _i, _i, _p, _p, _p]),
     "moe_align_workspace_size": (_sz, [_i, _i, _i]),
     "moe_align_by_expert": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _sz, _p, _p]),
+    "moe_align_by_expert_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p]),
     "moe_grouped_ffn_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_grouped_ffn": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p, _p]),
     "moe_layer_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
@@ -186,6 +188,34 @@ def moe_align_by_expert(indices, weights, num_experts, out=None, workspace=None,
         _ptr(indices), _ptr(weights), T, k, E, _ptr(counts), _ptr(offsets), _ptr(ids), _ptr(sw),
         _ptr(rev), _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream, d)))
+    return dict(counts=counts, offsets=offsets, sorted_token_ids=ids, sorted_weights=sw,
+                reverse_indices=rev)
+
+
+def moe_align_by_expert_noalloc(indices, weights, num_experts, out=None, status=None, stream=None):
+    """Align by expert for callers that cannot allocate device memory at call time.
+
+    Same results as :func:`moe_align_by_expert`; the library keeps the scratch in
+    a fixed device array of its own (limit: ceil(T*k / 4096) * E <=
+    MOE_ALIGN_NOALLOC_SCRATCH_INTS), so no workspace is passed. Calls that
+    overlap on the GPU share that array and race. Output tensors are created
+    here only when ``out`` does not supply them.
+    """
+    _dev(indices, "indices", torch.int32)
+    _dev(weights, "weights", torch.float32)
+    T, k = indices.shape
+    E = int(num_experts)
+    S = T * k
+    d = indices.device
+    out = dict(out or {})
+    counts = _out(out.get("counts"), (E,), torch.int32, d, "counts")
+    offsets = _out(out.get("offsets"), (E + 1,), torch.int32, d, "offsets")
+    ids = _out(out.get("sorted_token_ids"), (S,), torch.int32, d, "sorted_token_ids")
+    sw = _out(out.get("sorted_weights"), (S,), torch.float32, d, "sorted_weights")
+    rev = _out(out.get("reverse_indices"), (S,), torch.int32, d, "reverse_indices")
+    _check("moe_align_by_expert_noalloc", lib().moe_align_by_expert_noalloc(
+        _ptr(indices), _ptr(weights), T, k, E, _ptr(counts), _ptr(offsets), _ptr(ids), _ptr(sw),
+        _ptr(rev), _ptr(status), _stream(stream, d)))
     return dict(counts=counts, offsets=offsets, sorted_token_ids=ids, sorted_weights=sw,
                 reverse_indices=rev)
 

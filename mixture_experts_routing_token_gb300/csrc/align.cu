@@ -18,6 +18,8 @@
 //      warp by __match_any_sync + popc of lower lanes, across warps by a
 //      per-expert prefix over the warps' counts. A single-chunk problem runs
 //      as one launch (the CTA makes its own histogram).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -182,6 +184,57 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
   align_scatter_kernel<<<nchunks > 0 ? nchunks : 1, kThreads, smem, s>>>(
       idx, w, S, k, E, nchunks, hist, counts, offsets, sorted_ids, sorted_w, reverse, status);
   return check_launch("align_scatter");
+}
+
+// ---- fixed scratch for callers that cannot allocate --------------------------
+//
+// Some callers cannot obtain device memory at call time: host code that only
+// receives tensors from a framework without access to its allocator, or a
+// runtime whose device memory is planned once at start-up and may not grow.
+// They cannot pass a workspace, so moe_align_by_expert_noalloc keeps the
+// per-chunk histograms in this file-scope array instead. Every GPU that loads
+// the library holds it (MOE_ALIGN_NOALLOC_SCRATCH_INTS int32 = 256 KiB) until
+// the process exits. All calls share it: calls whose work overlaps on the GPU
+// (different streams, or different host threads) race on it. The histograms
+// are fully rewritten before they are read, so nothing needs clearing.
+static __device__ __align__(256) int32_t g_align_scratch[MOE_ALIGN_NOALLOC_SCRATCH_INTS];
+
+// Device address of g_align_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress, once per device with that device current, on the first
+// call that needs it (that first call should come before any stream capture).
+static int align_scratch_address(int32_t** out) {
+  static std::mutex mu;
+  static int32_t* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d above 63", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_align_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(align scratch): %s", cudaGetErrorString(e));
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = addr[dev];
+  return MOE_OK;
+}
+
+int launch_align_noalloc(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
+                         int32_t* status, cudaStream_t s) {
+  const size_t need = align_scratch_bytes(T * k, E);
+  if (need > sizeof(g_align_scratch))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "align without workspace: T*k=%ld with E=%d needs %zu bytes of scratch, above the "
+                "fixed %zu (ceil(T*k/4096)*E must not exceed %d)",
+                (long)T * k, E, need, sizeof(g_align_scratch), MOE_ALIGN_NOALLOC_SCRATCH_INTS);
+  int32_t* scratch = nullptr;
+  int rc = align_scratch_address(&scratch);
+  if (rc) return rc;
+  return launch_align(idx, w, T, k, E, counts, offsets, sorted_ids, sorted_w, reverse, scratch, status, s);
 }
 
 }  // namespace moe

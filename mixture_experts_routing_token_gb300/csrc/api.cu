@@ -253,6 +253,26 @@ MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, in
                       reverse_indices, ws, status, (cudaStream_t)stream);
 }
 
+MOE_API int moe_align_by_expert_noalloc(const int32_t* indices, const float* weights, int T, int k,
+                                        int E, int32_t* counts, int32_t* offsets,
+                                        int32_t* sorted_token_ids, float* sorted_weights,
+                                        int32_t* reverse_indices, int32_t* status, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  const long S = (long)T * k;
+  if ((rc = check_tensor(indices, S, "indices"))) return rc;
+  if ((rc = check_tensor(weights, S, "weights"))) return rc;
+  if ((rc = check_tensor(counts, E, "counts"))) return rc;
+  if ((rc = check_tensor(offsets, E + 1, "offsets"))) return rc;
+  if ((rc = check_tensor(sorted_token_ids, S, "sorted_token_ids"))) return rc;
+  if ((rc = check_tensor(sorted_weights, S, "sorted_weights"))) return rc;
+  if ((rc = check_tensor(reverse_indices, S, "reverse_indices"))) return rc;
+  if (status && (rc = check_tensor(status, 1, "status"))) return rc;
+  return launch_align_noalloc(indices, weights, T, k, E, counts, offsets, sorted_token_ids,
+                              sorted_weights, reverse_indices, status, (cudaStream_t)stream);
+}
+
 MOE_API size_t moe_grouped_ffn_workspace_size(int dtype, int T, int H, int I, int E, int k) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
   Carver c(nullptr);

@@ -55,6 +55,9 @@ int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E
                                float* probs, int32_t* idx, cudaStream_t s);
 
 size_t align_scratch_bytes(int S, int E);
+int launch_align_noalloc(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
+                         int32_t* status, cudaStream_t s);
 int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
                  int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
                  void* scratch, int32_t* status, cudaStream_t s);
