@@ -26,7 +26,9 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["topk", "softmax_topk"]
+__all__ = ["topk", "softmax_topk", "group_limited_topk", "FLOAT32_LOWEST"]
+
+FLOAT32_LOWEST = np.float32(np.finfo(np.float32).min)
 
 
 def topk(scores: np.ndarray, k: int):
@@ -58,3 +60,57 @@ def softmax_topk(logits: np.ndarray, k: int, norm_topk_prob: bool = True):
         prob = ex / ex.sum(axis=1, keepdims=True)
         w = np.take_along_axis(prob, idx, axis=1)
     return w.astype(np.float32), idx
+
+
+def group_limited_topk(scores: np.ndarray, k: int, n_group: int, topk_group: int,
+                       method: str = "group_limited_greedy", bias: np.ndarray | None = None):
+    """``group_limited_greedy_topk`` (mlc-llm ``moe_misc.py``): (weights [T,k] f32, indices [T,k] i32).
+
+    Steps, as the page takes them (all on float32 tensors, the page asserts
+    float32 scores):
+
+    1. scores for choice: the scores, plus ``bias`` for ``noaux_tc``;
+    2. experts are cut into ``n_group`` groups of ``E / n_group`` consecutive
+       experts; a group's score is its largest choice score
+       (``group_limited_greedy``) or the sum of its two largest (``noaux_tc``);
+    3. the ``topk_group`` best groups are kept (top-k rule: descending, ties to
+       the lower group index);
+    4. choice scores outside the kept groups become the lowest float32 value;
+    5. top-k of the result; the weights are those values (``group_limited_greedy``)
+       or the un-biased scores of the chosen experts (``noaux_tc``).
+
+    Needs ``k <= topk_group * E / n_group`` so that only kept experts are chosen,
+    and, for ``noaux_tc``, at least two experts per group (the page takes a
+    top-2 inside each group).
+    """
+    s32 = np.asarray(scores, dtype=np.float32)
+    T, E = s32.shape
+    if E % n_group or not 1 <= topk_group <= n_group or not 1 <= k <= topk_group * (E // n_group):
+        raise ValueError("need E % n_group == 0, 1 <= topk_group <= n_group, 1 <= k <= topk_group*E/n_group")
+    if method not in ("group_limited_greedy", "noaux_tc"):
+        raise ValueError(f"unknown method {method!r}")
+    choice = s32
+    if method == "noaux_tc":
+        if bias is None:
+            raise ValueError("noaux_tc needs a bias")
+        choice = (s32 + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    gs = E // n_group
+    if method == "noaux_tc" and gs < 2:
+        raise ValueError("noaux_tc needs at least two experts per group")
+    grouped = choice.reshape(T * n_group, gs)
+    if method == "noaux_tc":
+        top2 = topk(grouped, 2)[0].astype(np.float32)
+        gscore = top2[:, 0] + top2[:, 1]                                    # float32 sum of the two
+    else:
+        gscore = grouped.max(axis=1)
+    gscore = np.asarray(gscore, dtype=np.float32).reshape(T, n_group)
+    gidx = topk(gscore, topk_group)[1]
+    masked = np.full((T, E), FLOAT32_LOWEST, dtype=np.float32)
+    for j in range(topk_group):
+        for c in range(gs):
+            col = gidx[:, j].astype(np.int64) * gs + c
+            masked[np.arange(T), col] = choice[np.arange(T), col]
+    vals, idx = topk(masked, k)
+    if method == "noaux_tc":
+        vals = np.take_along_axis(s32, idx.astype(np.int64), axis=1)
+    return vals.astype(np.float32), idx

@@ -133,3 +133,81 @@ def test_rejects_non_finite_and_bad_k():
         gating.softmax_topk(np.array([[0.0, np.inf]], np.float32), 1)
     with pytest.raises(ValueError):
         gating.topk(np.zeros((2, 3), np.float32), 4)
+
+
+# ---- group-limited greedy / noaux_tc top-k ------------------------------------------
+
+def _page_group_limited(row, k, n_group, topk_group, method, bias):
+    """The page's steps for one row, written with the insertion top-k above."""
+    row = [np.float32(v) for v in row]
+    choice = row if method != "noaux_tc" else [np.float32(a + np.float32(b)) for a, b in zip(row, bias)]
+    gs = len(row) // n_group
+    gscore = []
+    for g in range(n_group):
+        grp = choice[g * gs:(g + 1) * gs]
+        if method == "noaux_tc":
+            v, _ = insertion_topk(grp, 2)
+            gscore.append(np.float32(v[0] + v[1]))
+        else:
+            gscore.append(max(grp))
+    _, gsel = insertion_topk(gscore, topk_group)
+    masked = [FLT_MIN_VALUE] * len(row)
+    for g in gsel:
+        for c in range(gs):
+            masked[g * gs + c] = choice[g * gs + c]
+    v, i = insertion_topk(masked, k)
+    if method == "noaux_tc":
+        v = [row[e] for e in i]
+    return [float(x) for x in v], i
+
+
+def test_group_limited_golden(gold):
+    g = gold("group_limited_topk")
+    x = np.array(g["scores"], np.float32)
+    w, i = gating.group_limited_topk(x, g["k"], g["n_group"], g["topk_group"], "group_limited_greedy")
+    assert i.tolist() == g["greedy_indices"]
+    np.testing.assert_array_equal(w, np.array(g["greedy_weights"], np.float32))
+    w, i = gating.group_limited_topk(x, g["k"], g["n_group"], g["topk_group"], "noaux_tc", np.zeros(8, np.float32))
+    assert i.tolist() == g["noaux_zero_bias_indices"]
+    np.testing.assert_array_equal(w, np.array(g["noaux_zero_bias_weights"], np.float32))
+    w, i = gating.group_limited_topk(x, g["k"], g["n_group"], g["topk_group"], "noaux_tc",
+                                     np.array(g["bias"], np.float32))
+    assert i.tolist() == g["noaux_bias_indices"]
+    np.testing.assert_array_equal(w, np.array(g["noaux_bias_weights"], np.float32))
+
+
+@pytest.mark.parametrize("method", ["group_limited_greedy", "noaux_tc"])
+@pytest.mark.parametrize("E,n_group,topk_group,k", [(8, 4, 2, 2), (12, 3, 2, 5), (16, 8, 3, 4), (12, 6, 6, 3)])
+def test_group_limited_matches_page_steps(method, E, n_group, topk_group, k):
+    rng = np.random.default_rng(E * 31 + k)
+    x = (rng.integers(0, 5, size=(40, E)) * 0.25).astype(np.float32)   # coarse: many ties
+    bias = (rng.integers(-2, 3, size=E) * 0.125).astype(np.float32)
+    w, i = gating.group_limited_topk(x, k, n_group, topk_group, method, bias)
+    for r in range(x.shape[0]):
+        pw, pi = _page_group_limited(x[r].tolist(), k, n_group, topk_group, method, bias.tolist())
+        assert i[r].tolist() == pi
+        assert w[r].tolist() == [float(np.float32(v)) for v in pw]
+
+
+@pytest.mark.parametrize("method", ["group_limited_greedy", "noaux_tc"])
+def test_group_limited_reduces_to_plain_topk(method):
+    x = gen_logits(np.random.SeedSequence(9), 100, 32, "distinct")
+    z = np.zeros(32, np.float32)
+    for n_group, topk_group in [(1, 1), (4, 4), (16, 16)]:
+        w, i = gating.group_limited_topk(x, 6, n_group, topk_group, method, z)
+        v, j = gating.topk(x, 6)
+        np.testing.assert_array_equal(i, j)
+        np.testing.assert_array_equal(w, v)
+
+
+def test_group_limited_choice_stays_in_kept_groups():
+    x = gen_logits(np.random.SeedSequence(2), 300, 256, "distinct")
+    bias = gen_logits(np.random.SeedSequence(3), 1, 256, "distinct")[0] * np.float32(0.1)
+    w, i = gating.group_limited_topk(x, 8, 8, 4, "noaux_tc", bias)
+    groups = i // 32
+    assert all(len(set(r)) <= 4 for r in groups.tolist())
+    np.testing.assert_array_equal(w, np.take_along_axis(x, i.astype(np.int64), 1))
+    with pytest.raises(ValueError):
+        gating.group_limited_topk(x, 200, 8, 4, "noaux_tc", bias)
+    with pytest.raises(ValueError):
+        gating.group_limited_topk(x, 4, 256, 4, "noaux_tc", bias)      # one expert per group
