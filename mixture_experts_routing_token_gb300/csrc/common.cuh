@@ -85,6 +85,10 @@ int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 // Token-count threshold at or below which the weight-streaming decode kernels run.
 constexpr int kDecodeMaxTokens = 64;
 int launch_ffn_decode(const FfnArgs& a, cudaStream_t s);
+// FC1 and FC2 on 2-SM clusters (tcgen05 cta_group::2), given the four tensor
+// maps (A: 128-row boxes of x_sorted / act; B: 128-row boxes of w13 / w2).
+int launch_ffn_pair_gemms(const FfnArgs& a, const CUtensorMap& tA1, const CUtensorMap& tB1,
+                          const CUtensorMap& tA2, const CUtensorMap& tB2, cudaStream_t s);
 
 bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);

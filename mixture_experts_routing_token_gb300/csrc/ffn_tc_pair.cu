@@ -1,0 +1,378 @@
+// Grouped expert FFN on SM pairs: tcgen05.mma.cta_group::2, M = 256 (128 rows
+// per SM) x N = 256 x K = 16, accumulators in both SMs' TMEM.
+//
+// Same semantics and tile list as the single-SM kernel in ffn_tc.cu
+// (project_6 moe_expert_gemm.cpp moe_prefill_experts: FC1, silu_and_mul,
+// FC2, routing weight; mlc-llm moe_misc.py scatter_output), with tiles of
+// 256 sorted rows per expert. Each SM of a 2-CTA cluster loads its own 128
+// rows of A and ONE HALF of the 256 B rows:
+//   FC1: CTA 0 the 128 gate rows n0.., CTA 1 the 128 matching up rows I+n0..;
+//   FC2: CTA 0 rows n0..n0+127 of w2[e], CTA 1 rows n0+128..n0+255.
+// The pair's MMA then leaves, in each SM's TMEM, its 128 rows x all 256
+// columns (FC1: gate columns 0..127, up columns 128..255), so the epilogues
+// are the single-SM ones. Per SM and k-step this moves 32 KB instead of 48 KB
+// for the same tensor work, which is what lets a 6-stage ring hide the
+// L2 -> shared-memory latency.
+//
+// Synchronisation:
+//   full[s]   leader CTA only; the leader's producer posts the pair's bytes
+//             (2 x 32 KB) and both CTAs' TMA loads complete on it
+//             (.cta_group::2 form, barrier addressed in the leader's window);
+//   empty[s]  in both CTAs; the leader's MMA commit multicasts to both;
+//   tfull[b]  in both CTAs; multicast commit after a tile's last k-step;
+//   tempty[b] leader only; one arrival per epilogue warp of both CTAs (8).
+// Waits are bounded as in the single-SM kernel; a cluster barrier brackets
+// the kernel so neither CTA leaves while the other may still touch its
+// shared memory.
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int PBM = 128;                // rows per CTA (256 per pair)
+constexpr int PBK = 64;
+constexpr int PBN = 256;                // MMA N
+constexpr int PSTAGES = 6;
+constexpr int PA_BYTES = PBM * PBK * 2;       // 16 KB
+constexpr int PB_BYTES = (PBN / 2) * PBK * 2; // 16 KB: this CTA's half of B
+constexpr int PSTAGE = PA_BYTES + PB_BYTES;
+constexpr int PDSMEM = PSTAGES * PSTAGE + 1024;
+constexpr int PTHREADS = 192;
+constexpr uint32_t PTMEM_COLS = 2 * PBN;
+constexpr uint64_t PWAIT_NS = 2000000000ull;
+constexpr uint32_t PIDESC = ptx::idesc_bf16_f32(2 * PBM, PBN);
+
+enum { PAIR_FC1 = 0, PAIR_FC2 = 1 };
+
+struct PairParams {
+  const int32_t* counts;
+  const int32_t* offsets;
+  const float* sorted_w;
+  const int32_t* reverse;
+  int E;
+  int K;          // H (FC1) or I (FC2)
+  int N_out;      // I (FC1) or H (FC2)
+  int NT;         // N tiles per expert
+  int b_rows;     // 2I (FC1) or H (FC2)
+  void* out;
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// shared::cta address -> shared::cluster address of the same variable in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                                 uint32_t leader_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(leader_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at `bar` (same offset) in every CTA of `mask`
+// when all previously issued pair MMAs of this thread complete.
+__device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+struct PTile {
+  int e, m_tile, n_tile;
+};
+
+__device__ __forceinline__ PTile ptile(int t, const int* tile_start, int E, int NT) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int local = t - tile_start[lo];
+  const int mt = (tile_start[lo + 1] - tile_start[lo]) / NT;
+  PTile d;
+  d.e = lo;
+  d.n_tile = local / mt;
+  d.m_tile = local - d.n_tile * mt;
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
+    ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const PairParams P) {
+  __shared__ __align__(8) uint64_t full_bar[PSTAGES], empty_bar[PSTAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int tile_start[MOE_MAX_EXPERTS + 1];
+  extern __shared__ uint8_t dsmem_raw[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const uint32_t dsmem = (ptx::smem_u32(dsmem_raw) + 1023u) & ~1023u;
+  auto sA = [&](int s) { return dsmem + (uint32_t)(s * PSTAGE); };
+  auto sB = [&](int s) { return dsmem + (uint32_t)(s * PSTAGE + PA_BYTES); };
+  volatile int* abort_p = &abort_flag;
+
+  if (tid == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
+      ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 8);
+    }
+    ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {   // both CTAs of the pair allocate together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     ptx::smem_u32(&tmem_slot)),
+                 "r"(PTMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  if (warp == 2) {   // tile_start[e] = sum over e' < e of ceil(count / 256) * NT
+    const int per = (P.E + 31) / 32;
+    const int e0 = min(P.E, lane * per), e1 = min(P.E, e0 + per);
+    int run = 0;
+    for (int e = e0; e < e1; ++e) run += (__ldg(P.counts + e) + 2 * PBM - 1) / (2 * PBM) * P.NT;
+    int incl = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int acc = incl - run;
+    for (int e = e0; e < e1; ++e) {
+      tile_start[e] = acc;
+      acc += (__ldg(P.counts + e) + 2 * PBM - 1) / (2 * PBM) * P.NT;
+    }
+    if (lane == 31) tile_start[P.E] = incl;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  cluster_sync();      // barriers of both CTAs initialised before any cross-CTA signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  const int total = tile_start[P.E];
+  const int KB = P.K / PBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int t = cluster_id; t < total; t += nclusters) {
+        const PTile ti = ptile(t, tile_start, P.E, P.NT);
+        const int a_row = __ldg(P.offsets + ti.e) + ti.m_tile * (2 * PBM) + (int)rank * PBM;
+        int b_row;
+        if (MODE == PAIR_FC1) b_row = ti.e * P.b_rows + ti.n_tile * 128 + (leader ? 0 : P.N_out);
+        else b_row = ti.e * P.b_rows + ti.n_tile * PBN + (int)rank * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, PWAIT_NS)) goto producer_done;
+          const uint32_t fb_local = ptx::smem_u32(&full_bar[stage]);
+          if (leader) ptx::mbar_arrive_expect_tx(fb_local, 2 * PSTAGE);
+          const uint32_t fb = map_to_rank(fb_local, 0);
+          tma_load_2d_pair(sA(stage), &tmA, kb * PBK, a_row, fb);
+          tma_load_2d_pair(sB(stage), &tmB, kb * PBK, b_row, fb);
+          if (++stage == PSTAGES) { stage = 0; ph ^= 1u; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (leader && lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int t = cluster_id; t < total; t += nclusters) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aph ^ 1u, abort_p, PWAIT_NS)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, PWAIT_NS)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = sA(stage), b0 = sB(stage);
+#pragma unroll
+          for (int kk = 0; kk < PBK / 16; ++kk)
+            mma_pair(d_tmem, ptx::sdesc_k128(a0 + kk * 32), ptx::sdesc_k128(b0 + kk * 32), PIDESC,
+                     (kb | kk) != 0);
+          commit_pair(ptx::smem_u32(&empty_bar[stage]), 0x3);
+          if (++stage == PSTAGES) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        commit_pair(ptx::smem_u32(&tfull_bar[acc]), 0x3);
+        if (++acc == 2) { acc = 0; aph ^= 1u; }
+      }
+      commit_pair(ptx::smem_u32(&drain_bar), 0x1);
+      int dummy = 0;
+      ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, &dummy, PWAIT_NS);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = cluster_id; t < total; t += nclusters) {
+      const PTile ti = ptile(t, tile_start, P.E, P.NT);
+      if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, PWAIT_NS)) break;
+      ptx::tc_fence_after();
+      const int cnt = __ldg(P.counts + ti.e);
+      const int r = ti.m_tile * (2 * PBM) + (int)rank * PBM + row;
+      const bool valid = r < cnt;
+      const long p = (long)__ldg(P.offsets + ti.e) + r;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PBN);
+      if (MODE == PAIR_FC1) {
+        const int I = P.N_out;
+        __nv_bfloat16* act = static_cast<__nv_bfloat16*>(P.out);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld32(taddr + c * 32, g);
+          ptx::tmem_ld32(taddr + 128 + c * 32, u);
+          ptx::tmem_ld_wait();
+          const int col0 = ti.n_tile * 128 + c * 32;
+          if (valid && col0 < I) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+              const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+              pk[i] = pack2(a0, a1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(act + p * I + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      } else {
+        const int H = P.N_out;
+        float* staging = static_cast<float*>(P.out);
+        const float wt = valid ? __ldg(P.sorted_w + p) : 0.0f;
+        const long dst_row = valid ? (long)__ldg(P.reverse + p) : 0;
+#pragma unroll 1
+        for (int c = 0; c < PBN / 32; ++c) {
+          uint32_t y[32];
+          ptx::tmem_ld32(taddr + c * 32, y);
+          ptx::tmem_ld_wait();
+          const int col0 = ti.n_tile * PBN + c * 32;
+          if (valid && col0 < H) {
+            float4* dst = reinterpret_cast<float4*>(staging + dst_row * H + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(y[4 * i]) * wt, __uint_as_float(y[4 * i + 1]) * wt,
+                                   __uint_as_float(y[4 * i + 2]) * wt, __uint_as_float(y[4 * i + 3]) * wt);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_remote(map_to_rank(ptx::smem_u32(&tempty_bar[acc]), 0));
+      if (++acc == 2) { acc = 0; aph ^= 1u; }
+    }
+  }
+
+  // Teardown. After a timeout, give copies that may still be in flight time
+  // to land before the shared memory is released.
+  if (*abort_p) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 1000000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(PTMEM_COLS)
+                 : "memory");
+  }
+  if (tid == 0 && abort_flag && P.status) atomicOr(P.status, MOE_STATUS_TIMEOUT);
+}
+
+template <int MODE>
+int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const PairParams& p, long S, cudaStream_t s,
+                const char* name) {
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    if (cudaFuncSetAttribute(ffn_tc_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, PDSMEM) !=
+        cudaSuccess)
+      return check_launch(name);
+    attr[dev] = true;
+  }
+  const long max_tiles = ((S + 2 * PBM - 1) / (2 * PBM) + p.E) * (long)p.NT;
+  const long pairs = num_sms() / 2;
+  const int grid = 2 * (int)(max_tiles < pairs ? max_tiles : pairs);
+  if (grid <= 0) return MOE_OK;
+  ProfScope ps(name, s);
+  ffn_tc_pair_kernel<MODE><<<grid, PTHREADS, PDSMEM, s>>>(a, b, p);
+  return check_launch(name);
+}
+
+}  // namespace
+
+int launch_ffn_pair_gemms(const FfnArgs& a, const CUtensorMap& tA1, const CUtensorMap& tB1,
+                          const CUtensorMap& tA2, const CUtensorMap& tB2, cudaStream_t s) {
+  const long S = (long)a.T * a.k;
+  PairParams p1{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.H, a.I, (a.I + 127) / 128,
+                2 * a.I, a.act, a.status};
+  int rc = launch_pair<PAIR_FC1>(tA1, tB1, p1, S, s, "ffn_fc1_tc");
+  if (rc) return rc;
+  PairParams p2{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.I, a.H, (a.H + PBN - 1) / PBN,
+                a.H, a.staging, a.status};
+  return launch_pair<PAIR_FC2>(tA2, tB2, p2, S, s, "ffn_fc2_tc");
+}
+
+}  // namespace moe
