@@ -39,6 +39,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-routing", action="store_true", help="skip the large-T routing bandwidth section")
+    ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                    help="time the step as a CUDA graph replay (auto: on for decode batches, T <= 64)")
     return ap.parse_args()
 
 
@@ -139,6 +142,70 @@ def make_device_inputs(wl, device, seed=0):
         w13[e] = (torch.randn((2 * I, H), generator=g, device=device) / H ** 0.5).to(dt)
         w2[e] = (torch.randn((H, I), generator=g, device=device) / I ** 0.5).to(dt)
     return hidden, logits, w13, w2
+
+
+def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
+    """Each routing kernel on a token count large enough that its inputs and outputs
+    (>= 768 MiB) stream through HBM rather than L2: algorithmic bytes / CUDA-event time.
+
+    Bytes per token (SURVEY-style accounting of what the method must move):
+      gating 4E + 8k; indices->multihot 8k + 9E; multihot->indices 8E + 8k (probs and
+      indices out); align 8k in + 12k out (+ E-sized tables); group-limited top-k
+      (DeepSeek-V3 shape E=256, 8 groups, keep 4, k=8) 4E + 8k.
+    """
+    import torch
+    E, k = wl.E, wl.k
+    per_tok = {"gating_softmax_topk": 4 * E + 8 * k, "indices_to_multihot": 8 * k + 9 * E,
+               "multihot_to_indices": 8 * E + 8 * k, "align_by_expert": 20 * k}
+    T = max(1, int(target_bytes // (8 * E + 8 * k)))
+    T = min(T, (1 << 31) // max(k, 1) - 1)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    logits = torch.randn((T, E), generator=g, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    w, idx = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
+    mh, pm, pos = moe.moe_indices_to_multihot(idx, w, E)
+    p2, i2 = moe.moe_multihot_to_indices(pm, pos, k)
+    ws = torch.empty(max(1, moe.moe_align_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+    al = moe.moe_align_by_expert(idx, w, E, workspace=ws)
+    calls = {
+        "gating_softmax_topk": lambda: moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob, weights=w,
+                                                                   indices=idx, stream=stream),
+        "indices_to_multihot": lambda: moe.moe_indices_to_multihot(idx, w, E, multihot=mh, probs_in_multihot=pm,
+                                                                   position_map=pos, stream=stream),
+        "multihot_to_indices": lambda: moe.moe_multihot_to_indices(pm, pos, k, probs=p2, indices=i2, stream=stream),
+        "align_by_expert": lambda: moe.moe_align_by_expert(idx, w, E, out=al, workspace=ws, stream=stream),
+    }
+    res = {}
+
+    def timed(fn, nbytes):
+        for _ in range(2):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"tokens": T, "us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+
+    for name, fn in calls.items():
+        res[name] = timed(fn, per_tok[name] * T)
+    del logits, mh, pm, pos, p2, i2, al, ws
+    # DeepSeek-V3-shaped group-limited routing on sigmoid scores
+    Eg, kg = 256, 8
+    Tg = int(target_bytes // (4 * Eg + 8 * kg))
+    sc = torch.sigmoid(torch.randn((Tg, Eg), generator=g, device=dev))
+    bias = 0.05 * torch.randn((Eg,), generator=g, device=dev)
+    gw, gi = moe.moe_group_limited_topk(sc, kg, 8, 4, "noaux_tc", bias=bias)
+    res["group_limited_topk"] = timed(
+        lambda: moe.moe_group_limited_topk(sc, kg, 8, 4, "noaux_tc", bias=bias, weights=gw, indices=gi, stream=stream),
+        (4 * Eg + 8 * kg) * Tg)
+    res["group_limited_topk"]["shape"] = "E=256, n_group=8, topk_group=4, k=8, noaux_tc"
+    return res
 
 
 def kernel_traffic(kernel, workload):
@@ -300,24 +367,60 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, device events on the launching stream, per-kernel events
+    use_graph = args.graph == "on" or (args.graph == "auto" and T <= 64)
+    graph = None
+    if use_graph:
+        # one layer step captured once; the timed region replays it (what a decode loop does)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step_side = lambda: moe.moe_layer_forward(hidden, logits, w13, w2, k, wl.norm_topk_prob, out=out,
+                                                      workspace=ws, stream=side)
+            step_side()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+                step_side()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    # per-kernel CUDA-event times: in the timed region itself when stepping eagerly,
+    # from a separate eager pass of the same length when the timed region replays a graph
+    kern = None
+    if use_graph:
+        moe.profiler_enable(True)
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+        moe.profiler_enable(False)
+        kern = moe.profiler_report()
+
+    # ---- timed region: K steps, device events on the launching stream
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
-    moe.profiler_enable(True)
+    if not use_graph:
+        moe.profiler_enable(True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
+    tstream = torch.cuda.current_stream(dev)
+    ev0.record(tstream)
     for _ in range(args.steps):
-        step()
-    ev1.record(stream)
+        if use_graph:
+            graph.replay()
+        else:
+            step()
+    ev1.record(tstream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    moe.profiler_enable(False)
-    kern = moe.profiler_report()
+    if not use_graph:
+        moe.profiler_enable(False)
+        kern = moe.profiler_report()
     clocks = clk.stop()
     ms_total = ev0.elapsed_time(ev1)
     if world > 1:
@@ -391,10 +494,14 @@ def main():
                        "norm_topk_prob": wl.norm_topk_prob, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (weights %.2f GB read per step)" % (
                            (w13.numel() + w2.numel()) * w13.element_size() / 1e9),
-                       "inputs": "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)))"},
+                       "inputs": "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)))",
+                       "timing": ("CUDA graph replay of one layer step; per-kernel times from an eager pass"
+                                  if use_graph else "eager steps; per-kernel CUDA events inside the timed region")},
             "layer_tflops": ffn_flops / (ms / 1e3) / 1e12,
             "roofline": roofline, "kernels": per_kernel, "gpu_launches": launches * args.steps,
             "gpu_launches_per_step": launches, "clocks": clocks, "e2e": e2e, "lib": moe.version()}
+    if not args.no_routing:
+        line["routing"] = routing_bandwidth(moe, wl, dev, peaks)
     if not args.no_cpu_baseline:
         try:
             line["cpu_baseline"] = cpu_baseline(wl, hidden, logits, w13, w2)

@@ -91,6 +91,27 @@ MOE_API int moe_gating_softmax_topk(const float* logits, int T, int E, int k, in
                                     float* weights, int32_t* indices, void* stream);
 
 /*
+ * Group-limited top-k (DeepSeek-style routing).  [mlc] group_limited_greedy_topk.
+ *   scores   [T, E] float32 (finite), E = n_group * group_size.
+ *   bias     [E] float32, the score correction added for the choice (method
+ *            MOE_GROUP_TOPK_NOAUX_TC; may be NULL for MOE_GROUP_TOPK_GREEDY).
+ *   weights  [T, k] float32 out, indices [T, k] int32 out.
+ * Steps: choice = scores (+ bias); group score = largest choice value of the
+ * group (GREEDY) or the float32 sum of its two largest (NOAUX_TC); the
+ * topk_group best groups are kept (ties to the lower group); experts of the
+ * other groups are excluded; the k largest remaining choice values are taken
+ * (ties to the lower expert). weights = the choice values (GREEDY) or the
+ * un-biased scores of the chosen experts (NOAUX_TC).
+ * Limits: 1 <= n_group <= 32, E % n_group == 0, 1 <= topk_group <= n_group,
+ * 1 <= k <= min(32, topk_group * E / n_group); NOAUX_TC needs E / n_group >= 2.
+ */
+#define MOE_GROUP_TOPK_GREEDY 0
+#define MOE_GROUP_TOPK_NOAUX_TC 1
+MOE_API int moe_group_limited_topk(const float* scores, const float* bias, int T, int E, int k,
+                                   int n_group, int topk_group, int method, float* weights,
+                                   int32_t* indices, void* stream);
+
+/*
  * Indices -> multihot routing map.  [mgt] _indices_to_multihot_kernel.
  *   indices            [T, k] int32; an entry outside [0, E) (e.g. -1) is not routed.
  *   probs              [T, k] float32.

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 0, 1, 2, 3, 4
 MOE_F32, MOE_BF16 = 0, 1
 MOE_STATUS_BAD_INDEX, MOE_STATUS_TIMEOUT = 1, 2
+MOE_GROUP_TOPK_GREEDY, MOE_GROUP_TOPK_NOAUX_TC = 0, 1
 MOE_MAX_TOPK, MOE_MAX_EXPERTS = 32, 1024
 MOE_ALIGN_NOALLOC_SCRATCH_INTS = 65536
 
@@ -28,6 +29,7 @@ _p, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 # name -> (restype, argtypes); mirrors include/moe.h
 SIGNATURES = {
     "moe_gating_softmax_topk": (_i, [_p, _i, _i, _i, _i, _p, _p, _p]),
+    "moe_group_limited_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p]),
     "moe_indices_to_multihot": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p]),
     "moe_multihot_to_indices": (_i, [_p, _p, _i, _i, _i, _p, _p, _p]),
     "moe_align_workspace_size": (_sz, [_i, _i, _i]),
@@ -126,6 +128,24 @@ def moe_gating_softmax_topk(logits, k, norm_topk_prob=True, weights=None, indice
     _check("moe_gating_softmax_topk", lib().moe_gating_softmax_topk(
         _ptr(logits), T, E, k, int(bool(norm_topk_prob)), _ptr(weights), _ptr(indices),
         _stream(stream, logits.device)))
+    return weights, indices
+
+
+def moe_group_limited_topk(scores, k, n_group, topk_group, method="group_limited_greedy", bias=None,
+                           weights=None, indices=None, stream=None):
+    """Group-limited top-k of ``scores [T,E]`` f32 -> (weights [T,k] f32, indices [T,k] i32).
+
+    ``method`` is "group_limited_greedy" or "noaux_tc" (needs ``bias [E]`` f32)."""
+    _dev(scores, "scores", torch.float32)
+    T, E = scores.shape
+    code = {"group_limited_greedy": MOE_GROUP_TOPK_GREEDY, "noaux_tc": MOE_GROUP_TOPK_NOAUX_TC}[method]
+    if bias is not None:
+        _dev(bias, "bias", torch.float32)
+    weights = _out(weights, (T, k), torch.float32, scores.device, "weights")
+    indices = _out(indices, (T, k), torch.int32, scores.device, "indices")
+    _check("moe_group_limited_topk", lib().moe_group_limited_topk(
+        _ptr(scores), _ptr(bias), T, E, k, n_group, topk_group, code, _ptr(weights), _ptr(indices),
+        _stream(stream, scores.device)))
     return weights, indices
 
 

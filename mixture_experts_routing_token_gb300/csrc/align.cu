@@ -10,24 +10,30 @@
 // experts, "tokens t' < t routed to e" equals "flat slots s' < s holding e",
 // so the sorted position of flat slot s = t*k + j is
 //     offsets[e] + #{s' < s : idx[s'] == e}.
-// Two launches:
+// Launches:
 //   1. align_hist: each CTA counts its chunk of slots per expert (shared-memory
 //      atomics; the counts are order-free) into chunk_hist[c][e];
-//   2. align_scatter: each CTA derives offsets and its chunk's per-expert base
-//      from chunk_hist, then ranks its slots in order, 512 at a time: within a
-//      warp by __match_any_sync + popc of lower lanes, across warps by a
-//      per-expert prefix over the warps' counts. A single-chunk problem runs
-//      as one launch (the CTA makes its own histogram).
+//   2. (many chunks only) align_scan: one CTA per expert turns its column of
+//      chunk_hist into an inclusive prefix over chunks, in place;
+//   3. align_scatter: each CTA derives offsets and its chunk's per-expert base
+//      from chunk_hist (summing the few chunks before it, or reading the
+//      prefix), then ranks its slots in order, 512 at a time: within a warp by
+//      __match_any_sync + popc of lower lanes, across warps by a per-expert
+//      prefix over the warps' counts.
+// A single-chunk problem runs as one launch (the CTA makes its own histogram).
 #include <mutex>
 
 #include "common.cuh"
+#include "gating_device.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 4096;   // slots per CTA
+constexpr int kSpt = 4;        // slots per thread per ranking round
+constexpr int kChunk = 4096;   // slots per CTA (a multiple of kThreads * kSpt)
+constexpr int kScanAbove = 16; // chunks above which the per-expert prefix gets its own launch
 
 __device__ __forceinline__ int valid_expert(int e, int E) { return (e >= 0 && e < E) ? e : -1; }
 
@@ -51,23 +57,70 @@ __global__ void __launch_bounds__(kThreads) align_hist_kernel(const int32_t* __r
   for (int e = threadIdx.x; e < E; e += kThreads) chunk_hist[(long)blockIdx.x * E + e] = hist[e];
 }
 
+// In place: chunk_hist[c][e] <- sum over c' <= c of chunk_hist[c'][e]; one CTA per expert,
+// each thread a contiguous run of chunks, block scan of the run totals.
+__global__ void __launch_bounds__(1024) align_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E) {
+  __shared__ int wsum[32];
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (nchunks + 1023) / 1024;
+  const int c0 = min(nchunks, tid * per), c1 = min(nchunks, c0 + per);
+  int run = 0;
+  for (int c = c0; c < c1; ++c) run += chunk_hist[(long)c * E + e];
+  int incl = run;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v += o;
+    }
+    wsum[lane] = v;   // inclusive over warps
+  }
+  __syncthreads();
+  int acc = (warp ? wsum[warp - 1] : 0) + incl - run;
+  for (int c = c0; c < c1; ++c) {
+    acc += chunk_hist[(long)c * E + e];
+    chunk_hist[(long)c * E + e] = acc;
+  }
+}
+
+// Loads of the routing (indices, weights): through the read-only path normally,
+// through L2 when the same kernel has just written them (fused small batches).
+template <bool FRESH>
+__device__ __forceinline__ int load_i(const int32_t* p) { return FRESH ? __ldcg(p) : __ldg(p); }
+template <bool FRESH>
+__device__ __forceinline__ float load_f(const float* p) { return FRESH ? __ldcg(p) : __ldg(p); }
+
+// Align chunk c of the slots (all kThreads threads of the CTA take part).
 // Shared layout: base[E] | off[E+1] | wcnt[kWarps][E]
-__global__ void __launch_bounds__(kThreads) align_scatter_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ wts, long S, int k, int E,
-    int nchunks, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
-    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
-  extern __shared__ int sm[];
+template <bool FRESH>
+__device__ __forceinline__ void align_chunk(
+    int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
+    const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_ids, float* __restrict__ sorted_w, int32_t* __restrict__ reverse,
+    int32_t* status, int* sm) {
   int* base = sm;
   int* off = sm + E;
   int* wcnt = sm + 2 * E + 1;
-  const int c = blockIdx.x;
   const long lo = (long)c * kChunk;
   const long hi = min(S, lo + kChunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // 1. per-expert totals (into off[]) and the base of this chunk (into base[])
-  if (chunk_hist) {
+  if (chunk_hist && hist_is_prefix) {
+    for (int e = tid; e < E; e += kThreads) {
+      base[e] = c > 0 ? __ldg(chunk_hist + (long)(c - 1) * E + e) : 0;
+      off[e] = __ldg(chunk_hist + (long)(nchunks - 1) * E + e);
+    }
+    __syncthreads();
+  } else if (chunk_hist) {
     for (int e = tid; e < E; e += kThreads) {
       int before = 0, total = 0;
       for (int cc = 0; cc < nchunks; ++cc) {
@@ -84,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
     __syncthreads();
     bool bad = false;
     for (long s = lo + tid; s < hi; s += kThreads) {
-      const int e = __ldg(idx + s);
+      const int e = load_i<FRESH>(idx + s);
       if (e >= 0 && e < E) atomicAdd(&off[e], 1);
       else bad = true;
     }
@@ -120,15 +173,27 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
   if (c == 0)
     for (int e = tid; e < E; e += kThreads) offsets[e] = off[e];
 
-  // 3. ordered ranking and scatter, kThreads slots per round
-  for (long r0 = lo; r0 < hi; r0 += kThreads) {
+  // 3. ordered ranking and scatter, kThreads * kSpt slots per round: warp w takes
+  //    the round's slots [w * 32 * kSpt, (w + 1) * 32 * kSpt) as kSpt consecutive
+  //    sub-rounds of 32, ranking each by __match_any_sync on top of the warp's
+  //    running per-expert count; a per-expert prefix over warps then places them.
+  for (long r0 = lo; r0 < hi; r0 += (long)kThreads * kSpt) {
     for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
     __syncthreads();
-    const long s = r0 + tid;
-    const int e = s < hi ? valid_expert(__ldg(idx + s), E) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    int eu[kSpt], ru[kSpt];
+#pragma unroll
+    for (int u = 0; u < kSpt; ++u) {
+      const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
+      const int e = s < hi ? valid_expert(load_i<FRESH>(idx + s), E) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int below = __popc(peers & ((1u << lane) - 1u));
+      const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
+      __syncwarp();
+      if (e >= 0 && below == 0) wcnt[warp * E + e] = prior + __popc(peers);
+      __syncwarp();
+      eu[u] = e;
+      ru[u] = prior + below;
+    }
     __syncthreads();
     for (int x = tid; x < E; x += kThreads) {
       int run = base[x];
@@ -141,17 +206,77 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
       base[x] = run;
     }
     __syncthreads();
-    if (e >= 0) {
-      const int p = off[e] + wcnt[warp * E + e] + rank;
-      sorted_ids[p] = (int)(s / k);
-      reverse[p] = (int)s;
-      sorted_w[p] = __ldg(wts + s);
+#pragma unroll
+    for (int u = 0; u < kSpt; ++u) {
+      const int e = eu[u];
+      if (e >= 0) {
+        const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
+        const int p = off[e] + wcnt[warp * E + e] + ru[u];
+        sorted_ids[p] = (int)(s / k);
+        reverse[p] = (int)s;
+        sorted_w[p] = load_f<FRESH>(wts + s);
+      }
     }
     __syncthreads();
   }
 }
 
+__global__ void __launch_bounds__(kThreads) align_scatter_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ wts, long S, int k, int E,
+    int nchunks, int hist_is_prefix, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
+  extern __shared__ int sm[];
+  align_chunk<false>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
+                     sorted_ids, sorted_w, reverse, status, sm);
+}
+
+// Small batches (all routed slots in one align chunk): gating and align in one
+// CTA and one launch. Groups of L lanes gate the tokens, the CTA synchronises,
+// then ranks and scatters the slots it has just written.
+template <int L, int V>
+__global__ void __launch_bounds__(kThreads) route_small_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int norm, float* w_out, int32_t* idx_out,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
+  extern __shared__ int sm[];
+  constexpr int groups = kThreads / L;
+  for (long t = threadIdx.x / L; t < T; t += groups)
+    gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
+  __syncthreads();
+  align_chunk<true>(0, idx_out, w_out, (long)T * k, k, E, 1, 0, nullptr, counts, offsets, sorted_ids,
+                    sorted_w, reverse, status, sm);
+}
+
+template <int L, int V>
+int launch_route_small_t(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
+                         int32_t* reverse, int32_t* status, cudaStream_t s) {
+  const size_t smem = (size_t)(2 * E + 1 + kWarps * E) * sizeof(int);
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    cudaFuncSetAttribute(route_small_kernel<L, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)((2 * MOE_MAX_EXPERTS + 1 + kWarps * MOE_MAX_EXPERTS) * sizeof(int)));
+    attr[dev] = true;
+  }
+  ProfScope ps("route_small", s);
+  route_small_kernel<L, V><<<1, kThreads, smem, s>>>(logits, T, E, k, norm, w, idx, counts, offsets,
+                                                    sorted_ids, sorted_w, reverse, status);
+  return check_launch("route_small");
+}
+
 }  // namespace
+
+bool route_fits_one_chunk(int T, int k) { return (long)T * k <= kChunk; }
+
+int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                       int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
+                       int32_t* reverse, int32_t* status, cudaStream_t s) {
+  MOE_DISPATCH_LV(E, launch_route_small_t, logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids,
+                  sorted_w, reverse, status, s);
+}
 
 size_t align_scratch_bytes(int S, int E) {
   const size_t nchunks = (size_t)(S + kChunk - 1) / kChunk;
@@ -180,9 +305,16 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
     int rc = check_launch("align_hist");
     if (rc) return rc;
   }
+  const int prefix = nchunks > kScanAbove;
+  if (prefix) {
+    ProfScope ps("align_scan", s);
+    align_scan_kernel<<<E, 1024, 0, s>>>(hist, nchunks, E);
+    int rc = check_launch("align_scan");
+    if (rc) return rc;
+  }
   ProfScope ps("align_scatter", s);
   align_scatter_kernel<<<nchunks > 0 ? nchunks : 1, kThreads, smem, s>>>(
-      idx, w, S, k, E, nchunks, hist, counts, offsets, sorted_ids, sorted_w, reverse, status);
+      idx, w, S, k, E, nchunks, prefix, hist, counts, offsets, sorted_ids, sorted_w, reverse, status);
   return check_launch("align_scatter");
 }
 

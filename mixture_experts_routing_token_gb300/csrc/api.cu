@@ -198,6 +198,26 @@ MOE_API int moe_gating_softmax_topk(const float* logits, int T, int E, int k, in
   return launch_gating(logits, T, E, k, norm_topk_prob != 0, weights, indices, (cudaStream_t)stream);
 }
 
+MOE_API int moe_group_limited_topk(const float* scores, const float* bias, int T, int E, int k,
+                                   int n_group, int topk_group, int method, float* weights,
+                                   int32_t* indices, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  REQUIRE(method == MOE_GROUP_TOPK_GREEDY || method == MOE_GROUP_TOPK_NOAUX_TC, "unknown method %d", method);
+  REQUIRE(n_group >= 1 && n_group <= 32 && E % n_group == 0, "n_group must be in [1, 32] and divide E");
+  REQUIRE(topk_group >= 1 && topk_group <= n_group, "topk_group must be in [1, n_group]");
+  REQUIRE((long)k <= (long)topk_group * (E / n_group), "k must not exceed topk_group * E / n_group");
+  REQUIRE(method != MOE_GROUP_TOPK_NOAUX_TC || E / n_group >= 2, "noaux_tc needs two experts per group");
+  REQUIRE(method != MOE_GROUP_TOPK_NOAUX_TC || bias != nullptr, "noaux_tc needs a bias");
+  if ((rc = check_tensor(scores, (long)T * E, "scores"))) return rc;
+  if (bias && (rc = check_tensor(bias, E, "bias"))) return rc;
+  if ((rc = check_tensor(weights, (long)T * k, "weights"))) return rc;
+  if ((rc = check_tensor(indices, (long)T * k, "indices"))) return rc;
+  return launch_group_limited_topk(scores, bias, T, E, k, n_group, topk_group,
+                                   method == MOE_GROUP_TOPK_NOAUX_TC, weights, indices, (cudaStream_t)stream);
+}
+
 MOE_API int moe_indices_to_multihot(const int32_t* indices, const float* probs, int T, int k, int E,
                                     uint8_t* multihot, float* probs_in_multihot,
                                     int32_t* position_map, void* stream) {
@@ -350,10 +370,16 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
   const AlignWs al = carve_align(c, S, E);
   const FfnWs fw = carve_ffn(c, dtype, S, H, I);
 
-  if ((rc = launch_gating(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, s))) return rc;
-  if ((rc = launch_align(ti, tw, T, k, E, al.counts, al.offsets, al.sorted_ids, al.sorted_w,
-                         al.reverse, al.scratch, status, s)))
-    return rc;
+  if (route_fits_one_chunk(T, k)) {
+    if ((rc = launch_route_small(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, al.counts, al.offsets,
+                                 al.sorted_ids, al.sorted_w, al.reverse, status, s)))
+      return rc;
+  } else {
+    if ((rc = launch_gating(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, s))) return rc;
+    if ((rc = launch_align(ti, tw, T, k, E, al.counts, al.offsets, al.sorted_ids, al.sorted_w,
+                           al.reverse, al.scratch, status, s)))
+      return rc;
+  }
   return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, al.counts, al.offsets, al.sorted_ids,
                  al.sorted_w, al.reverse, out, fw, status, s);
 }

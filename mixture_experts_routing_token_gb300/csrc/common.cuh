@@ -49,12 +49,19 @@ struct Carver {
 
 int launch_gating(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                   cudaStream_t s);
+int launch_group_limited_topk(const float* scores, const float* bias, int T, int E, int k, int n_group,
+                              int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s);
 int launch_indices_to_multihot(const int32_t* idx, const float* probs, int T, int k, int E,
                                uint8_t* mh, float* pm, int32_t* pos, cudaStream_t s);
 int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E, int k,
                                float* probs, int32_t* idx, cudaStream_t s);
 
 size_t align_scratch_bytes(int S, int E);
+// Gating + align in one single-CTA launch, for T*k within one align chunk.
+bool route_fits_one_chunk(int T, int k);
+int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                       int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
+                       int32_t* reverse, int32_t* status, cudaStream_t s);
 int launch_align_noalloc(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
                          int32_t* status, cudaStream_t s);

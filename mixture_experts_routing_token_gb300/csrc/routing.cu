@@ -11,101 +11,24 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "gating_device.cuh"
 
 namespace moe {
 namespace {
 
+using gate::better;
+using gate::group_mask;
+using gate::kNone;
+
 constexpr int kBlock = 256;
-constexpr int kNone = 0x7fffffff;   // "no candidate" index
-
-// (value, index) order of the page's top-k: larger value first; equal values
-// keep the lower expert index first. kNone loses to everything.
-__device__ __forceinline__ bool better(float av, int ai, float bv, int bi) {
-  if (ai == kNone) return false;
-  if (bi == kNone) return true;
-  return av > bv || (av == bv && ai < bi);
-}
-
-template <int L>
-__device__ __forceinline__ unsigned group_mask() {
-  if constexpr (L == 32) {
-    return 0xffffffffu;
-  } else {
-    const unsigned lane = threadIdx.x & 31;
-    return ((1u << L) - 1u) << (lane & ~(unsigned)(L - 1));
-  }
-}
-
-// exp(a - b) with the rounding error of the float subtraction folded back in
-// (a - b = s + err exactly, exp(s + err) ~= exp(s) * (1 + err)).
-__device__ __forceinline__ float exp_diff(float a, float b) {
-  const float s = a - b;
-  const float bb = s - a;
-  const float err = (a - (s - bb)) + (-b - bb);
-  const float e = expf(s);
-  return fmaf(e, err, e);
-}
-
 template <int L, int V>
 __global__ void __launch_bounds__(kBlock) gating_kernel(const float* __restrict__ logits, int T,
                                                         int E, int k, int norm,
                                                         float* __restrict__ w_out,
                                                         int32_t* __restrict__ idx_out) {
-  const int g = threadIdx.x & (L - 1);
   const long t = (long)blockIdx.x * (kBlock / L) + threadIdx.x / L;
   if (t >= T) return;   // whole groups leave together
-  const unsigned gm = group_mask<L>();
-  const float* row = logits + t * (long)E;
-
-  float v[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = g + i * L;
-    v[i] = e < E ? __ldg(row + e) : 0.0f;
-  }
-  unsigned taken = 0;
-#pragma unroll
-  for (int i = 0; i < V; ++i)
-    if (g + i * L >= E) taken |= 1u << i;
-
-  float my_v = 0.0f, row_max = 0.0f;
-  int my_i = -1;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = kNone;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int e = g + i * L;
-      if (!((taken >> i) & 1u) && better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
-    }
-#pragma unroll
-    for (int off = L / 2; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(gm, bv, off, L);
-      const int oi = __shfl_xor_sync(gm, bi, off, L);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if ((bi & (L - 1)) == g) taken |= 1u << (bi / L);
-    if (j == 0) row_max = bv;
-    if (g == j) { my_v = bv; my_i = bi; }
-  }
-
-  // denominator: the k selected (norm) or the whole row, summed in double
-  double part = 0.0;
-  if (norm) {
-    if (g < k) part = (double)exp_diff(my_v, row_max);
-  } else {
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-      if (g + i * L < E) part += (double)exp_diff(v[i], row_max);
-  }
-#pragma unroll
-  for (int off = L / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(gm, part, off, L);
-
-  if (g < k) {
-    const float num = exp_diff(my_v, row_max);
-    w_out[t * k + g] = (float)((double)num / part);
-    idx_out[t * k + g] = my_i;
-  }
+  gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
 }
 
 template <int L, int V>
@@ -118,45 +41,134 @@ int launch_gating_t(const float* logits, int T, int E, int k, int norm, float* w
 }
 
 // ---------------------------------------------------------------------------
-// indices -> multihot: one thread writes 4 consecutive experts of one row.
+// indices -> multihot: one thread writes 4 consecutive experts of one row
+// (three 16/4-byte vector stores); it reads the row's k indices and probs as
+// vectors when k is 1, 2, 4 or 8 (the rows of a token's threads share them in L1).
 
+template <int K>
+__device__ __forceinline__ void load_row(const int32_t* __restrict__ idx, const float* __restrict__ probs,
+                                         long t, int (&e)[K], float (&p)[K]) {
+  if constexpr (K == 8) {
+    const int4 a = __ldg(reinterpret_cast<const int4*>(idx + t * 8));
+    const int4 b = __ldg(reinterpret_cast<const int4*>(idx + t * 8) + 1);
+    const float4 c = __ldg(reinterpret_cast<const float4*>(probs + t * 8));
+    const float4 d = __ldg(reinterpret_cast<const float4*>(probs + t * 8) + 1);
+    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w; e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
+    p[0] = c.x; p[1] = c.y; p[2] = c.z; p[3] = c.w; p[4] = d.x; p[5] = d.y; p[6] = d.z; p[7] = d.w;
+  } else if constexpr (K == 4) {
+    const int4 a = __ldg(reinterpret_cast<const int4*>(idx + t * 4));
+    const float4 c = __ldg(reinterpret_cast<const float4*>(probs + t * 4));
+    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
+    p[0] = c.x; p[1] = c.y; p[2] = c.z; p[3] = c.w;
+  } else if constexpr (K == 2) {
+    const int2 a = __ldg(reinterpret_cast<const int2*>(idx + t * 2));
+    const float2 c = __ldg(reinterpret_cast<const float2*>(probs + t * 2));
+    e[0] = a.x; e[1] = a.y;
+    p[0] = c.x; p[1] = c.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      e[j] = __ldg(idx + t * K + j);
+      p[j] = __ldg(probs + t * K + j);
+    }
+  }
+}
+
+// K > 0: k == K known at compile time; K == 0: any k (scalar loads).
+template <int K>
 __global__ void __launch_bounds__(kBlock) indices_to_multihot_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ probs, int T, int k, int E,
     uint8_t* __restrict__ mh, float* __restrict__ pm, int32_t* __restrict__ pos) {
   const int E4 = (E + 3) >> 2;
-  const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (tid >= (long)T * E4) return;
-  const long t = tid / E4;
-  const int e0 = (int)(tid - t * E4) * 4;
-  unsigned m[4] = {0, 0, 0, 0};
-  float p[4] = {0.f, 0.f, 0.f, 0.f};
-  int q[4] = {-1, -1, -1, -1};
-  for (int j = k - 1; j >= 0; --j) {       // descending, so the lowest j is kept on a repeat
-    const int e = __ldg(idx + t * k + j);
-    const int d = e - e0;
-    if (e >= 0 && e < E && d >= 0 && d < 4) {
-      m[d] = 1;
-      p[d] = __ldg(probs + t * k + j);
-      q[d] = j;
+  const long n = (long)T * E4;
+  for (long tid = (long)blockIdx.x * blockDim.x + threadIdx.x; tid < n; tid += (long)gridDim.x * blockDim.x) {
+    const long t = tid / E4;
+    const int e0 = (int)(tid - t * E4) * 4;
+    unsigned m[4] = {0, 0, 0, 0};
+    float p[4] = {0.f, 0.f, 0.f, 0.f};
+    int q[4] = {-1, -1, -1, -1};
+    if constexpr (K > 0) {
+      int re[K];
+      float rp[K];
+      load_row<K>(idx, probs, t, re, rp);
+#pragma unroll
+      for (int j = K - 1; j >= 0; --j) {   // descending, so the lowest j is kept on a repeat
+        const int d = re[j] - e0;
+        if (re[j] >= 0 && re[j] < E && d >= 0 && d < 4) {
+          m[d] = 1;
+          p[d] = rp[j];
+          q[d] = j;
+        }
+      }
+    } else {
+      for (int j = k - 1; j >= 0; --j) {
+        const int e = __ldg(idx + t * k + j);
+        const int d = e - e0;
+        if (e >= 0 && e < E && d >= 0 && d < 4) {
+          m[d] = 1;
+          p[d] = __ldg(probs + t * k + j);
+          q[d] = j;
+        }
+      }
     }
-  }
-  const long base = t * (long)E + e0;
-  if ((E & 3) == 0) {
-    *reinterpret_cast<uchar4*>(mh + base) = make_uchar4(m[0], m[1], m[2], m[3]);
-    *reinterpret_cast<float4*>(pm + base) = make_float4(p[0], p[1], p[2], p[3]);
-    *reinterpret_cast<int4*>(pos + base) = make_int4(q[0], q[1], q[2], q[3]);
-  } else {
-    for (int d = 0; d < 4 && e0 + d < E; ++d) {
-      mh[base + d] = (uint8_t)m[d];
-      pm[base + d] = p[d];
-      pos[base + d] = q[d];
+    const long base = t * (long)E + e0;
+    if ((E & 3) == 0) {
+      __stcs(reinterpret_cast<unsigned*>(mh + base), m[0] | (m[1] << 8) | (m[2] << 16) | (m[3] << 24));
+      __stcs(reinterpret_cast<float4*>(pm + base), make_float4(p[0], p[1], p[2], p[3]));
+      __stcs(reinterpret_cast<int4*>(pos + base), make_int4(q[0], q[1], q[2], q[3]));
+    } else {
+      for (int d = 0; d < 4 && e0 + d < E; ++d) {
+        mh[base + d] = (uint8_t)m[d];
+        pm[base + d] = p[d];
+        pos[base + d] = q[d];
+      }
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// multihot -> indices: a group of L lanes per row; each output slot is written
-// once, by the lane that owns its expert or (unfilled) by lane j % L.
+// multihot -> indices. Vector form (E % 4 == 0): G lanes per row, each reading
+// NV aligned 16-byte vectors of the position map and of the probs; a lane
+// writes the slots its experts fill, the group ORs the filled-slot masks and
+// lane j % G writes any slot j that no expert fills. Every output slot is
+// written once. Scalar form for other E.
+
+template <int G, int NV>
+__global__ void __launch_bounds__(kBlock) multihot_to_indices_vec_kernel(
+    const float* __restrict__ pm, const int32_t* __restrict__ pos, int T, int E, int k,
+    float* __restrict__ probs, int32_t* __restrict__ idx_out) {
+  const int g = threadIdx.x & (G - 1);
+  const unsigned gm = group_mask<G>();
+  const long rows_per_grid = (long)gridDim.x * (kBlock / G);
+  for (long t = (long)blockIdx.x * (kBlock / G) + threadIdx.x / G; t < T; t += rows_per_grid) {
+    unsigned filled = 0;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int e0 = (v * G + g) * 4;
+      const int4 q = __ldcs(reinterpret_cast<const int4*>(pos + t * E + e0));
+      const float4 w = __ldcs(reinterpret_cast<const float4*>(pm + t * E + e0));
+      const int qa[4] = {q.x, q.y, q.z, q.w};
+      const float wa[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+        const int p = qa[d];
+        if (p >= 0 && p < k) {
+          probs[t * k + p] = wa[d];
+          if (idx_out) idx_out[t * k + p] = e0 + d;
+          filled |= 1u << p;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = G / 2; off >= 1; off >>= 1) filled |= __shfl_xor_sync(gm, filled, off, G);
+    for (int j = g; j < k; j += G) {
+      if (!((filled >> j) & 1u)) {
+        probs[t * k + j] = 0.0f;
+        if (idx_out) idx_out[t * k + j] = -1;
+      }
+    }
+  }
+}
 
 template <int L, int V>
 __global__ void __launch_bounds__(kBlock) multihot_to_indices_kernel(
@@ -197,23 +209,132 @@ int launch_m2i_t(const float* pm, const int32_t* pos, int T, int E, int k, float
   return check_launch("multihot_to_indices");
 }
 
+template <int G, int NV>
+int launch_m2i_vec(const float* pm, const int32_t* pos, int T, int E, int k, float* probs, int32_t* idx,
+                   cudaStream_t s) {
+  const int rows_per_block = kBlock / G;
+  long blocks = ((long)T + rows_per_block - 1) / rows_per_block;
+  const long cap = (long)num_sms() * 16;
+  multihot_to_indices_vec_kernel<G, NV><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
+      pm, pos, T, E, k, probs, idx);
+  return check_launch("multihot_to_indices");
+}
+
+template <int K>
+int launch_i2m(const int32_t* idx, const float* probs, int T, int k, int E, uint8_t* mh, float* pm,
+               int32_t* pos, cudaStream_t s) {
+  const long n = (long)T * ((E + 3) / 4);
+  long blocks = (n + kBlock - 1) / kBlock;
+  const long cap = (long)num_sms() * 16;
+  indices_to_multihot_kernel<K><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
+      idx, probs, T, k, E, mh, pm, pos);
+  return check_launch("indices_to_multihot");
+}
+
+// ---------------------------------------------------------------------------
+// Group-limited top-k: mlc-llm moe_misc.py, group_limited_greedy_topk.
+// One warp per token; the choice scores (scores, + bias for noaux_tc) are kept
+// in registers (lane l holds experts l, l+32, ...) and in a per-warp shared row
+// from which lane g < n_group scores group g (its max, or the sum of its two
+// largest for noaux_tc, both as float32 like the page). topk_group rounds of
+// warp arg-max pick the groups, then k rounds pick experts inside them; the
+// tie rule is the page's (larger value first, lower index on equality).
+
+constexpr int kGroupWarps = 8;
+
+template <int V>
+__global__ void __launch_bounds__(kGroupWarps * 32) group_topk_kernel(
+    const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k, int n_group,
+    int topk_group, int noaux, float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  extern __shared__ float rows[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long t = (long)blockIdx.x * kGroupWarps + wid;
+  if (t >= T) return;                          // whole warps leave together
+  float* row = rows + wid * E;
+  const int gs = E / n_group;
+  float sv[V], cv[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    sv[i] = e < E ? __ldg(scores + t * E + e) : 0.0f;
+    cv[i] = (e < E && noaux) ? sv[i] + __ldg(bias + e) : sv[i];
+    if (e < E) row[e] = cv[i];
+  }
+  __syncwarp();
+  // group scores (lanes g < n_group); each lane starts its scan at a different
+  // column so the lanes hit different shared-memory banks (max and top-2 do not
+  // depend on the scan order)
+  unsigned gkey = 0;
+  if (lane < n_group) {
+    const float* g = row + lane * gs;
+    float b1 = -FLT_MAX, b2 = -FLT_MAX;
+    int c = lane % gs;
+    for (int n = 0; n < gs; ++n) {
+      const float x = g[c];
+      if (x > b1) { b2 = b1; b1 = x; }
+      else if (x > b2) b2 = x;
+      if (++c == gs) c = 0;
+    }
+    gkey = gate::okey(noaux ? b1 + b2 : b1);
+  }
+  unsigned gsel = 0;
+  {
+    unsigned gk[1] = {gkey};
+    unsigned gtaken = lane < n_group ? 0u : 1u;
+    for (int j = 0; j < topk_group; ++j) {
+      unsigned m;
+      const int bi = gate::warp_argmax_round<1>(gk, gtaken, lane, &m);
+      gsel |= 1u << bi;
+      if (bi == lane) gtaken = 1u;
+    }
+  }
+  // experts of the kept groups
+  unsigned taken = 0;
+  unsigned key[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = gate::okey(cv[i]);
+    if (e >= E || !((gsel >> (e / gs)) & 1u)) taken |= 1u << i;
+  }
+  float my_w = 0.0f;
+  int my_i = -1;
+  for (int j = 0; j < k; ++j) {
+    unsigned m;
+    const int bi = gate::warp_argmax_round<V>(key, taken, lane, &m);
+    float s_owner = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (lane + 32 * i == bi) s_owner = sv[i];
+    const float bs = __shfl_sync(0xffffffffu, s_owner, bi & 31);
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) { my_w = noaux ? bs : gate::okey_value(m); my_i = bi; }
+  }
+  if (lane < k) {
+    w_out[t * k + lane] = my_w;
+    idx_out[t * k + lane] = my_i;
+  }
+}
+
+template <int V>
+int launch_group_t(const float* scores, const float* bias, int T, int E, int k, int n_group,
+                   int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
+  const size_t smem = (size_t)kGroupWarps * E * sizeof(float);
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    cudaFuncSetAttribute(group_topk_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kGroupWarps * MOE_MAX_EXPERTS * (int)sizeof(float));
+    attr[dev] = true;
+  }
+  group_topk_kernel<V><<<(T + kGroupWarps - 1) / kGroupWarps, kGroupWarps * 32, smem, s>>>(
+      scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
+  return check_launch("group_limited_topk");
+}
+
 }  // namespace
 
-// Dispatch on E: L lanes per row, V = ceil(E / L) values per lane.
-#define MOE_DISPATCH_LV(E, FN, ...)                                        \
-  do {                                                                     \
-    if ((E) <= 1) return FN<1, 1>(__VA_ARGS__);                            \
-    if ((E) <= 2) return FN<2, 1>(__VA_ARGS__);                            \
-    if ((E) <= 4) return FN<4, 1>(__VA_ARGS__);                            \
-    if ((E) <= 8) return FN<8, 1>(__VA_ARGS__);                            \
-    if ((E) <= 16) return FN<16, 1>(__VA_ARGS__);                          \
-    if ((E) <= 32) return FN<32, 1>(__VA_ARGS__);                          \
-    if ((E) <= 64) return FN<32, 2>(__VA_ARGS__);                          \
-    if ((E) <= 128) return FN<32, 4>(__VA_ARGS__);                         \
-    if ((E) <= 256) return FN<32, 8>(__VA_ARGS__);                         \
-    if ((E) <= 512) return FN<32, 16>(__VA_ARGS__);                        \
-    return FN<32, 32>(__VA_ARGS__);                                        \
-  } while (0)
 
 int launch_gating(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                   cudaStream_t s) {
@@ -226,17 +347,44 @@ int launch_indices_to_multihot(const int32_t* idx, const float* probs, int T, in
                                uint8_t* mh, float* pm, int32_t* pos, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   ProfScope ps("indices_to_multihot", s);
-  const long n = (long)T * ((E + 3) / 4);
-  indices_to_multihot_kernel<<<(unsigned)((n + kBlock - 1) / kBlock), kBlock, 0, s>>>(
-      idx, probs, T, k, E, mh, pm, pos);
-  return check_launch("indices_to_multihot");
+  switch (k) {
+    case 1: return launch_i2m<1>(idx, probs, T, k, E, mh, pm, pos, s);
+    case 2: return launch_i2m<2>(idx, probs, T, k, E, mh, pm, pos, s);
+    case 4: return launch_i2m<4>(idx, probs, T, k, E, mh, pm, pos, s);
+    case 8: return launch_i2m<8>(idx, probs, T, k, E, mh, pm, pos, s);
+    default: return launch_i2m<0>(idx, probs, T, k, E, mh, pm, pos, s);
+  }
 }
 
 int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E, int k,
                                float* probs, int32_t* idx, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   ProfScope ps("multihot_to_indices", s);
+  switch (E) {
+    case 4: return launch_m2i_vec<1, 1>(pm, pos, T, E, k, probs, idx, s);
+    case 8: return launch_m2i_vec<2, 1>(pm, pos, T, E, k, probs, idx, s);
+    case 16: return launch_m2i_vec<4, 1>(pm, pos, T, E, k, probs, idx, s);
+    case 32: return launch_m2i_vec<8, 1>(pm, pos, T, E, k, probs, idx, s);
+    case 64: return launch_m2i_vec<16, 1>(pm, pos, T, E, k, probs, idx, s);
+    case 128: return launch_m2i_vec<32, 1>(pm, pos, T, E, k, probs, idx, s);
+    case 256: return launch_m2i_vec<32, 2>(pm, pos, T, E, k, probs, idx, s);
+    case 512: return launch_m2i_vec<32, 4>(pm, pos, T, E, k, probs, idx, s);
+    case 1024: return launch_m2i_vec<32, 8>(pm, pos, T, E, k, probs, idx, s);
+    default: break;
+  }
   MOE_DISPATCH_LV(E, launch_m2i_t, pm, pos, T, E, k, probs, idx, s);
+}
+
+int launch_group_limited_topk(const float* scores, const float* bias, int T, int E, int k, int n_group,
+                              int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  ProfScope ps("group_limited_topk", s);
+  if (E <= 32) return launch_group_t<1>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (E <= 64) return launch_group_t<2>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (E <= 128) return launch_group_t<4>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (E <= 256) return launch_group_t<8>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (E <= 512) return launch_group_t<16>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  return launch_group_t<32>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
 }
 
 }  // namespace moe

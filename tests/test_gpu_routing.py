@@ -163,3 +163,56 @@ def test_align_invalid_index_sets_status_and_drops_slot():
         w = np.ones(i.shape, np.float32)
         st = _align_case(moe, i, w, 3)
         assert st & moe.MOE_STATUS_BAD_INDEX
+
+
+# ---- group-limited top-k ------------------------------------------------------------
+
+def _group_case(moe, x, bias, k, n_group, topk_group, method):
+    w_ref, i_ref = gating.group_limited_topk(x, k, n_group, topk_group, method, bias)
+    b = torch.from_numpy(bias).to(DEV) if bias is not None else None
+    w, i = moe.moe_group_limited_topk(torch.from_numpy(x).to(DEV), k, n_group, topk_group, method, bias=b)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(i.cpu().numpy(), i_ref)
+    np.testing.assert_array_equal(w.cpu().numpy(), w_ref)     # weights are copies of input scores
+
+
+def _sigmoid_scores(T, E, seed):
+    x = gen_logits(np.random.SeedSequence(seed), T, E, "distinct").astype(np.float64)
+    return (1.0 / (1.0 + np.exp(-x))).astype(np.float32)
+
+
+@pytest.mark.parametrize("T,E,k,n_group,topk_group", [
+    (4096, 256, 8, 8, 4),      # DeepSeek-V3-shaped routing
+    (3000, 160, 6, 8, 3),      # DeepSeek-V2-shaped routing
+    (777, 64, 6, 8, 3), (100, 8, 2, 4, 2), (50, 1024, 32, 32, 7), (1, 256, 8, 8, 4), (0, 256, 8, 8, 4),
+    (64, 96, 4, 3, 1), (64, 32, 3, 16, 2),
+])
+@pytest.mark.parametrize("method", ["group_limited_greedy", "noaux_tc"])
+def test_group_limited_topk(T, E, k, n_group, topk_group, method):
+    moe = need_gpu()
+    x = _sigmoid_scores(T, E, T + E)
+    bias = (gen_logits(np.random.SeedSequence(E), 1, E, "distinct")[0] * np.float32(0.05)).astype(np.float32)
+    _group_case(moe, x, bias if method == "noaux_tc" else None, k, n_group, topk_group, method)
+
+
+@pytest.mark.parametrize("method", ["group_limited_greedy", "noaux_tc"])
+def test_group_limited_topk_ties_and_golden(method, gold):
+    moe = need_gpu()
+    rng = np.random.default_rng(4)
+    x = (rng.integers(0, 4, size=(500, 48)) * 0.25).astype(np.float32)
+    bias = (rng.integers(-1, 2, size=48) * 0.25).astype(np.float32)
+    _group_case(moe, x, bias, 5, 6, 3, method)
+    g = gold("group_limited_topk")
+    x = np.array(g["scores"], np.float32)
+    _group_case(moe, x, np.array(g["bias"], np.float32), g["k"], g["n_group"], g["topk_group"], method)
+
+
+def test_group_limited_topk_rejects_bad_arguments():
+    moe = need_gpu()
+    x = torch.rand((4, 256), device=DEV)
+    with pytest.raises(moe.MoeError):
+        moe.moe_group_limited_topk(x, 8, 7, 3)                      # 7 does not divide 256
+    with pytest.raises(moe.MoeError):
+        moe.moe_group_limited_topk(x, 8, 8, 4, "noaux_tc")          # no bias
+    with pytest.raises(moe.MoeError):
+        moe.moe_group_limited_topk(x, 100, 8, 1)                    # k > topk_group * group size
