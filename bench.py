@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-routing", action="store_true", help="skip the large-T routing bandwidth section")
+    ap.add_argument("--routing-only", action="store_true",
+                    help="only the large-T routing bandwidth section (prints it as JSON; for profiling)")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="time the step as a CUDA graph replay (auto: on for decode batches, T <= 64)")
     return ap.parse_args()
@@ -50,6 +52,23 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (the slowest rank's time); x itself when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, world: int, steps: int, ms_total: float) -> float:
+    """Tokens/s of the whole job: every rank runs its own replica of the workload, so the
+    job processes tokens_per_rank * world tokens per step in the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms_total / 1e3)
 
 
 def measured_peaks():
@@ -352,6 +371,11 @@ def main():
         dist.barrier()
     moe.lib()
 
+    if args.routing_only:
+        if rank == 0:
+            print(json.dumps({"workload": wl.name, "routing": routing_bandwidth(moe, wl, dev, measured_peaks(),
+                                                                                 reps=max(1, args.steps))}), flush=True)
+        return
     hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=rank)
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
     dcode = moe.MOE_BF16 if wl.dtype == "bf16" else moe.MOE_F32
@@ -422,13 +446,9 @@ def main():
         moe.profiler_enable(False)
         kern = moe.profiler_report()
     clocks = clk.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
     ms = ms_total / args.steps
-    value = T * world * args.steps / (ms_total / 1e3)
+    value = whole_job_rate(T, world, args.steps, ms_total)
 
     # ---- end to end through the public call: pinned host inputs in, output back to host
     e2e = None
@@ -455,12 +475,8 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": T * world * args.steps / (e_ms / 1e3), "unit": UNIT,
+        e_ms = max_over_ranks(a.elapsed_time(b), dev)
+        e2e = {"value": whole_job_rate(T, world, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size() + h_logits.numel() * 4,
                "d2h_bytes_per_step": h_out.numel() * h_out.element_size()}
 

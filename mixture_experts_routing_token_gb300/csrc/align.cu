@@ -37,6 +37,11 @@ constexpr int kScanAbove = 16; // chunks above which the per-expert prefix gets 
 
 __device__ __forceinline__ int valid_expert(int e, int E) { return (e >= 0 && e < E) ? e : -1; }
 
+// Dynamic shared memory of align_chunk for E experts.
+__host__ __device__ inline size_t align_smem_bytes(int E) {
+  return (size_t)(4 * E + 2 + kWarps * E + 3 * kChunk) * sizeof(int);
+}
+
 __global__ void __launch_bounds__(kThreads) align_hist_kernel(const int32_t* __restrict__ idx,
                                                               long S, int E,
                                                               int32_t* __restrict__ chunk_hist,
@@ -98,8 +103,37 @@ __device__ __forceinline__ int load_i(const int32_t* p) { return FRESH ? __ldcg(
 template <bool FRESH>
 __device__ __forceinline__ float load_f(const float* p) { return FRESH ? __ldcg(p) : __ldg(p); }
 
+// Exclusive scan of v[0..n) in place by warp 0 (lane l owns a run of entries);
+// returns the total in lane 31.
+__device__ __forceinline__ int warp0_exclusive_scan(int* v, int n) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int e0 = min(n, lane * per), e1 = min(n, e0 + per);
+  int run = 0;
+  for (int e = e0; e < e1; ++e) run += v[e];
+  int incl = run;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  int acc = incl - run;
+  for (int e = e0; e < e1; ++e) {
+    const int c = v[e];
+    v[e] = acc;
+    acc += c;
+  }
+  return incl;
+}
+
 // Align chunk c of the slots (all kThreads threads of the CTA take part).
-// Shared layout: base[E] | off[E+1] | wcnt[kWarps][E]
+// Shared layout (ints): base[E] | off[E+1] | cb[E] | cpre[E+1] | wcnt[kWarps][E]
+//                       | staged token ids, slots, weights [kChunk] each.
+// base[e] runs over the chunk's slots of expert e (global rank among all slots
+// of e), cb[e] is its value at the chunk start, cpre[e] the chunk-local start of
+// e's slots. Slots are ranked into the staging arrays in expert-sorted order,
+// then each expert's run is copied to its global positions by consecutive
+// threads (coalesced stores).
 template <bool FRESH>
 __device__ __forceinline__ void align_chunk(
     int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
@@ -107,16 +141,23 @@ __device__ __forceinline__ void align_chunk(
     int32_t* __restrict__ sorted_ids, float* __restrict__ sorted_w, int32_t* __restrict__ reverse,
     int32_t* status, int* sm) {
   int* base = sm;
-  int* off = sm + E;
-  int* wcnt = sm + 2 * E + 1;
+  int* off = base + E;
+  int* cb = off + E + 1;
+  int* cpre = cb + E;
+  int* wcnt = cpre + E + 1;
+  int* s_tok = wcnt + kWarps * E;
+  int* s_rev = s_tok + kChunk;
+  float* s_w = reinterpret_cast<float*>(s_rev + kChunk);
   const long lo = (long)c * kChunk;
   const long hi = min(S, lo + kChunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // 1. per-expert totals (into off[]) and the base of this chunk (into base[])
+  // 1. per-expert totals (off[]), base of this chunk (base[], cb[]) and this chunk's counts (cpre[])
   if (chunk_hist && hist_is_prefix) {
     for (int e = tid; e < E; e += kThreads) {
-      base[e] = c > 0 ? __ldg(chunk_hist + (long)(c - 1) * E + e) : 0;
+      const int before = c > 0 ? __ldg(chunk_hist + (long)(c - 1) * E + e) : 0;
+      base[e] = cb[e] = before;
+      cpre[e] = __ldg(chunk_hist + (long)c * E + e) - before;
       off[e] = __ldg(chunk_hist + (long)(nchunks - 1) * E + e);
     }
     __syncthreads();
@@ -128,12 +169,13 @@ __device__ __forceinline__ void align_chunk(
         before += cc < c ? h : 0;
         total += h;
       }
-      base[e] = before;
+      base[e] = cb[e] = before;
+      cpre[e] = __ldg(chunk_hist + (long)c * E + e);
       off[e] = total;
     }
     __syncthreads();
   } else {   // single chunk: histogram here
-    for (int e = tid; e < E; e += kThreads) { base[e] = 0; off[e] = 0; }
+    for (int e = tid; e < E; e += kThreads) { base[e] = 0; cb[e] = 0; off[e] = 0; }
     __syncthreads();
     bool bad = false;
     for (long s = lo + tid; s < hi; s += kThreads) {
@@ -143,48 +185,50 @@ __device__ __forceinline__ void align_chunk(
     }
     if (bad && status) atomicOr(status, MOE_STATUS_BAD_INDEX);
     __syncthreads();
+    for (int e = tid; e < E; e += kThreads) cpre[e] = off[e];
+    __syncthreads();
   }
 
-  // 2. exclusive scan of the totals over experts (warp 0; lane l owns a run of experts)
+  // 2. exclusive scans over experts: totals -> offsets (warp 0), chunk counts -> cpre (warp 1)
   if (warp == 0) {
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int run = 0;
-    for (int e = e0; e < e1; ++e) run += off[e];
-    int incl = run;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += o;
+    int cnt0 = 0;
+    if (c == 0) {
+      for (int e = lane; e < E; e += 32) counts[e] = off[e];
     }
-    int acc = incl - run;
-    for (int e = e0; e < e1; ++e) {
-      const int cnt = off[e];
-      if (c == 0) counts[e] = cnt;
-      off[e] = acc;
-      acc += cnt;
-    }
+    __syncwarp();
+    const int total = warp0_exclusive_scan(off, E);
     if (lane == 31) {
-      off[E] = incl;
-      if (c == 0) offsets[E] = incl;
+      off[E] = total;
+      if (c == 0) offsets[E] = total;
     }
+    (void)cnt0;
+  } else if (warp == 1) {
+    const int total = warp0_exclusive_scan(cpre, E);
+    if (lane == 31) cpre[E] = total;
   }
   __syncthreads();
   if (c == 0)
     for (int e = tid; e < E; e += kThreads) offsets[e] = off[e];
 
-  // 3. ordered ranking and scatter, kThreads * kSpt slots per round: warp w takes
-  //    the round's slots [w * 32 * kSpt, (w + 1) * 32 * kSpt) as kSpt consecutive
-  //    sub-rounds of 32, ranking each by __match_any_sync on top of the warp's
-  //    running per-expert count; a per-expert prefix over warps then places them.
+  // 3. ordered ranking into the staging arrays, kThreads * kSpt slots per round: warp w
+  //    takes the round's slots [w * 32 * kSpt, (w + 1) * 32 * kSpt) as kSpt consecutive
+  //    sub-rounds of 32, ranking each by __match_any_sync on top of the warp's running
+  //    per-expert count; a per-expert prefix over warps then places them.
   for (long r0 = lo; r0 < hi; r0 += (long)kThreads * kSpt) {
     for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
     __syncthreads();
     int eu[kSpt], ru[kSpt];
+    float wu[kSpt];
+    // issue all of this thread's loads for the round before ranking
 #pragma unroll
     for (int u = 0; u < kSpt; ++u) {
       const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
-      const int e = s < hi ? valid_expert(load_i<FRESH>(idx + s), E) : -1;
+      eu[u] = s < hi ? load_i<FRESH>(idx + s) : -1;
+      wu[u] = s < hi ? load_f<FRESH>(wts + s) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kSpt; ++u) {
+      const int e = valid_expert(eu[u], E);
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int below = __popc(peers & ((1u << lane) - 1u));
       const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
@@ -211,13 +255,27 @@ __device__ __forceinline__ void align_chunk(
       const int e = eu[u];
       if (e >= 0) {
         const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
-        const int p = off[e] + wcnt[warp * E + e] + ru[u];
-        sorted_ids[p] = (int)(s / k);
-        reverse[p] = (int)s;
-        sorted_w[p] = load_f<FRESH>(wts + s);
+        const int q = cpre[e] + wcnt[warp * E + e] + ru[u] - cb[e];   // chunk-local, expert-sorted
+        s_tok[q] = (int)(s / k);
+        s_rev[q] = (int)s;
+        s_w[q] = wu[u];
       }
     }
     __syncthreads();
+  }
+
+  // 4. copy each expert's run of the chunk to its global positions (coalesced)
+  const int n = cpre[E];
+  for (int q = tid; q < n; q += kThreads) {
+    int lo_e = 0, hi_e = E - 1;               // expert e with cpre[e] <= q < cpre[e + 1]
+    while (lo_e < hi_e) {
+      const int mid = (lo_e + hi_e + 1) >> 1;
+      if (cpre[mid] <= q) lo_e = mid; else hi_e = mid - 1;
+    }
+    const int p = off[lo_e] + cb[lo_e] + (q - cpre[lo_e]);
+    sorted_ids[p] = s_tok[q];
+    reverse[p] = s_rev[q];
+    sorted_w[p] = s_w[q];
   }
 }
 
@@ -240,6 +298,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
   extern __shared__ int sm[];
+  pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
   constexpr int groups = kThreads / L;
   for (long t = threadIdx.x / L; t < T; t += groups)
     gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
@@ -252,13 +311,13 @@ template <int L, int V>
 int launch_route_small_t(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                          int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                          int32_t* reverse, int32_t* status, cudaStream_t s) {
-  const size_t smem = (size_t)(2 * E + 1 + kWarps * E) * sizeof(int);
+  const size_t smem = align_smem_bytes(E);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
     cudaFuncSetAttribute(route_small_kernel<L, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)((2 * MOE_MAX_EXPERTS + 1 + kWarps * MOE_MAX_EXPERTS) * sizeof(int)));
+                         (int)align_smem_bytes(MOE_MAX_EXPERTS));
     attr[dev] = true;
   }
   ProfScope ps("route_small", s);
@@ -274,8 +333,16 @@ bool route_fits_one_chunk(int T, int k) { return (long)T * k <= kChunk; }
 int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                        int32_t* reverse, int32_t* status, cudaStream_t s) {
-  MOE_DISPATCH_LV(E, launch_route_small_t, logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids,
-                  sorted_w, reverse, status, s);
+  // a whole warp per token: few tokens, so the per-token latency matters
+#define MOE_ROUTE_SMALL(V) \
+  return launch_route_small_t<32, V>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, status, s)
+  if (E <= 32) MOE_ROUTE_SMALL(1);
+  if (E <= 64) MOE_ROUTE_SMALL(2);
+  if (E <= 128) MOE_ROUTE_SMALL(4);
+  if (E <= 256) MOE_ROUTE_SMALL(8);
+  if (E <= 512) MOE_ROUTE_SMALL(16);
+  MOE_ROUTE_SMALL(32);
+#undef MOE_ROUTE_SMALL
 }
 
 size_t align_scratch_bytes(int S, int E) {
@@ -288,13 +355,13 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
                  void* scratch, int32_t* status, cudaStream_t s) {
   const long S = (long)T * k;
   const int nchunks = (int)((S + kChunk - 1) / kChunk);
-  const size_t smem = (size_t)(2 * E + 1 + kWarps * E) * sizeof(int);
+  const size_t smem = align_smem_bytes(E);
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
     cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)((2 * MOE_MAX_EXPERTS + 1 + kWarps * MOE_MAX_EXPERTS) * sizeof(int)));
+                         (int)align_smem_bytes(MOE_MAX_EXPERTS));
     attr_set[dev] = true;
   }
   int32_t* hist = nullptr;

@@ -3,6 +3,9 @@
 // mlc-llm moe_misc.py moe_sum (sum of the [T, k, H] expert outputs over k);
 // the routing weight was already applied by the FC2 epilogue.
 // HBM-bound streaming kernel: 16-byte loads, one thread per 4 output columns.
+// Launched with programmatic dependency on the FC2 kernel (waits before reading).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -30,6 +33,8 @@ struct Out4<__nv_bfloat16> {
 template <class OutT>
 __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restrict__ staging, long T,
                                                           int k, int H4, OutT* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const long n = T * H4;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
     const long t = i / H4;
@@ -50,6 +55,8 @@ __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restri
 template <class OutT>
 __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __restrict__ staging, long T,
                                                              int k, int H, OutT* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const long n = T * H;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
     const long t = i / H;
@@ -63,11 +70,16 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __rest
 template <class OutT>
 int launch_t(const float* staging, int T, int k, int H, OutT* out, cudaStream_t s) {
   ProfScope ps("combine", s);
-  const int grid = num_sms() * 8;
+  const long units = (long)T * (H % 4 == 0 ? H / 4 : H);
+  const long cap = (long)num_sms() * 8;
+  const int grid = (int)std::max(1L, std::min(cap, (units + 255) / 256));
+  cudaError_t e;
   if (H % 4 == 0)
-    combine_vec_kernel<OutT><<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(staging), T, k, H / 4, out);
+    e = launch_pdl(combine_vec_kernel<OutT>, grid, 256, 0, s, reinterpret_cast<const float4*>(staging), (long)T, k,
+                   H / 4, out);
   else
-    combine_scalar_kernel<OutT><<<grid, 256, 0, s>>>(staging, T, k, H, out);
+    e = launch_pdl(combine_scalar_kernel<OutT>, grid, 256, 0, s, staging, (long)T, k, H, out);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "combine: %s", cudaGetErrorString(e));
   return check_launch("combine");
 }
 

@@ -104,7 +104,34 @@ int launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
 int launch_combine(const float* staging, int T, int k, int H, int dtype, void* out,
                    cudaStream_t s);
 
+// Launch with programmatic stream serialization (PDL): the kernel may start while
+// the previous kernel on the stream is still running; it must execute
+// pdl_wait() before touching anything that kernel writes, and every kernel
+// calls pdl_trigger() only after its own pdl_wait(), so that everything two or
+// more launches back is complete whenever a kernel starts.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- device side -----------------------------------------------------------
+
+// Wait until the kernels this one depends on (programmatically) have completed
+// and their writes are visible; returns at once without such a dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel on the stream to start launching.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -12,17 +12,16 @@
 //
 // CTA = 6 warps, one per SM, persistent over (expert, token chunk, weight
 // tile) tiles built on the device from the counts:
-//   warp 0      TMA producer: 128 weight rows (FC1: 64 gate rows over the 64
-//               matching up rows, i.e. 64 activation columns per tile; FC2: 128
-//               rows of w2[e]) and the chunk's token rows (FC1: 4-row TMA
-//               gathers from `hidden`; FC2: a tiled load of the expert-sorted
-//               activation rows), 8-stage ring;
-//   warp 1      MMA issuer: tcgen05.mma M=128, N=NTOK, K=16;
-//   warps 2..5  epilogue: FC1: the two warps holding the up rows pass them
-//               through shared memory to the two warps holding the gate rows
-//               (bounded mbarrier hand-off), which form act = silu(g) * u and
-//               store bf16 activation rows; FC2: y * routing weight -> float32
-//               staging row of the slot.
+//   warp 0      TMA producer: weight rows (FC1: 128 gate rows and the matching
+//               128 up rows; FC2: 128 rows of w2[e]) and the chunk's token rows
+//               (FC1: 4-row TMA gathers from `hidden`; FC2: a tiled load of the
+//               expert-sorted activation rows), a ring of as many stages as
+//               fit in ~205 KB (5-11) to keep enough weight bytes in flight;
+//   warp 1      MMA issuer: tcgen05.mma M=128, N=NTOK, K=16 (FC1: two MMAs per
+//               step, gate and up into separate accumulators, so one TMEM lane
+//               holds the gate and up value of the same activation column);
+//   warps 2..5  epilogue: FC1 act = silu(g) * u -> bf16 act row of each token;
+//               FC2 y * routing weight -> float32 staging row of the slot.
 // All waits are bounded as in the prefill kernel.
 #include "common.cuh"
 #include "sm100_ptx.cuh"
@@ -32,7 +31,7 @@ namespace {
 
 constexpr int DM = 128;          // weight rows per tile (MMA M)
 constexpr int DK = 64;           // K per stage (one 128-byte swizzle row)
-constexpr int DSTAGES_MAX = 8;
+constexpr int DSTAGES_MAX = 12;
 constexpr int DTHREADS = 192;
 constexpr uint64_t DWAIT_NS = 2000000000ull;
 
@@ -47,7 +46,7 @@ struct DecParams {
   int E;
   int K;          // reduction length: H (FC1) or I (FC2)
   int N_out;      // output columns: I (FC1) or H (FC2)
-  int NTW;        // weight tiles per expert: I / 64 (FC1) or ceil(H / 128) (FC2)
+  int NTW;        // weight tiles per expert: ceil(I / 128) or ceil(H / 128)
   int w_rows;     // rows of one expert's weight matrix: 2I or H
   void* out;      // FC1: act bf16 [S, I]; FC2: staging f32 [S, H]
   int32_t* status;
@@ -55,16 +54,17 @@ struct DecParams {
 
 template <int MODE, int NTOK>
 struct DecCfg {
-  static constexpr int A_BYTES = DM * DK * 2;
+  static constexpr int NA = MODE == DEC_FC1 ? 2 : 1;       // weight boxes (and MMAs) per stage
+  static constexpr int A_BYTES = NA * DM * DK * 2;
   static constexpr int B_BYTES = NTOK * DK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;            // multiple of 1024
-  static constexpr int STAGES = 8;
-  static constexpr int XBUF = MODE == DEC_FC1 ? 64 * NTOK * 4 : 0;   // up-row hand-off
-  static constexpr int DSMEM = STAGES * STAGE + XBUF + 1024;
-  static constexpr int ACC_COLS = NTOK;                      // one accumulator buffer
+  static constexpr int STAGES_FIT = (205 * 1024) / STAGE;    // ring within ~205 KB of shared memory
+  static constexpr int STAGES = STAGES_FIT < 12 ? STAGES_FIT : 12;
+  static constexpr int DSMEM = STAGES * STAGE + 1024;
+  static constexpr int ACC_COLS = NA * NTOK;                 // one accumulator buffer
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
-  static_assert(STAGES <= DSTAGES_MAX && DSMEM <= 209 * 1024, "shared memory budget");
+  static_assert(STAGES >= 4 && STAGES <= DSTAGES_MAX && DSMEM <= 206 * 1024, "shared memory budget");
   static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of two");
 };
 
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   using C = DecCfg<MODE, NTOK>;
   constexpr uint32_t IDESC = ptx::idesc_bf16_f32(DM, NTOK);
   __shared__ __align__(8) uint64_t full_bar[DSTAGES_MAX], empty_bar[DSTAGES_MAX];
-  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar, xfull_bar, xempty_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ int tile_start[MOE_MAX_EXPERTS + 1];
@@ -103,8 +103,6 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   const uint32_t dsmem = (ptx::smem_u32(dsmem_raw) + 1023u) & ~1023u;
   auto sA = [&](int s) { return dsmem + (uint32_t)(s * C::STAGE); };
   auto sB = [&](int s) { return dsmem + (uint32_t)(s * C::STAGE + C::A_BYTES); };
-  // up-row hand-off buffer [NTOK][64] floats, after the ring
-  float* xbuf = reinterpret_cast<float*>(dsmem_raw + (dsmem - ptx::smem_u32(dsmem_raw)) + C::STAGES * C::STAGE);
   volatile int* abort_p = &abort_flag;
 
   if (tid == 0) {
@@ -112,8 +110,6 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&xfull_bar), 64);
-    ptx::mbar_init(ptx::smem_u32(&xempty_bar), 64);
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
       ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 128);
@@ -127,6 +123,12 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     ptx::prefetch_tmap(&tmX);
   }
   if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), C::TMEM_COLS);
+  // Programmatic dependency: FC1 follows the routing kernel, whose counts, offsets
+  // and ids it reads from here on. FC2 follows FC1 and reads only its activations
+  // (after pdl_wait in the producer); the routing outputs it reads earlier come
+  // from two launches back and are complete once FC1 has triggered.
+  if (MODE == DEC_FC1) pdl_wait();
+  pdl_trigger();
   if (warp == 2) {   // tile_start[e] = sum over e' < e of ceil(count / NTOK) * NTW
     const int per = (P.E + 31) / 32;
     const int e0 = min(P.E, lane * per), e1 = min(P.E, e0 + per);
@@ -159,13 +161,29 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     int issued_parity[C::STAGES];
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) issued_parity[s] = -1;
+    // FC2: the weight rows of the first stages of this CTA's first tile do not
+    // depend on FC1, so they are requested before waiting for its activations.
+    int pre = 0;
+    if (MODE == DEC_FC2) {
+      if ((int)blockIdx.x < total) {
+        const DecTile d = dec_tile(blockIdx.x, tile_start, P.E, P.NTW);
+        const int w0 = d.e * P.w_rows + d.wt * DM;
+        pre = KB < C::STAGES ? KB : C::STAGES;
+        if (lane == 0)
+          for (int kb = 0; kb < pre; ++kb) {     // fresh ring: stage kb is free
+            const uint32_t fb = ptx::smem_u32(&full_bar[kb]);
+            ptx::mbar_arrive_expect_tx(fb, C::STAGE);
+            ptx::tma_load_2d(sA(kb), &tmW, kb * DK, w0, fb);
+          }
+      }
+      pdl_wait();
+    }
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const DecTile d = dec_tile(t, tile_start, P.E, P.NTW);
       const int cnt = __ldg(P.counts + d.e);
       const int p0 = __ldg(P.offsets + d.e) + d.chunk * NTOK;
-      // FC1: 64 gate rows of the tile's activation columns, then the 64 matching up rows
-      const int w0 = MODE == DEC_FC1 ? d.e * P.w_rows + d.wt * 64 : d.e * P.w_rows + d.wt * DM;
-      const int w1 = w0 + P.N_out;
+      const int w0 = d.e * P.w_rows + d.wt * DM;           // FC1: gate rows; FC2: w2 rows
+      const int w1 = w0 + P.N_out;                          // FC1: matching up rows (I further)
       int rid[4] = {0, 0, 0, 0};
       if (MODE == DEC_FC1 && lane < NTOK / 4) {
         const int valid = min(NTOK, cnt - d.chunk * NTOK);
@@ -177,17 +195,20 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         }
       }
       for (int kb = 0; kb < KB; ++kb) {
+        const bool preloaded = t == (int)blockIdx.x && kb < pre;   // weights already requested
         int ok = 1;
-        if (lane == 0)
+        if (lane == 0 && !preloaded)
           ok = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, DWAIT_NS);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto producer_done;
         {
           const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
           if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(fb, C::STAGE);
-            ptx::tma_load_2d(sA(stage), &tmW, kb * DK, w0, fb);
-            if (MODE == DEC_FC1) ptx::tma_load_2d(sA(stage) + 64 * 128, &tmW, kb * DK, w1, fb);
+            if (!preloaded) {
+              ptx::mbar_arrive_expect_tx(fb, C::STAGE);
+              ptx::tma_load_2d(sA(stage), &tmW, kb * DK, w0, fb);
+            }
+            if (MODE == DEC_FC1) ptx::tma_load_2d(sA(stage) + DM * 128, &tmW, kb * DK, w1, fb);
             if (MODE == DEC_FC2) ptx::tma_load_2d(sB(stage), &tmX, kb * DK, p0, fb);
           }
           if (MODE == DEC_FC1) {
@@ -225,9 +246,12 @@ __global__ void __launch_bounds__(DTHREADS, 1)
           ptx::tc_fence_after();
           const uint32_t a0 = sA(stage), b0 = sB(stage);
 #pragma unroll
-          for (int kk = 0; kk < DK / 16; ++kk)
-            ptx::mma_bf16(d0, ptx::sdesc_k128(a0 + kk * 32), ptx::sdesc_k128(b0 + kk * 32), IDESC,
-                          (kb | kk) != 0);
+          for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint64_t bd = ptx::sdesc_k128(b0 + kk * 32);
+            ptx::mma_bf16(d0, ptx::sdesc_k128(a0 + kk * 32), bd, IDESC, (kb | kk) != 0);
+            if (MODE == DEC_FC1)
+              ptx::mma_bf16(d0 + NTOK, ptx::sdesc_k128(a0 + DM * 128 + kk * 32), bd, IDESC, (kb | kk) != 0);
+          }
           ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
           if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
         }
@@ -242,9 +266,9 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    const int row = q * 32 + lane;     // weight row within the tile
+    const int row = q * 32 + lane;     // weight row within the tile = output column offset
     int acc = 0;
-    uint32_t aph = 0, xph = 0;
+    uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const DecTile d = dec_tile(t, tile_start, P.E, P.NTW);
       if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, DWAIT_NS)) break;
@@ -252,53 +276,23 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       const int cnt = __ldg(P.counts + d.e);
       const int valid = min(NTOK, cnt - d.chunk * NTOK);
       const long p0 = (long)__ldg(P.offsets + d.e) + d.chunk * NTOK;
+      const int col = d.wt * DM + row;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::ACC_COLS);
-      bool ok = true;
-      if (MODE == DEC_FC1) {
-        // rows 0..63: gate of activation column wt*64 + row; rows 64..127: up of column wt*64 + row - 64
-        const bool up = row >= 64;
-        const int r64 = row & 63;
-        if (up && !ptx::mbar_wait(ptx::smem_u32(&xempty_bar), xph ^ 1u, abort_p, DWAIT_NS)) ok = false;
-        const int col = d.wt * 64 + r64;
 #pragma unroll
-        for (int c0 = 0; c0 < NTOK; c0 += 16) {
-          uint32_t v[16];
-          ptx::tmem_ld16(taddr + c0, v);
-          ptx::tmem_ld_wait();
-          if (up) {
-            if (ok) {
+      for (int c0 = 0; c0 < NTOK; c0 += 16) {
+        uint32_t v[16], u[16];
+        ptx::tmem_ld16(taddr + c0, v);
+        if (MODE == DEC_FC1) ptx::tmem_ld16(taddr + NTOK + c0, u);
+        ptx::tmem_ld_wait();
+        if (col < P.N_out) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) xbuf[(c0 + i) * 64 + r64] = __uint_as_float(v[i]);
-            }
-          } else {
-            if (c0 == 0 && !ptx::mbar_wait(ptx::smem_u32(&xfull_bar), xph, abort_p, DWAIT_NS)) ok = false;
-            if (ok) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int c = c0 + i;
-                if (c < valid) {
-                  const float a = silu(__uint_as_float(v[i])) * xbuf[c * 64 + r64];
-                  static_cast<__nv_bfloat16*>(P.out)[(p0 + c) * P.N_out + col] = __float2bfloat16_rn(a);
-                }
-              }
-            }
-          }
-          if (up && c0 + 16 >= NTOK && ok) ptx::mbar_arrive(ptx::smem_u32(&xfull_bar));
-        }
-        if (!up && ok) ptx::mbar_arrive(ptx::smem_u32(&xempty_bar));
-        xph ^= 1u;
-      } else {
-        const int col = d.wt * DM + row;
-#pragma unroll
-        for (int c0 = 0; c0 < NTOK; c0 += 16) {
-          uint32_t v[16];
-          ptx::tmem_ld16(taddr + c0, v);
-          ptx::tmem_ld_wait();
-          if (col < P.N_out) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int c = c0 + i;
-              if (c < valid) {
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            if (c < valid) {
+              if (MODE == DEC_FC1) {
+                const float a = silu(__uint_as_float(v[i])) * __uint_as_float(u[i]);
+                static_cast<__nv_bfloat16*>(P.out)[(p0 + c) * P.N_out + col] = __float2bfloat16_rn(a);
+              } else {
                 const float w = __ldg(P.sorted_w + p0 + c);
                 const long dst = (long)__ldg(P.reverse + p0 + c);
                 static_cast<float*>(P.out)[dst * P.N_out + col] = __uint_as_float(v[i]) * w;
@@ -307,7 +301,6 @@ __global__ void __launch_bounds__(DTHREADS, 1)
           }
         }
       }
-      if (!ok) break;
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[acc]));
       if (++acc == 2) { acc = 0; aph ^= 1u; }
@@ -340,7 +333,8 @@ int launch_dec(const CUtensorMap& w, const CUtensorMap& x, const DecParams& p, l
   const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
   if (grid <= 0) return MOE_OK;
   ProfScope ps(name, s);
-  ffn_decode_kernel<MODE, NTOK><<<grid, DTHREADS, C::DSMEM, s>>>(w, x, p);
+  const cudaError_t e = launch_pdl(ffn_decode_kernel<MODE, NTOK>, grid, DTHREADS, C::DSMEM, s, w, x, p);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
   return check_launch(name);
 }
 
@@ -349,12 +343,12 @@ int run_decode(const FfnArgs& a, cudaStream_t s) {
   const long S = (long)a.T * a.k;
   CUtensorMap w1, x1, w2, x2;
   int rc;
-  if ((rc = make_tmap(&w1, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, 64))) return rc;
+  if ((rc = make_tmap(&w1, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, DM))) return rc;
   if ((rc = make_tmap(&x1, a.hidden, (uint64_t)a.T, (uint64_t)a.H, 1))) return rc;
   if ((rc = make_tmap(&w2, a.w2, (uint64_t)a.E * a.H, (uint64_t)a.I, DM))) return rc;
   if ((rc = make_tmap(&x2, a.act, (uint64_t)S, (uint64_t)a.I, NTOK))) return rc;
   DecParams p1{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.H, a.I,
-               a.I / 64, 2 * a.I, a.act, a.status};
+               (a.I + DM - 1) / DM, 2 * a.I, a.act, a.status};
   if ((rc = launch_dec<DEC_FC1, NTOK>(w1, x1, p1, S, s, "ffn_fc1_decode"))) return rc;
   DecParams p2{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H,
                (a.H + DM - 1) / DM, a.H, a.staging, a.status};

@@ -26,6 +26,8 @@ namespace {
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
                                    const int32_t* __restrict__ offsets, int E, int H16,
                                    uint4* __restrict__ xs) {
+  pdl_wait();
+  pdl_trigger();
   const int n = __ldg(offsets + E);
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < (long)n * H16;
        i += (long)gridDim.x * blockDim.x) {
@@ -86,8 +88,10 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   int rc;
   {
     ProfScope ps("gather_rows", s);
-    gather_rows_kernel<<<num_sms() * 4, 256, 0, s>>>(static_cast<const uint4*>(a.hidden), a.sorted_ids,
-                                                     a.offsets, a.E, a.H / 8, static_cast<uint4*>(a.xs));
+    const cudaError_t e = launch_pdl(gather_rows_kernel, num_sms() * 4, 256, 0, s,
+                                     static_cast<const uint4*>(a.hidden), a.sorted_ids, a.offsets, a.E,
+                                     a.H / 8, static_cast<uint4*>(a.xs));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gather_rows: %s", cudaGetErrorString(e));
     if ((rc = check_launch("gather_rows"))) return rc;
   }
   if ((rc = make_tmap(&tA1, a.xs, (uint64_t)S, (uint64_t)a.H, 128))) return rc;

@@ -21,6 +21,9 @@
 //   empty[s]  in both CTAs; the leader's MMA commit multicasts to both;
 //   tfull[b]  in both CTAs; multicast commit after a tile's last k-step;
 //   tempty[b] leader only; one arrival per epilogue warp of both CTAs (8).
+// Launched with a programmatic dependency on the previous kernel: the prologue
+// (barriers, TMEM, tile list from the counts of the align step, which is
+// complete by then) overlaps that kernel's tail; everything after waits for it.
 // Waits are bounded as in the single-SM kernel; a cluster barrier brackets
 // the kernel so neither CTA leaves while the other may still touch its
 // shared memory.
@@ -198,6 +201,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   __syncthreads();
   cluster_sync();      // barriers of both CTAs initialised before any cross-CTA signal
   ptx::tc_fence_after();
+  pdl_wait();          // the previous kernel's output (x_sorted / act) is read from here on
+  pdl_trigger();
   const uint32_t tmem_base = tmem_slot;
   const int total = tile_start[P.E];
   const int KB = P.K / PBK;
@@ -357,7 +362,8 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const PairParams& p,
   const int grid = 2 * (int)(max_tiles < pairs ? max_tiles : pairs);
   if (grid <= 0) return MOE_OK;
   ProfScope ps(name, s);
-  ffn_tc_pair_kernel<MODE><<<grid, PTHREADS, PDSMEM, s>>>(a, b, p);
+  const cudaError_t e = launch_pdl(ffn_tc_pair_kernel<MODE>, grid, PTHREADS, PDSMEM, s, a, b, p);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
   return check_launch(name);
 }
 

@@ -78,102 +78,91 @@ __device__ __forceinline__ int warp_argmax_round(const unsigned (&key)[V], unsig
   return (int)__reduce_min_sync(0xffffffffu, cand);
 }
 
-// Top-k and softmax of one token's logits row, by the L lanes of a group
-// (lane g of the group holds experts g, g + L, ...; E <= L * V, k <= L).
-// Lane j < k of the group writes output slot j. The softmax denominator is a
-// compensated float32 sum; each weight is one correctly rounded division.
+// Top-k and softmax of one token's logits row by the L lanes of a group (V <= 64); lane
+// g holds the contiguous experts [g*V, g*V + V) (vector loads when E % 4 == 0).
+// Each of the k rounds takes the best remaining value of every lane (strictly
+// greater wins, so the lower index stays first within a lane) and merges the
+// lanes with a butterfly on (value desc, index asc). Round j's winner is
+// written to slot j by lane j % L (its raw logit first); the denominator is a
+// TwoSum-compensated float32 sum (identical in every lane), and a last pass
+// turns each slot's logit into its weight with one correctly rounded division.
 template <int L, int V>
 __device__ __forceinline__ void gate_one_token(const float* __restrict__ logits, long t, int E, int k,
                                                int norm, float* __restrict__ w_out,
                                                int32_t* __restrict__ idx_out) {
   const int g = threadIdx.x & (L - 1);
   const unsigned gm = group_mask<L>();
+  const int base = g * V;
   const float* row = logits + t * (long)E;
   float v[V];
+  if ((V % 4) == 0 && (E & 3) == 0) {
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = g + i * L;
-    v[i] = e < E ? __ldg(row + e) : 0.0f;
+    for (int q = 0; q < V / 4; ++q) {
+      const int e0 = base + 4 * q;
+      const float4 x = e0 < E ? __ldg(reinterpret_cast<const float4*>(row + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) v[i] = base + i < E ? __ldg(row + base + i) : 0.0f;
   }
-  unsigned taken = 0;
+  uint64_t taken = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i)
-    if (g + i * L >= E) taken |= 1u << i;
+    if (base + i >= E) taken |= 1ull << i;
 
-  float my_v = 0.0f, row_max = 0.0f;
-  int my_i = -1;
-  if constexpr (L == 32) {
-    unsigned key[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) key[i] = okey(v[i]);
-    for (int j = 0; j < k; ++j) {
-      unsigned m;
-      const int bi = warp_argmax_round<V>(key, taken, g, &m);
-      if ((bi & 31) == g) taken |= 1u << (bi >> 5);
-      const float bv = okey_value(m);
-      if (j == 0) row_max = bv;
-      if (g == j) { my_v = bv; my_i = bi; }
-    }
-  } else {
-    for (int j = 0; j < k; ++j) {
-      float bv = 0.0f;
-      int bi = kNone;
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const int e = g + i * L;
-        if (!((taken >> i) & 1u) && better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
-      }
-#pragma unroll
-      for (int off = L / 2; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(gm, bv, off, L);
-        const int oi = __shfl_xor_sync(gm, bi, off, L);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if ((bi & (L - 1)) == g) taken |= 1u << (bi / L);
-      if (j == 0) row_max = bv;
-      if (g == j) { my_v = bv; my_i = bi; }
-    }
-  }
-
-  // denominator: the k selected (norm) or the whole row
-  float hi = 0.0f, lo = 0.0f;
-  if (norm) {
-    if (g < k) hi = exp_diff(my_v, row_max);
-  } else {
+  float m = 0.0f, hi = 0.0f, lo = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int bi = kNone;
 #pragma unroll
     for (int i = 0; i < V; ++i)
-      if (g + i * L < E) two_sum_add(hi, lo, exp_diff(v[i], row_max));
-  }
+      if (!((taken >> i) & 1ull) && (bi == kNone || v[i] > bv)) { bv = v[i]; bi = base + i; }
 #pragma unroll
-  for (int off = L / 2; off >= 1; off >>= 1) {
-    const float ohi = __shfl_xor_sync(gm, hi, off, L);
-    const float olo = __shfl_xor_sync(gm, lo, off, L);
-    two_sum_add(hi, lo, ohi);
-    lo += olo;
+    for (int off = L / 2; off >= 1; off >>= 1) {
+      const float ov = __shfl_xor_sync(gm, bv, off, L);
+      const int oi = __shfl_xor_sync(gm, bi, off, L);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (bi / V == g) taken |= 1ull << (bi - base);
+    if (j == 0) m = bv;
+    if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
+    if ((j & (L - 1)) == g) {
+      idx_out[t * k + j] = bi;
+      w_out[t * k + j] = bv;
+    }
   }
-
-  if (g < k) {
-    const float num = exp_diff(my_v, row_max);
-    w_out[t * k + g] = __fdiv_rn(num, hi + lo);
-    idx_out[t * k + g] = my_i;
+  if (!norm) {
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (base + i < E) two_sum_add(hi, lo, exp_diff(v[i], m));
+#pragma unroll
+    for (int off = L / 2; off >= 1; off >>= 1) {
+      const float ohi = __shfl_xor_sync(gm, hi, off, L);
+      const float olo = __shfl_xor_sync(gm, lo, off, L);
+      two_sum_add(hi, lo, ohi);
+      lo += olo;
+    }
+  }
+  const float denom = hi + lo;
+  for (int j = g; j < k; j += L) {
+    const float x = w_out[t * k + j];        // this lane's own store above
+    w_out[t * k + j] = __fdiv_rn(exp_diff(x, m), denom);
   }
 }
 
 }  // namespace gate
 }  // namespace moe
 
-// Dispatch on E: L lanes per row, V = ceil(E / L) values per lane.
+// Dispatch on E: L lanes per row, V values per lane (L * V >= E).
 #define MOE_DISPATCH_LV(E, FN, ...)                                        \
   do {                                                                     \
-    if ((E) <= 1) return FN<1, 1>(__VA_ARGS__);                            \
-    if ((E) <= 2) return FN<2, 1>(__VA_ARGS__);                            \
-    if ((E) <= 4) return FN<4, 1>(__VA_ARGS__);                            \
-    if ((E) <= 8) return FN<8, 1>(__VA_ARGS__);                            \
-    if ((E) <= 16) return FN<16, 1>(__VA_ARGS__);                          \
-    if ((E) <= 32) return FN<32, 1>(__VA_ARGS__);                          \
-    if ((E) <= 64) return FN<32, 2>(__VA_ARGS__);                          \
-    if ((E) <= 128) return FN<32, 4>(__VA_ARGS__);                         \
-    if ((E) <= 256) return FN<32, 8>(__VA_ARGS__);                         \
-    if ((E) <= 512) return FN<32, 16>(__VA_ARGS__);                        \
-    return FN<32, 32>(__VA_ARGS__);                                        \
+    if ((E) <= 8) return FN<1, 8>(__VA_ARGS__);                            \
+    if ((E) <= 16) return FN<1, 16>(__VA_ARGS__);                          \
+    if ((E) <= 32) return FN<1, 32>(__VA_ARGS__);                          \
+    if ((E) <= 64) return FN<1, 64>(__VA_ARGS__);                          \
+    if ((E) <= 128) return FN<2, 64>(__VA_ARGS__);                         \
+    if ((E) <= 256) return FN<4, 64>(__VA_ARGS__);                         \
+    if ((E) <= 512) return FN<8, 64>(__VA_ARGS__);                         \
+    return FN<16, 64>(__VA_ARGS__);                                        \
   } while (0)

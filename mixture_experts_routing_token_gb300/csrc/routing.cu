@@ -31,6 +31,110 @@ __global__ void __launch_bounds__(kBlock) gating_kernel(const float* __restrict_
   gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
 }
 
+// Gating for E <= 128, one thread per token. The row is parked in shared memory
+// column-major (element i of the block's thread t at [i][t], so every access
+// pattern below is bank-conflict free) and the maxima of its groups of 8
+// experts are kept in registers. Each of the k rounds scans the group maxima,
+// takes the winner (value desc, then index asc: scans run in ascending index
+// with strict >), marks it taken (-inf; logits are finite) and rescans only the
+// winner's group. Weights as in gate::gate_one_token.
+constexpr int kSmemGateThreads = 128;
+
+template <int EP>
+__global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
+    int32_t* __restrict__ idx_out) {
+  constexpr int G = EP / 8;
+  constexpr int LD = kSmemGateThreads + 1;         // padded column stride
+  extern __shared__ float col[];                   // [EP][LD]
+  const int tid = threadIdx.x;
+  const long t0 = (long)blockIdx.x * kSmemGateThreads;
+  const int nt = (int)min((long)kSmemGateThreads, (long)T - t0);
+  // the block's rows are contiguous: coalesced 16-byte loads, transposed into shared memory
+  const float* blk = logits + t0 * (long)E;
+  if ((E & 3) == 0) {
+    const int n4 = nt * E / 4;
+    for (int f = tid; f < n4; f += kSmemGateThreads) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);
+      const int tl = (4 * f) / E, e0 = 4 * f - tl * E;
+      col[e0 * LD + tl] = q.x;
+      col[(e0 + 1) * LD + tl] = q.y;
+      col[(e0 + 2) * LD + tl] = q.z;
+      col[(e0 + 3) * LD + tl] = q.w;
+    }
+  } else {
+    for (int f = tid; f < nt * E; f += kSmemGateThreads) {
+      const int tl = f / E;
+      col[(f - tl * E) * LD + tl] = __ldg(blk + f);
+    }
+  }
+  for (int e = E; e < EP; ++e) col[e * LD + tid] = -INFINITY;
+  __syncthreads();
+  if (tid >= nt) return;
+  const long t = t0 + tid;
+  auto at = [&](int i) -> float& { return col[i * LD + tid]; };
+  float gv[G];
+  int gi[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float bv = at(8 * g);
+    int bi = 8 * g;
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float x = at(8 * g + c);
+      if (x > bv) { bv = x; bi = 8 * g + c; }
+    }
+    gv[g] = bv;
+    gi[g] = bi;
+  }
+  float m = gv[0];
+#pragma unroll
+  for (int g = 1; g < G; ++g) m = fmaxf(m, gv[g]);
+  float hi = 0.0f, lo = 0.0f;
+  if (!norm) {
+    for (int i = 0; i < E; ++i) gate::two_sum_add(hi, lo, gate::exp_diff(at(i), m));
+  }
+  for (int j = 0; j < k; ++j) {
+    float bv = gv[0];
+    int bi = gi[0], bg = 0;
+#pragma unroll
+    for (int g = 1; g < G; ++g)
+      if (gv[g] > bv) { bv = gv[g]; bi = gi[g]; bg = g; }
+    at(bi) = -INFINITY;
+    float nv = at(8 * bg);
+    int ni = 8 * bg;
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float x = at(8 * bg + c);
+      if (x > nv) { nv = x; ni = 8 * bg + c; }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (g == bg) { gv[g] = nv; gi[g] = ni; }
+    if (norm) gate::two_sum_add(hi, lo, gate::exp_diff(bv, m));
+    idx_out[t * k + j] = bi;
+    w_out[t * k + j] = bv;
+  }
+  const float denom = hi + lo;
+  for (int j = 0; j < k; ++j) w_out[t * k + j] = __fdiv_rn(gate::exp_diff(w_out[t * k + j], m), denom);
+}
+
+template <int EP>
+int launch_gating_smem(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                       cudaStream_t s) {
+  const size_t smem = (size_t)EP * (kSmemGateThreads + 1) * sizeof(float);
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    cudaFuncSetAttribute(gating_smem_kernel<EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr[dev] = true;
+  }
+  gating_smem_kernel<EP><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
+      logits, T, E, k, norm, w, idx);
+  return check_launch("gating_softmax_topk");
+}
+
 template <int L, int V>
 int launch_gating_t(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                     cudaStream_t s) {
@@ -316,6 +420,230 @@ __global__ void __launch_bounds__(kGroupWarps * 32) group_topk_kernel(
   }
 }
 
+// Lane-per-group form (n_group <= 32, group size <= 32): lane g of a group of
+// L lanes holds expert group g (contiguous, gs experts) and its bias for the
+// whole token loop; the group score is lane-local, topk_group rounds then k
+// rounds of butterfly arg-max pick groups and experts.
+template <int L, int V>
+__global__ void __launch_bounds__(kBlock) group_topk_lane_kernel(
+    const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k, int n_group,
+    int topk_group, int noaux, float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  const int g = threadIdx.x & (L - 1);
+  const unsigned gm = group_mask<L>();
+  const int gs = E / n_group;
+  const bool has = g < n_group;
+  const int base = g * gs;
+  const bool vec = (gs & 3) == 0;
+  const long step = (long)gridDim.x * (kBlock / L);
+  for (long t = (long)blockIdx.x * (kBlock / L) + threadIdx.x / L; t < T; t += step) {
+    const float* row = scores + t * (long)E + base;
+    float cv[V];
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (has && 4 * q < gs) {
+          x = __ldg(reinterpret_cast<const float4*>(row) + q);
+          if (noaux) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(bias + base) + q);
+            x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+          }
+        }
+        cv[4 * q] = x.x; cv[4 * q + 1] = x.y; cv[4 * q + 2] = x.z; cv[4 * q + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        cv[i] = (has && i < gs) ? (noaux ? __ldg(row + i) + __ldg(bias + base + i) : __ldg(row + i)) : 0.0f;
+    }
+    unsigned taken = 0;
+    float b1 = -FLT_MAX, b2 = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      if (!has || i >= gs) {
+        taken |= 1u << i;
+      } else {
+        const float x = cv[i];
+        if (x > b1) { b2 = b1; b1 = x; }
+        else if (x > b2) b2 = x;
+      }
+    }
+    const float gscore = noaux ? b1 + b2 : b1;
+    unsigned gsel = 0;
+    for (int j = 0; j < topk_group; ++j) {
+      float bv = gscore;
+      int bi = (has && !((gsel >> g) & 1u)) ? g : kNone;
+#pragma unroll
+      for (int off = L / 2; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(gm, bv, off, L);
+        const int oi = __shfl_xor_sync(gm, bi, off, L);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      gsel |= 1u << bi;
+    }
+    if (!((gsel >> g) & 1u)) taken = 0xffffffffu;
+    for (int j = 0; j < k; ++j) {
+      float bv = 0.0f;
+      int bi = kNone;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (!((taken >> i) & 1u) && (bi == kNone || cv[i] > bv)) { bv = cv[i]; bi = base + i; }
+#pragma unroll
+      for (int off = L / 2; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(gm, bv, off, L);
+        const int oi = __shfl_xor_sync(gm, bi, off, L);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (bi >= base && bi < base + gs) taken |= 1u << (bi - base);
+      if ((j & (L - 1)) == g) {
+        // noaux_tc reports the un-biased score of the chosen expert (a cached re-read)
+        w_out[t * k + j] = noaux ? __ldg(scores + t * (long)E + bi) : bv;
+        idx_out[t * k + j] = bi;
+      }
+    }
+  }
+}
+
+// Thread-per-token form for E <= 256: the choice row and the group scores live in
+// shared memory (column-major, conflict free); groups are picked by scanning
+// the group scores, experts of the other groups are set to -inf, then k rounds
+// over register maxima of 8-expert blocks as in gating_smem_kernel.
+constexpr int kSmemGroupThreads = 64;
+
+template <int EP>
+__global__ void __launch_bounds__(kSmemGroupThreads) group_topk_smem_kernel(
+    const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k, int n_group,
+    int topk_group, int noaux, float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  constexpr int B = EP / 8;
+  constexpr int LD = kSmemGroupThreads + 1;        // padded column stride
+  extern __shared__ float sm[];                    // [EP][LD] choice | [32][LD] group score
+  const int tid = threadIdx.x;
+  const long t0 = (long)blockIdx.x * kSmemGroupThreads;
+  const int nt = (int)min((long)kSmemGroupThreads, (long)T - t0);
+  const float* blk = scores + t0 * (long)E;
+  if ((E & 3) == 0) {
+    const int n4 = nt * E / 4;
+    for (int f = tid; f < n4; f += kSmemGroupThreads) {
+      float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);
+      const int tl = (4 * f) / E, e0 = 4 * f - tl * E;
+      if (noaux) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(bias + e0));
+        q.x += b.x; q.y += b.y; q.z += b.z; q.w += b.w;
+      }
+      sm[e0 * LD + tl] = q.x;
+      sm[(e0 + 1) * LD + tl] = q.y;
+      sm[(e0 + 2) * LD + tl] = q.z;
+      sm[(e0 + 3) * LD + tl] = q.w;
+    }
+  } else {
+    for (int f = tid; f < nt * E; f += kSmemGroupThreads) {
+      const int tl = f / E, e = f - tl * E;
+      sm[e * LD + tl] = noaux ? __ldg(blk + f) + __ldg(bias + e) : __ldg(blk + f);
+    }
+  }
+  for (int e = E; e < EP; ++e) sm[e * LD + tid] = -INFINITY;
+  __syncthreads();
+  if (tid >= nt) return;
+  const long t = t0 + tid;
+  auto at = [&](int i) -> float& { return sm[i * LD + tid]; };
+  auto gsc = [&](int g) -> float& { return sm[(EP + g) * LD + tid]; };
+  const float* row = scores + t * (long)E;
+  const int gs = E / n_group;
+  // group scores: max, or the float32 sum of the two largest
+  for (int g = 0; g < n_group; ++g) {
+    float b1 = -FLT_MAX, b2 = -FLT_MAX;
+    for (int c = 0; c < gs; ++c) {
+      const float x = at(g * gs + c);
+      if (x > b1) { b2 = b1; b1 = x; }
+      else if (x > b2) b2 = x;
+    }
+    gsc(g) = noaux ? b1 + b2 : b1;
+  }
+  unsigned gsel = 0;
+  for (int j = 0; j < topk_group; ++j) {
+    int bg = -1;
+    float bv = 0.0f;
+    for (int g = 0; g < n_group; ++g)
+      if (!((gsel >> g) & 1u) && (bg < 0 || gsc(g) > bv)) { bv = gsc(g); bg = g; }
+    gsel |= 1u << bg;
+  }
+  for (int g = 0; g < n_group; ++g)
+    if (!((gsel >> g) & 1u))
+      for (int c = 0; c < gs; ++c) at(g * gs + c) = -INFINITY;
+  float bvv[B];
+  int bii[B];
+#pragma unroll
+  for (int b = 0; b < B; ++b) {
+    float v = at(8 * b);
+    int i = 8 * b;
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float x = at(8 * b + c);
+      if (x > v) { v = x; i = 8 * b + c; }
+    }
+    bvv[b] = v;
+    bii[b] = i;
+  }
+  for (int j = 0; j < k; ++j) {
+    float bv = bvv[0];
+    int bi = bii[0], bb = 0;
+#pragma unroll
+    for (int b = 1; b < B; ++b)
+      if (bvv[b] > bv) { bv = bvv[b]; bi = bii[b]; bb = b; }
+    at(bi) = -INFINITY;
+    float nv = at(8 * bb);
+    int ni = 8 * bb;
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float x = at(8 * bb + c);
+      if (x > nv) { nv = x; ni = 8 * bb + c; }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+      if (b == bb) { bvv[b] = nv; bii[b] = ni; }
+    w_out[t * k + j] = noaux ? __ldg(row + bi) : bv;
+    idx_out[t * k + j] = bi;
+  }
+}
+
+template <int EP>
+int launch_group_smem(const float* scores, const float* bias, int T, int E, int k, int n_group, int topk_group,
+                      int noaux, float* w, int32_t* idx, cudaStream_t s) {
+  const size_t smem = (size_t)(EP + 32) * (kSmemGroupThreads + 1) * sizeof(float);
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    cudaFuncSetAttribute(group_topk_smem_kernel<EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr[dev] = true;
+  }
+  group_topk_smem_kernel<EP><<<(T + kSmemGroupThreads - 1) / kSmemGroupThreads, kSmemGroupThreads, smem, s>>>(
+      scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
+  return check_launch("group_limited_topk");
+}
+
+template <int L, int V>
+int launch_group_lane_t(const float* scores, const float* bias, int T, int E, int k, int n_group,
+                        int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
+  const int tpb = kBlock / L;
+  long blocks = ((long)T + tpb - 1) / tpb;
+  const long cap = (long)num_sms() * 16;
+  group_topk_lane_kernel<L, V><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
+      scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
+  return check_launch("group_limited_topk");
+}
+
+template <int V>
+int launch_group_lane_v(const float* scores, const float* bias, int T, int E, int k, int n_group,
+                        int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
+  if (n_group <= 1) return launch_group_lane_t<1, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (n_group <= 2) return launch_group_lane_t<2, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (n_group <= 4) return launch_group_lane_t<4, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (n_group <= 8) return launch_group_lane_t<8, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (n_group <= 16) return launch_group_lane_t<16, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  return launch_group_lane_t<32, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+}
+
 template <int V>
 int launch_group_t(const float* scores, const float* bias, int T, int E, int k, int n_group,
                    int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
@@ -340,6 +668,11 @@ int launch_gating(const float* logits, int T, int E, int k, int norm, float* w, 
                   cudaStream_t s) {
   if (T == 0) return MOE_OK;
   ProfScope ps("gating_softmax_topk", s);
+  if (E <= 8) return launch_gating_t<1, 8>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 16) return launch_gating_smem<16>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 32) return launch_gating_smem<32>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 64) return launch_gating_smem<64>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 128) return launch_gating_smem<128>(logits, T, E, k, norm, w, idx, s);
   MOE_DISPATCH_LV(E, launch_gating_t, logits, T, E, k, norm, w, idx, s);
 }
 
@@ -379,6 +712,13 @@ int launch_group_limited_topk(const float* scores, const float* bias, int T, int
                               int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   ProfScope ps("group_limited_topk", s);
+  const int gs = E / n_group;
+  if (E <= 64) return launch_group_smem<64>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (E <= 128) return launch_group_smem<128>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (E <= 256) return launch_group_smem<256>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (gs <= 8) return launch_group_lane_v<8>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (gs <= 16) return launch_group_lane_v<16>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  if (gs <= 32) return launch_group_lane_v<32>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 32) return launch_group_t<1>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 64) return launch_group_t<2>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 128) return launch_group_t<4>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);

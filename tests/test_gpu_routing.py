@@ -63,7 +63,8 @@ def test_gating_empty_and_single():
     _gating_case(moe, np.array([[0.5, -1.0, 3.0]], np.float32), 2, True)
 
 
-@pytest.mark.parametrize("T,E,k", [(16384, 64, 8), (37, 5, 2), (3, 1024, 32), (1000, 128, 8), (1, 4, 4)])
+@pytest.mark.parametrize("T,E,k", [(16384, 64, 8), (37, 5, 2), (37, 12, 3), (3, 1024, 32), (1000, 128, 8),
+                                   (1, 4, 4), (5000, 8, 2), (333, 320, 6)])
 def test_multihot_round_trip(T, E, k):
     moe = need_gpu()
     x = gen_logits(np.random.SeedSequence(T + E), T, E, "distinct")
@@ -216,3 +217,18 @@ def test_group_limited_topk_rejects_bad_arguments():
         moe.moe_group_limited_topk(x, 8, 8, 4, "noaux_tc")          # no bias
     with pytest.raises(moe.MoeError):
         moe.moe_group_limited_topk(x, 100, 8, 1)                    # k > topk_group * group size
+
+
+def test_converter_backward_on_dense_gradient():
+    """The converter's backward is the inverse kernel applied to the upstream gradient
+    (Megatron-LM IndicesToMultihot.backward); checked with a dense gradient."""
+    moe = need_gpu()
+    T, E, k = 3000, 64, 8
+    x = gen_logits(np.random.SeedSequence(77), T, E, "distinct")
+    w, i = gating.softmax_topk(x, k, True)
+    _, _, pos = multihot.indices_to_multihot(i, w, E)
+    grad = np.random.default_rng(6).standard_normal((T, E)).astype(np.float32)
+    ref, _ = multihot.multihot_to_indices(grad, pos, k)
+    got, _ = moe.moe_multihot_to_indices(torch.from_numpy(grad).to(DEV), torch.from_numpy(pos).to(DEV), k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got.cpu().numpy(), ref)

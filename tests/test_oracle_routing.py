@@ -95,3 +95,19 @@ def test_align_drops_invalid_slots():
 def test_align_empty():
     al = align.align_by_expert(np.zeros((0, 2), np.int32), np.zeros((0, 2), np.float32), 4)
     assert al["counts"].tolist() == [0, 0, 0, 0] and al["offsets"].tolist() == [0] * 5
+
+
+def test_converter_backward_is_the_inverse_map_on_the_gradient():
+    """Megatron-LM IndicesToMultihot.backward: grad of probs_in_multihot -> grad of the
+    [T, k] probs through the saved position map. Pinned against torch autograd of the
+    forward scatter (a library differentiation, independent of the oracle)."""
+    import torch
+    x = gen_logits(np.random.SeedSequence(41), 50, 12, "distinct")
+    w, i = gating.softmax_topk(x, 3, True)
+    _, _, pos = multihot.indices_to_multihot(i, w, 12)
+    grad = np.random.default_rng(5).standard_normal((50, 12)).astype(np.float32)   # dense upstream grad
+    probs = torch.tensor(w, requires_grad=True)
+    pm = torch.zeros((50, 12)).scatter(1, torch.tensor(i, dtype=torch.int64), probs)
+    pm.backward(torch.tensor(grad))
+    got, _ = multihot.multihot_to_indices(grad, pos, 3)
+    np.testing.assert_array_equal(got, probs.grad.numpy())
