@@ -289,16 +289,35 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
                      sorted_ids, sorted_w, reverse, status, sm);
 }
 
-// Small batches (all routed slots in one align chunk): gating and align in one
-// CTA and one launch. Groups of L lanes gate the tokens, the CTA synchronises,
-// then ranks and scatters the slots it has just written.
+// Small batches (at most kStageRows tokens, all routed slots in one align
+// chunk): gating and align in one CTA and one launch. For E <= 128 the CTA
+// stages the logits rows in shared memory and one thread per token runs the
+// staged top-k (gate::topk_staged_row); wider rows take a warp per token
+// (gate::gate_one_token). After a barrier the CTA ranks and scatters the slots
+// it has just written.
+template <int EP>
+__global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
+    const float* logits, int T, int E, int k, int norm, float* w_out, int32_t* idx_out,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
+  extern __shared__ int sm[];
+  pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
+  float* col = reinterpret_cast<float*>(sm);
+  gate::stage_rows<EP>(logits, 0, T, E, col, threadIdx.x, kThreads);
+  __syncthreads();
+  if ((int)threadIdx.x < T) gate::topk_staged_row<EP>(col, threadIdx.x, threadIdx.x, E, k, norm, w_out, idx_out);
+  __syncthreads();
+  align_chunk<true>(0, idx_out, w_out, (long)T * k, k, E, 1, 0, nullptr, counts, offsets, sorted_ids,
+                    sorted_w, reverse, status, sm + EP * gate::kStageLd);
+}
+
 template <int L, int V>
 __global__ void __launch_bounds__(kThreads) route_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int norm, float* w_out, int32_t* idx_out,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
   extern __shared__ int sm[];
-  pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
+  pdl_trigger();
   constexpr int groups = kThreads / L;
   for (long t = threadIdx.x / L; t < T; t += groups)
     gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
@@ -307,42 +326,65 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(
                     sorted_w, reverse, status, sm);
 }
 
-template <int L, int V>
-int launch_route_small_t(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
-                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
-                         int32_t* reverse, int32_t* status, cudaStream_t s) {
-  const size_t smem = align_smem_bytes(E);
-  static bool attr[64] = {};
+template <typename Kernel>
+int launch_route_small_k(Kernel kernel, size_t smem, size_t smem_max, const float* logits, int T, int E,
+                         int k, int norm, float* w, int32_t* idx, int32_t* counts, int32_t* offsets,
+                         int32_t* sorted_ids, float* sorted_w, int32_t* reverse, int32_t* status,
+                         cudaStream_t s, bool* attr) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
-    cudaFuncSetAttribute(route_small_kernel<L, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)align_smem_bytes(MOE_MAX_EXPERTS));
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
     attr[dev] = true;
   }
   ProfScope ps("route_small", s);
-  route_small_kernel<L, V><<<1, kThreads, smem, s>>>(logits, T, E, k, norm, w, idx, counts, offsets,
-                                                    sorted_ids, sorted_w, reverse, status);
+  kernel<<<1, kThreads, smem, s>>>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w,
+                                   reverse, status);
   return check_launch("route_small");
+}
+
+template <int EP>
+int launch_route_staged(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
+                        int32_t* reverse, int32_t* status, cudaStream_t s) {
+  static bool attr[64] = {};
+  const size_t stage = (size_t)EP * gate::kStageLd * sizeof(float);
+  return launch_route_small_k(route_small_staged_kernel<EP>, stage + align_smem_bytes(E),
+                              stage + align_smem_bytes(EP), logits, T, E, k, norm, w, idx, counts, offsets,
+                              sorted_ids, sorted_w, reverse, status, s, attr);
+}
+
+template <int V>
+int launch_route_warp(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                      int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
+                      int32_t* reverse, int32_t* status, cudaStream_t s) {
+  static bool attr[64] = {};
+  return launch_route_small_k(route_small_kernel<32, V>, align_smem_bytes(E), align_smem_bytes(MOE_MAX_EXPERTS),
+                              logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse,
+                              status, s, attr);
 }
 
 }  // namespace
 
-bool route_fits_one_chunk(int T, int k) { return (long)T * k <= kChunk; }
+bool route_is_small(int T, int k) { return T <= gate::kStageRows && (long)T * k <= kChunk; }
 
 int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                        int32_t* reverse, int32_t* status, cudaStream_t s) {
-  // a whole warp per token: few tokens, so the per-token latency matters
-#define MOE_ROUTE_SMALL(V) \
-  return launch_route_small_t<32, V>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, status, s)
-  if (E <= 32) MOE_ROUTE_SMALL(1);
-  if (E <= 64) MOE_ROUTE_SMALL(2);
-  if (E <= 128) MOE_ROUTE_SMALL(4);
-  if (E <= 256) MOE_ROUTE_SMALL(8);
-  if (E <= 512) MOE_ROUTE_SMALL(16);
-  MOE_ROUTE_SMALL(32);
-#undef MOE_ROUTE_SMALL
+#define MOE_ROUTE_STAGED(EP) \
+  return launch_route_staged<EP>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, status, s)
+#define MOE_ROUTE_WARP(V) \
+  return launch_route_warp<V>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, status, s)
+  if (E <= 8) MOE_ROUTE_STAGED(8);
+  if (E <= 16) MOE_ROUTE_STAGED(16);
+  if (E <= 32) MOE_ROUTE_STAGED(32);
+  if (E <= 64) MOE_ROUTE_STAGED(64);
+  if (E <= 128) MOE_ROUTE_STAGED(128);
+  if (E <= 256) MOE_ROUTE_WARP(8);
+  if (E <= 512) MOE_ROUTE_WARP(16);
+  MOE_ROUTE_WARP(32);
+#undef MOE_ROUTE_STAGED
+#undef MOE_ROUTE_WARP
 }
 
 size_t align_scratch_bytes(int S, int E) {

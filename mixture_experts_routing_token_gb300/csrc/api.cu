@@ -370,7 +370,7 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
   const AlignWs al = carve_align(c, S, E);
   const FfnWs fw = carve_ffn(c, dtype, S, H, I);
 
-  if (route_fits_one_chunk(T, k)) {
+  if (route_is_small(T, k)) {
     if ((rc = launch_route_small(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, al.counts, al.offsets,
                                  al.sorted_ids, al.sorted_w, al.reverse, status, s)))
       return rc;

@@ -57,8 +57,9 @@ int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E
                                float* probs, int32_t* idx, cudaStream_t s);
 
 size_t align_scratch_bytes(int S, int E);
-// Gating + align in one single-CTA launch, for T*k within one align chunk.
-bool route_fits_one_chunk(int T, int k);
+// Gating + align in one single-CTA launch, for at most 128 tokens whose T*k
+// slots fit one align chunk.
+bool route_is_small(int T, int k);
 int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                        int32_t* reverse, int32_t* status, cudaStream_t s);
@@ -92,10 +93,12 @@ int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 // Token-count threshold at or below which the weight-streaming decode kernels run.
 constexpr int kDecodeMaxTokens = 64;
 int launch_ffn_decode(const FfnArgs& a, cudaStream_t s);
-// FC1 and FC2 on 2-SM clusters (tcgen05 cta_group::2), given the four tensor
-// maps (A: 128-row boxes of x_sorted / act; B: 128-row boxes of w13 / w2).
+// FC1 and FC2 on 2-SM clusters (tcgen05 cta_group::2), given the five tensor
+// maps (A: 128-row boxes of x_sorted / act; B: 128-row boxes of w13 / w2;
+// S2: 32-row boxes of act for FC2's swapped remainder tiles).
 int launch_ffn_pair_gemms(const FfnArgs& a, const CUtensorMap& tA1, const CUtensorMap& tB1,
-                          const CUtensorMap& tA2, const CUtensorMap& tB2, cudaStream_t s);
+                          const CUtensorMap& tA2, const CUtensorMap& tB2, const CUtensorMap& tS2,
+                          cudaStream_t s);
 
 bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);

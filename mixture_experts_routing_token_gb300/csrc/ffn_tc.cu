@@ -84,7 +84,7 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   const long S = (long)a.T * a.k;
   if (S == 0) return MOE_OK;
   if (a.T <= kDecodeMaxTokens) return launch_ffn_decode(a, s);
-  CUtensorMap tA1, tB1, tA2, tB2;
+  CUtensorMap tA1, tB1, tA2, tB2, tS2;
   int rc;
   {
     ProfScope ps("gather_rows", s);
@@ -98,8 +98,9 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   if ((rc = make_tmap(&tB1, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, 128))) return rc;
   if ((rc = make_tmap(&tA2, a.act, (uint64_t)S, (uint64_t)a.I, 128))) return rc;
   if ((rc = make_tmap(&tB2, a.w2, (uint64_t)a.E * a.H, (uint64_t)a.I, 128))) return rc;
+  if ((rc = make_tmap(&tS2, a.act, (uint64_t)S, (uint64_t)a.I, 32))) return rc;
 
-  if ((rc = launch_ffn_pair_gemms(a, tA1, tB1, tA2, tB2, s))) return rc;
+  if ((rc = launch_ffn_pair_gemms(a, tA1, tB1, tA2, tB2, tS2, s))) return rc;
   return launch_combine(a.staging, a.T, a.k, a.H, a.dtype, a.out, s);
 }
 

@@ -14,6 +14,16 @@
 // for the same tensor work, which is what lets a 6-stage ring hide the
 // L2 -> shared-memory latency.
 //
+// Swapped remainder tiles (FC2). An expert's last tile of at most kSwapMax
+// rows would waste most of a 256-row M tile, so FC2 runs it with the operands
+// swapped: A = 256 rows of w2[e] (128 per SM: output features), B = the
+// leftover act rows (N = 64 or 128, half of them per SM), D = features x
+// tokens in TMEM; the epilogue writes staging columns. Measured 2-16% faster
+// FC2 launches on ragged counts. FC1 keeps plain tiles: its swapped form
+// needs two passes over K (gate, then up rows), so it issues as many k-steps
+// per feature as the plain tile, and those k-steps, bounded by the ring's
+// latency rather than by the MMA, measured no faster.
+//
 // Synchronisation:
 //   full[s]   leader CTA only; the leader's producer posts the pair's bytes
 //             (2 x 32 KB) and both CTAs' TMA loads complete on it
@@ -45,6 +55,8 @@ constexpr int PTHREADS = 192;
 constexpr uint32_t PTMEM_COLS = 2 * PBN;
 constexpr uint64_t PWAIT_NS = 2000000000ull;
 constexpr uint32_t PIDESC = ptx::idesc_bf16_f32(2 * PBM, PBN);
+constexpr int kSwapMax = 128;           // FC2 remainders up to this many rows take a swapped tile
+constexpr int kSwapBox = 32;            // token rows per TMA box of a swapped tile's B operand
 
 enum { PAIR_FC1 = 0, PAIR_FC2 = 1 };
 
@@ -57,6 +69,7 @@ struct PairParams {
   int K;          // H (FC1) or I (FC2)
   int N_out;      // I (FC1) or H (FC2)
   int NT;         // N tiles per expert
+  int NTs;        // swapped tiles per expert remainder (256 output features each; 0: none)
   int b_rows;     // 2I (FC1) or H (FC2)
   void* out;
   int32_t* status;
@@ -113,20 +126,45 @@ __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
 
 struct PTile {
   int e, m_tile, n_tile;
+  int swap_n;     // 0: a 256-row tile; 64 or 128: a swapped tile with this many token columns
 };
 
-__device__ __forceinline__ PTile ptile(int t, const int* tile_start, int E, int NT) {
+// Token columns of the swapped remainder tile of an expert with cnt rows, 0 when
+// it has none (no swapped tiles at all when NTs == 0).
+__host__ __device__ __forceinline__ int swap_cols(int cnt, int NTs) {
+  const int rem = cnt % (2 * PBM);
+  return (NTs == 0 || rem == 0 || rem > kSwapMax) ? 0 : (rem <= 64 ? 64 : 128);
+}
+// 256-row tiles of an expert with cnt rows (a remainder without a swapped tile gets one too).
+__host__ __device__ __forceinline__ int full_mtiles(int cnt, int NTs) {
+  return cnt / (2 * PBM) + (cnt % (2 * PBM) != 0 && swap_cols(cnt, NTs) == 0 ? 1 : 0);
+}
+__host__ __device__ __forceinline__ int expert_tiles(int cnt, int NT, int NTs) {
+  return full_mtiles(cnt, NTs) * NT + (swap_cols(cnt, NTs) ? NTs : 0);
+}
+
+// Tile t of the list: the expert's 256-row tiles N-tile-major, then its swapped tiles.
+__device__ __forceinline__ PTile ptile(int t, const int* tile_start, const int32_t* counts, int E, int NT,
+                                       int NTs) {
   int lo = 0, hi = E;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
   }
   const int local = t - tile_start[lo];
-  const int mt = (tile_start[lo + 1] - tile_start[lo]) / NT;
+  const int cnt = __ldg(counts + lo);
+  const int mt = full_mtiles(cnt, NTs);
   PTile d;
   d.e = lo;
-  d.n_tile = local / mt;
-  d.m_tile = local - d.n_tile * mt;
+  if (local < mt * NT) {
+    d.n_tile = local / mt;
+    d.m_tile = local - d.n_tile * mt;
+    d.swap_n = 0;
+  } else {
+    d.n_tile = local - mt * NT;
+    d.m_tile = mt;
+    d.swap_n = swap_cols(cnt, NTs);
+  }
   return d;
 }
 
@@ -138,7 +176,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const PairParams P) {
+                       const __grid_constant__ CUtensorMap tmS, const PairParams P) {
   __shared__ __align__(8) uint64_t full_bar[PSTAGES], empty_bar[PSTAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_slot;
@@ -171,6 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmS);
   }
   if (warp == 1) {   // both CTAs of the pair allocate together
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -179,11 +218,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
-  if (warp == 2) {   // tile_start[e] = sum over e' < e of ceil(count / 256) * NT
+  if (warp == 2) {   // tile_start[e] = sum over e' < e of the tiles of expert e'
     const int per = (P.E + 31) / 32;
     const int e0 = min(P.E, lane * per), e1 = min(P.E, e0 + per);
     int run = 0;
-    for (int e = e0; e < e1; ++e) run += (__ldg(P.counts + e) + 2 * PBM - 1) / (2 * PBM) * P.NT;
+    for (int e = e0; e < e1; ++e) run += expert_tiles(__ldg(P.counts + e), P.NT, P.NTs);
     int incl = run;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -193,7 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     int acc = incl - run;
     for (int e = e0; e < e1; ++e) {
       tile_start[e] = acc;
-      acc += (__ldg(P.counts + e) + 2 * PBM - 1) / (2 * PBM) * P.NT;
+      acc += expert_tiles(__ldg(P.counts + e), P.NT, P.NTs);
     }
     if (lane == 31) tile_start[P.E] = incl;
   }
@@ -213,7 +252,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       int stage = 0;
       uint32_t ph = 0;
       for (int t = cluster_id; t < total; t += nclusters) {
-        const PTile ti = ptile(t, tile_start, P.E, P.NT);
+        const PTile ti = ptile(t, tile_start, P.counts, P.E, P.NT, P.NTs);
+        if (MODE == PAIR_FC2 && ti.swap_n) {
+          // A: 128 rows of w2[e] per SM; B: this SM's half of the act rows, in boxes of kSwapBox rows
+          const int half = ti.swap_n / 2;
+          const int tok_row = __ldg(P.offsets + ti.e) + ti.m_tile * (2 * PBM) + (int)rank * half;
+          const int w_row = ti.e * P.b_rows + ti.n_tile * (2 * PBM) + (int)rank * PBM;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, PWAIT_NS)) goto producer_done;
+            const uint32_t fb_local = ptx::smem_u32(&full_bar[stage]);
+            if (leader) ptx::mbar_arrive_expect_tx(fb_local, 2 * (PA_BYTES + half * PBK * 2));
+            const uint32_t fb = map_to_rank(fb_local, 0);
+            tma_load_2d_pair(sA(stage), &tmB, kb * PBK, w_row, fb);
+            for (int b = 0; b < half; b += kSwapBox)
+              tma_load_2d_pair(sB(stage) + (uint32_t)(b * PBK * 2), &tmS, kb * PBK, tok_row + b, fb);
+            if (++stage == PSTAGES) { stage = 0; ph ^= 1u; }
+          }
+          continue;
+        }
         const int a_row = __ldg(P.offsets + ti.e) + ti.m_tile * (2 * PBM) + (int)rank * PBM;
         int b_row;
         if (MODE == PAIR_FC1) b_row = ti.e * P.b_rows + ti.n_tile * 128 + (leader ? 0 : P.N_out);
@@ -236,10 +292,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       int stage = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       for (int t = cluster_id; t < total; t += nclusters) {
+        const PTile ti = ptile(t, tile_start, P.counts, P.E, P.NT, P.NTs);
+        const uint32_t idesc = ti.swap_n ? ptx::idesc_bf16_f32(2 * PBM, ti.swap_n) : PIDESC;
         if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aph ^ 1u, abort_p, PWAIT_NS)) break;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
         bool ok = true;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
         for (int kb = 0; kb < KB; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, PWAIT_NS)) {
             ok = false;
@@ -249,7 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           const uint32_t a0 = sA(stage), b0 = sB(stage);
 #pragma unroll
           for (int kk = 0; kk < PBK / 16; ++kk)
-            mma_pair(d_tmem, ptx::sdesc_k128(a0 + kk * 32), ptx::sdesc_k128(b0 + kk * 32), PIDESC,
+            mma_pair(d_tmem, ptx::sdesc_k128(a0 + kk * 32), ptx::sdesc_k128(b0 + kk * 32), idesc,
                      (kb | kk) != 0);
           commit_pair(ptx::smem_u32(&empty_bar[stage]), 0x3);
           if (++stage == PSTAGES) { stage = 0; ph ^= 1u; }
@@ -269,10 +327,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int t = cluster_id; t < total; t += nclusters) {
-      const PTile ti = ptile(t, tile_start, P.E, P.NT);
+      const PTile ti = ptile(t, tile_start, P.counts, P.E, P.NT, P.NTs);
       if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, PWAIT_NS)) break;
       ptx::tc_fence_after();
       const int cnt = __ldg(P.counts + ti.e);
+      if (MODE == PAIR_FC2 && ti.swap_n) {
+        // lane = output feature f of this SM's 128; TMEM column j = act row r0 + j
+        const int r0 = ti.m_tile * (2 * PBM);
+        const long p0 = (long)__ldg(P.offsets + ti.e) + r0;
+        const int f = ti.n_tile * (2 * PBM) + (int)rank * PBM + row;
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PBN);
+        const int H = P.N_out;
+        float* staging = static_cast<float*>(P.out);
+#pragma unroll 1
+        for (int c = 0; c < ti.swap_n / 32; ++c) {
+          uint32_t y[32];
+          ptx::tmem_ld32(taddr + c * 32, y);
+          ptx::tmem_ld_wait();
+          const bool vl = r0 + c * 32 + lane < cnt;   // lane l fetches row c*32 + l's weight and slot
+          const float wl = vl ? __ldg(P.sorted_w + p0 + c * 32 + lane) : 0.0f;
+          const int sl = vl ? __ldg(P.reverse + p0 + c * 32 + lane) : 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wl, j);
+            const int sj = __shfl_sync(0xffffffffu, sl, j);
+            if (r0 + c * 32 + j < cnt && f < H) staging[(long)sj * H + f] = __uint_as_float(y[j]) * wj;
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_remote(map_to_rank(ptx::smem_u32(&tempty_bar[acc]), 0));
+        if (++acc == 2) { acc = 0; aph ^= 1u; }
+        continue;
+      }
       const int r = ti.m_tile * (2 * PBM) + (int)rank * PBM + row;
       const bool valid = r < cnt;
       const long p = (long)__ldg(P.offsets + ti.e) + r;
@@ -346,8 +433,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
 }
 
 template <int MODE>
-int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const PairParams& p, long S, cudaStream_t s,
-                const char* name) {
+int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sw, const PairParams& p, long S,
+                cudaStream_t s, const char* name) {
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -362,7 +449,7 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const PairParams& p,
   const int grid = 2 * (int)(max_tiles < pairs ? max_tiles : pairs);
   if (grid <= 0) return MOE_OK;
   ProfScope ps(name, s);
-  const cudaError_t e = launch_pdl(ffn_tc_pair_kernel<MODE>, grid, PTHREADS, PDSMEM, s, a, b, p);
+  const cudaError_t e = launch_pdl(ffn_tc_pair_kernel<MODE>, grid, PTHREADS, PDSMEM, s, a, b, sw, p);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
   return check_launch(name);
 }
@@ -370,15 +457,16 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const PairParams& p,
 }  // namespace
 
 int launch_ffn_pair_gemms(const FfnArgs& a, const CUtensorMap& tA1, const CUtensorMap& tB1,
-                          const CUtensorMap& tA2, const CUtensorMap& tB2, cudaStream_t s) {
+                          const CUtensorMap& tA2, const CUtensorMap& tB2, const CUtensorMap& tS2,
+                          cudaStream_t s) {
   const long S = (long)a.T * a.k;
-  PairParams p1{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.H, a.I, (a.I + 127) / 128,
+  PairParams p1{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.H, a.I, (a.I + 127) / 128, 0,
                 2 * a.I, a.act, a.status};
-  int rc = launch_pair<PAIR_FC1>(tA1, tB1, p1, S, s, "ffn_fc1_tc");
+  int rc = launch_pair<PAIR_FC1>(tA1, tB1, tA1, p1, S, s, "ffn_fc1_tc");   // (no swapped tiles: tmS unused)
   if (rc) return rc;
   PairParams p2{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.I, a.H, (a.H + PBN - 1) / PBN,
-                a.H, a.staging, a.status};
-  return launch_pair<PAIR_FC2>(tA2, tB2, p2, S, s, "ffn_fc2_tc");
+                (a.H + 2 * PBM - 1) / (2 * PBM), a.H, a.staging, a.status};
+  return launch_pair<PAIR_FC2>(tA2, tB2, tS2, p2, S, s, "ffn_fc2_tc");
 }
 
 }  // namespace moe

@@ -151,6 +151,97 @@ __device__ __forceinline__ void gate_one_token(const float* __restrict__ logits,
   }
 }
 
+// ---- thread-per-token top-k over rows parked in shared memory (E <= EP <= 128)
+//
+// A block of up to kStageRows rows is stored column-major, element e of row r at
+// col[e * kStageLd + r] (padded stride: every access below is bank-conflict
+// free). The thread of row r keeps the maxima of its groups of 8 experts in
+// registers; each of the k rounds scans the group maxima, takes the winner
+// (value desc, then index asc: scans run in ascending index with strict >),
+// marks it taken (-inf; logits are finite) and rescans only the winner's group.
+// Weights as in gate_one_token.
+constexpr int kStageRows = 128;
+constexpr int kStageLd = kStageRows + 1;
+
+// Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into col[EP][kStageLd],
+// experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows); the
+// caller synchronises before reading.
+template <int EP>
+__device__ __forceinline__ void stage_rows(const float* __restrict__ logits, long t0, int nt, int E,
+                                           float* col, int tid, int nthr) {
+  const float* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
+  if ((E & 3) == 0) {
+    const int n4 = nt * E / 4;
+    for (int f = tid; f < n4; f += nthr) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);
+      const int tl = (4 * f) / E, e0 = 4 * f - tl * E;
+      col[e0 * kStageLd + tl] = q.x;
+      col[(e0 + 1) * kStageLd + tl] = q.y;
+      col[(e0 + 2) * kStageLd + tl] = q.z;
+      col[(e0 + 3) * kStageLd + tl] = q.w;
+    }
+  } else {
+    for (int f = tid; f < nt * E; f += nthr) {
+      const int tl = f / E;
+      col[(f - tl * E) * kStageLd + tl] = __ldg(blk + f);
+    }
+  }
+  if (tid < kStageRows)
+    for (int e = E; e < EP; ++e) col[e * kStageLd + tid] = -INFINITY;
+}
+
+// Top-k and softmax of staged row r (called by one thread), written as token t.
+template <int EP>
+__device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E, int k, int norm,
+                                                float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  constexpr int G = EP / 8;
+  auto at = [&](int i) -> float& { return col[i * kStageLd + r]; };
+  float gv[G];
+  int gi[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float bv = at(8 * g);
+    int bi = 8 * g;
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float x = at(8 * g + c);
+      if (x > bv) { bv = x; bi = 8 * g + c; }
+    }
+    gv[g] = bv;
+    gi[g] = bi;
+  }
+  float m = gv[0];
+#pragma unroll
+  for (int g = 1; g < G; ++g) m = fmaxf(m, gv[g]);
+  float hi = 0.0f, lo = 0.0f;
+  if (!norm) {
+    for (int i = 0; i < E; ++i) two_sum_add(hi, lo, exp_diff(at(i), m));
+  }
+  for (int j = 0; j < k; ++j) {
+    float bv = gv[0];
+    int bi = gi[0], bg = 0;
+#pragma unroll
+    for (int g = 1; g < G; ++g)
+      if (gv[g] > bv) { bv = gv[g]; bi = gi[g]; bg = g; }
+    at(bi) = -INFINITY;
+    float nv = at(8 * bg);
+    int ni = 8 * bg;
+#pragma unroll
+    for (int c = 1; c < 8; ++c) {
+      const float x = at(8 * bg + c);
+      if (x > nv) { nv = x; ni = 8 * bg + c; }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (g == bg) { gv[g] = nv; gi[g] = ni; }
+    if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
+    idx_out[t * k + j] = bi;
+    w_out[t * k + j] = bv;
+  }
+  const float denom = hi + lo;
+  for (int j = 0; j < k; ++j) w_out[t * k + j] = __fdiv_rn(exp_diff(w_out[t * k + j], m), denom);
+}
+
 }  // namespace gate
 }  // namespace moe
 

@@ -31,98 +31,27 @@ __global__ void __launch_bounds__(kBlock) gating_kernel(const float* __restrict_
   gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
 }
 
-// Gating for E <= 128, one thread per token. The row is parked in shared memory
-// column-major (element i of the block's thread t at [i][t], so every access
-// pattern below is bank-conflict free) and the maxima of its groups of 8
-// experts are kept in registers. Each of the k rounds scans the group maxima,
-// takes the winner (value desc, then index asc: scans run in ascending index
-// with strict >), marks it taken (-inf; logits are finite) and rescans only the
-// winner's group. Weights as in gate::gate_one_token.
-constexpr int kSmemGateThreads = 128;
+// Gating for E <= 128, one thread per token: each CTA stages its 128 rows in
+// shared memory and runs gate::topk_staged_row on them (gating_device.cuh).
+constexpr int kSmemGateThreads = gate::kStageRows;
 
 template <int EP>
 __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
     const float* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
     int32_t* __restrict__ idx_out) {
-  constexpr int G = EP / 8;
-  constexpr int LD = kSmemGateThreads + 1;         // padded column stride
-  extern __shared__ float col[];                   // [EP][LD]
+  extern __shared__ float col[];                   // [EP][kStageLd]
   const int tid = threadIdx.x;
   const long t0 = (long)blockIdx.x * kSmemGateThreads;
   const int nt = (int)min((long)kSmemGateThreads, (long)T - t0);
-  // the block's rows are contiguous: coalesced 16-byte loads, transposed into shared memory
-  const float* blk = logits + t0 * (long)E;
-  if ((E & 3) == 0) {
-    const int n4 = nt * E / 4;
-    for (int f = tid; f < n4; f += kSmemGateThreads) {
-      const float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);
-      const int tl = (4 * f) / E, e0 = 4 * f - tl * E;
-      col[e0 * LD + tl] = q.x;
-      col[(e0 + 1) * LD + tl] = q.y;
-      col[(e0 + 2) * LD + tl] = q.z;
-      col[(e0 + 3) * LD + tl] = q.w;
-    }
-  } else {
-    for (int f = tid; f < nt * E; f += kSmemGateThreads) {
-      const int tl = f / E;
-      col[(f - tl * E) * LD + tl] = __ldg(blk + f);
-    }
-  }
-  for (int e = E; e < EP; ++e) col[e * LD + tid] = -INFINITY;
+  gate::stage_rows<EP>(logits, t0, nt, E, col, tid, kSmemGateThreads);
   __syncthreads();
-  if (tid >= nt) return;
-  const long t = t0 + tid;
-  auto at = [&](int i) -> float& { return col[i * LD + tid]; };
-  float gv[G];
-  int gi[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float bv = at(8 * g);
-    int bi = 8 * g;
-#pragma unroll
-    for (int c = 1; c < 8; ++c) {
-      const float x = at(8 * g + c);
-      if (x > bv) { bv = x; bi = 8 * g + c; }
-    }
-    gv[g] = bv;
-    gi[g] = bi;
-  }
-  float m = gv[0];
-#pragma unroll
-  for (int g = 1; g < G; ++g) m = fmaxf(m, gv[g]);
-  float hi = 0.0f, lo = 0.0f;
-  if (!norm) {
-    for (int i = 0; i < E; ++i) gate::two_sum_add(hi, lo, gate::exp_diff(at(i), m));
-  }
-  for (int j = 0; j < k; ++j) {
-    float bv = gv[0];
-    int bi = gi[0], bg = 0;
-#pragma unroll
-    for (int g = 1; g < G; ++g)
-      if (gv[g] > bv) { bv = gv[g]; bi = gi[g]; bg = g; }
-    at(bi) = -INFINITY;
-    float nv = at(8 * bg);
-    int ni = 8 * bg;
-#pragma unroll
-    for (int c = 1; c < 8; ++c) {
-      const float x = at(8 * bg + c);
-      if (x > nv) { nv = x; ni = 8 * bg + c; }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (g == bg) { gv[g] = nv; gi[g] = ni; }
-    if (norm) gate::two_sum_add(hi, lo, gate::exp_diff(bv, m));
-    idx_out[t * k + j] = bi;
-    w_out[t * k + j] = bv;
-  }
-  const float denom = hi + lo;
-  for (int j = 0; j < k; ++j) w_out[t * k + j] = __fdiv_rn(gate::exp_diff(w_out[t * k + j], m), denom);
+  if (tid < nt) gate::topk_staged_row<EP>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
 }
 
 template <int EP>
 int launch_gating_smem(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
-  const size_t smem = (size_t)EP * (kSmemGateThreads + 1) * sizeof(float);
+  const size_t smem = (size_t)EP * gate::kStageLd * sizeof(float);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

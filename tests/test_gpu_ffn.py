@@ -32,6 +32,7 @@ def _full_check(moe, d):
     ref = ffn.layer_forward(d["logits"], d["hidden"], d["w13"], d["w2"], d["k"], d["norm_topk_prob"],
                             d["dtype"])
     np.testing.assert_array_equal(ti.cpu().numpy(), ref["topk_indices"])
+    np.testing.assert_allclose(tw.cpu().numpy(), ref["topk_weights"], rtol=1e-6, atol=0)
     assert_close_rel_max(to_np64(out), ref["out"], layer_tolerance(d["dtype"]), "layer out")
 
 
@@ -56,6 +57,10 @@ def test_decode_workloads_full(name):
     (513, 320, 640, 5, 3, True),        # H % 256 == 64: partial FC2 N tile
     (2048, 1024, 512, 64, 8, False),
     (257, 128, 128, 128, 8, True),      # many empty experts
+    (128, 128, 256, 128, 8, True),      # largest batch of the one-launch routing, E = 128
+    (100, 128, 128, 256, 8, False),     # one-launch routing with a warp per token (E > 128)
+    (129, 256, 128, 64, 8, True),       # first batch size past the one-launch routing
+    (90, 192, 192, 12, 3, False),       # E % 4 != 0: scalar row staging
 ])
 def test_layer_tensor_core_shapes(T, H, I, E, k, norm):
     moe = need_gpu()
@@ -103,6 +108,35 @@ def test_grouped_ffn_entry_point_with_oracle_routing():
     ref = ffn.grouped_ffn(d["hidden"], d["w13"], d["w2"], "bf16", 3, al["counts"], al["offsets"],
                           al["sorted_token_ids"], al["sorted_weights"], al["reverse_indices"])
     assert_close_rel_max(to_np64(out), ref, 2e-2, "grouped ffn")
+
+
+# Expert counts chosen so that every kind of last M tile occurs: none (a multiple of 256),
+# swapped with 64 token columns (remainder 1..64), swapped with 128 (65..128), and a plain
+# 256-row tile (129..255); k = 2 with even experts in slot 0 and odd experts in slot 1.
+@pytest.mark.parametrize("H,I", [(320, 384), (256, 320)])
+def test_grouped_ffn_every_last_tile_kind(H, I):
+    moe = need_gpu()
+    even = [256, 300, 64, 385, 0, 571]
+    odd = [330, 384, 65, 129, 1, 667]
+    T, E, k = sum(even), 12, 2
+    assert sum(odd) == T
+    rng = np.random.default_rng(H + I)
+    idx = np.empty((T, k), np.int32)
+    idx[:, 0] = rng.permutation(np.repeat(np.arange(0, E, 2), even))
+    idx[:, 1] = rng.permutation(np.repeat(np.arange(1, E, 2), odd))
+    w = rng.uniform(0.05, 1.0, size=(T, k)).astype(np.float32)
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, dtype="bf16", logits="distinct", seed=H * I)
+    al = align.align_by_expert(idx, w, E)
+    assert al["counts"][0::2].tolist() == even and al["counts"][1::2].tolist() == odd
+    t = {k_: torch.from_numpy(np.ascontiguousarray(al[k_])).to(DEV)
+         for k_ in ("counts", "offsets", "sorted_token_ids", "sorted_weights", "reverse_indices")}
+    out = moe.moe_grouped_ffn(to_dev(d["hidden"], "bf16"), to_dev(d["w13"], "bf16"), to_dev(d["w2"], "bf16"),
+                              k, t["counts"], t["offsets"], t["sorted_token_ids"], t["sorted_weights"],
+                              t["reverse_indices"])
+    torch.cuda.synchronize()
+    ref = ffn.grouped_ffn(d["hidden"], d["w13"], d["w2"], "bf16", k, al["counts"], al["offsets"],
+                          al["sorted_token_ids"], al["sorted_weights"], al["reverse_indices"])
+    assert_close_rel_max(to_np64(out), ref, 2e-2, "grouped ffn, every last-tile kind")
 
 
 def test_layer_repeated_calls_are_identical():

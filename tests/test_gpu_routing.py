@@ -187,6 +187,8 @@ def _sigmoid_scores(T, E, seed):
     (3000, 160, 6, 8, 3),      # DeepSeek-V2-shaped routing
     (777, 64, 6, 8, 3), (100, 8, 2, 4, 2), (50, 1024, 32, 32, 7), (1, 256, 8, 8, 4), (0, 256, 8, 8, 4),
     (64, 96, 4, 3, 1), (64, 32, 3, 16, 2),
+    (300, 512, 8, 4, 2),       # groups of 128 experts: warp-per-token form
+    (200, 320, 6, 10, 4),      # E > 256 with groups of 32: lane-per-group form
 ])
 @pytest.mark.parametrize("method", ["group_limited_greedy", "noaux_tc"])
 def test_group_limited_topk(T, E, k, n_group, topk_group, method):
