@@ -168,19 +168,21 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
     (>= 768 MiB) stream through HBM rather than L2: algorithmic bytes / CUDA-event time.
 
     Bytes per token (SURVEY-style accounting of what the method must move):
-      gating 4E + 8k; indices->multihot 8k + 9E; multihot->indices 8E + 8k (probs and
-      indices out); align 8k in + 12k out (+ E-sized tables); group-limited top-k
-      (DeepSeek-V3 shape E=256, 8 groups, keep 4, k=8) 4E + 8k.
+      gating 4E + 8k (bf16 logits: 2E + 8k); indices->multihot 8k + 9E;
+      multihot->indices 8E + 8k (probs and indices out); align 8k in + 12k out (+ E-sized
+      tables); group-limited top-k (DeepSeek-V3 shape E=256, 8 groups, keep 4, k=8) 4E + 8k.
     """
     import torch
     E, k = wl.E, wl.k
-    per_tok = {"gating_softmax_topk": 4 * E + 8 * k, "indices_to_multihot": 8 * k + 9 * E,
+    per_tok = {"gating_softmax_topk": 4 * E + 8 * k, "gating_softmax_topk_bf16": 2 * E + 8 * k,
+               "indices_to_multihot": 8 * k + 9 * E,
                "multihot_to_indices": 8 * E + 8 * k, "align_by_expert": 20 * k}
     T = max(1, int(target_bytes // (8 * E + 8 * k)))
     T = min(T, (1 << 31) // max(k, 1) - 1)
     g = torch.Generator(device=dev)
     g.manual_seed(1)
     logits = torch.randn((T, E), generator=g, device=dev)
+    logits_bf16 = logits.to(torch.bfloat16)
     stream = torch.cuda.current_stream(dev)
     w, idx = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
     mh, pm, pos = moe.moe_indices_to_multihot(idx, w, E)
@@ -190,6 +192,8 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
     calls = {
         "gating_softmax_topk": lambda: moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob, weights=w,
                                                                    indices=idx, stream=stream),
+        "gating_softmax_topk_bf16": lambda: moe.moe_gating_softmax_topk_bf16(
+            logits_bf16, k, wl.norm_topk_prob, weights=w, indices=idx, stream=stream),
         "indices_to_multihot": lambda: moe.moe_indices_to_multihot(idx, w, E, multihot=mh, probs_in_multihot=pm,
                                                                    position_map=pos, stream=stream),
         "multihot_to_indices": lambda: moe.moe_multihot_to_indices(pm, pos, k, probs=p2, indices=i2, stream=stream),
@@ -213,7 +217,7 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
 
     for name, fn in calls.items():
         res[name] = timed(fn, per_tok[name] * T)
-    del logits, mh, pm, pos, p2, i2, al, ws
+    del logits, logits_bf16, mh, pm, pos, p2, i2, al, ws
     # DeepSeek-V3-shaped group-limited routing on sigmoid scores
     Eg, kg = 256, 8
     Tg = int(target_bytes // (4 * Eg + 8 * kg))

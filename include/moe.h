@@ -91,6 +91,19 @@ MOE_API int moe_gating_softmax_topk(const float* logits, int T, int E, int k, in
                                     float* weights, int32_t* indices, void* stream);
 
 /*
+ * Gating softmax-top-k on bf16 logits ([T, E], raw bfloat16 bits, finite).
+ * [mlc] gating_softmax_topk takes the logits dtype as a parameter; this is the
+ * bf16 instance. Each logit is widened to float32 exactly, and the result is
+ * bit-identical to moe_gating_softmax_topk on the widened row: same indices,
+ * same float32 weights. The page casts the weights back to the logits dtype;
+ * here they stay float32, the precision the align and FFN steps take. Ties are
+ * frequent with 8-bit mantissas and follow the same rule (lower index first).
+ * Errors and alignment as moe_gating_softmax_topk.
+ */
+MOE_API int moe_gating_softmax_topk_bf16(const void* logits, int T, int E, int k, int norm_topk_prob,
+                                         float* weights, int32_t* indices, void* stream);
+
+/*
  * Group-limited top-k (DeepSeek-style routing).  [mlc] group_limited_greedy_topk.
  *   scores   [T, E] float32 (finite), E = n_group * group_size.
  *   bias     [E] float32, the score correction added for the choice (method

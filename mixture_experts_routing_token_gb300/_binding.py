@@ -29,6 +29,7 @@ _p, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 # name -> (restype, argtypes); mirrors include/moe.h
 SIGNATURES = {
     "moe_gating_softmax_topk": (_i, [_p, _i, _i, _i, _i, _p, _p, _p]),
+    "moe_gating_softmax_topk_bf16": (_i, [_p, _i, _i, _i, _i, _p, _p, _p]),
     "moe_group_limited_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p]),
     "moe_indices_to_multihot": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p]),
     "moe_multihot_to_indices": (_i, [_p, _p, _i, _i, _i, _p, _p, _p]),
@@ -126,6 +127,18 @@ def moe_gating_softmax_topk(logits, k, norm_topk_prob=True, weights=None, indice
     weights = _out(weights, (T, k), torch.float32, logits.device, "weights")
     indices = _out(indices, (T, k), torch.int32, logits.device, "indices")
     _check("moe_gating_softmax_topk", lib().moe_gating_softmax_topk(
+        _ptr(logits), T, E, k, int(bool(norm_topk_prob)), _ptr(weights), _ptr(indices),
+        _stream(stream, logits.device)))
+    return weights, indices
+
+
+def moe_gating_softmax_topk_bf16(logits, k, norm_topk_prob=True, weights=None, indices=None, stream=None):
+    """Top-k experts per row of bf16 ``logits [T,E]`` -> (weights [T,k] f32, indices [T,k] i32)."""
+    _dev(logits, "logits", torch.bfloat16)
+    T, E = logits.shape
+    weights = _out(weights, (T, k), torch.float32, logits.device, "weights")
+    indices = _out(indices, (T, k), torch.int32, logits.device, "indices")
+    _check("moe_gating_softmax_topk_bf16", lib().moe_gating_softmax_topk_bf16(
         _ptr(logits), T, E, k, int(bool(norm_topk_prob)), _ptr(weights), _ptr(indices),
         _stream(stream, logits.device)))
     return weights, indices

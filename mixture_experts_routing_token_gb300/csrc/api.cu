@@ -198,6 +198,17 @@ MOE_API int moe_gating_softmax_topk(const float* logits, int T, int E, int k, in
   return launch_gating(logits, T, E, k, norm_topk_prob != 0, weights, indices, (cudaStream_t)stream);
 }
 
+MOE_API int moe_gating_softmax_topk_bf16(const void* logits, int T, int E, int k, int norm_topk_prob,
+                                         float* weights, int32_t* indices, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_tensor(logits, (long)T * E, "logits"))) return rc;
+  if ((rc = check_tensor(weights, (long)T * k, "weights"))) return rc;
+  if ((rc = check_tensor(indices, (long)T * k, "indices"))) return rc;
+  return launch_gating_bf16(logits, T, E, k, norm_topk_prob != 0, weights, indices, (cudaStream_t)stream);
+}
+
 MOE_API int moe_group_limited_topk(const float* scores, const float* bias, int T, int E, int k,
                                    int n_group, int topk_group, int method, float* weights,
                                    int32_t* indices, void* stream) {

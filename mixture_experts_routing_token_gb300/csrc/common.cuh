@@ -49,6 +49,9 @@ struct Carver {
 
 int launch_gating(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                   cudaStream_t s);
+// Same top-k on bf16 logits (widened exactly to float32 on load).
+int launch_gating_bf16(const void* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                       cudaStream_t s);
 int launch_group_limited_topk(const float* scores, const float* bias, int T, int E, int k, int n_group,
                               int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s);
 int launch_indices_to_multihot(const int32_t* idx, const float* probs, int T, int k, int E,

@@ -5,12 +5,29 @@
 
 #include <float.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace moe {
 namespace gate {
 
 constexpr int kNone = 0x7fffffff;   // "no candidate" index
+
+// Logits are float32 or bf16; bf16 values are widened to float32 exactly, so
+// everything after the load is the float32 computation on the widened row.
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float load_logit(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_logit(const __nv_bfloat16* p) {
+  return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+// 8 consecutive bf16 logits from a 16-byte aligned address
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+  x[0] = lo_bf16(q.x); x[1] = hi_bf16(q.x); x[2] = lo_bf16(q.y); x[3] = hi_bf16(q.y);
+  x[4] = lo_bf16(q.z); x[5] = hi_bf16(q.z); x[6] = lo_bf16(q.w); x[7] = hi_bf16(q.w);
+}
 
 // (value, index) order of the page's top-k: larger value first; equal values
 // keep the lower expert index first. kNone loses to everything.
@@ -86,16 +103,30 @@ __device__ __forceinline__ int warp_argmax_round(const unsigned (&key)[V], unsig
 // written to slot j by lane j % L (its raw logit first); the denominator is a
 // TwoSum-compensated float32 sum (identical in every lane), and a last pass
 // turns each slot's logit into its weight with one correctly rounded division.
-template <int L, int V>
-__device__ __forceinline__ void gate_one_token(const float* __restrict__ logits, long t, int E, int k,
+template <int L, int V, typename In = float>
+__device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, long t, int E, int k,
                                                int norm, float* __restrict__ w_out,
                                                int32_t* __restrict__ idx_out) {
   const int g = threadIdx.x & (L - 1);
   const unsigned gm = group_mask<L>();
   const int base = g * V;
-  const float* row = logits + t * (long)E;
+  const In* row = logits + t * (long)E;
   float v[V];
-  if ((V % 4) == 0 && (E & 3) == 0) {
+  if constexpr (!std::is_same<In, float>::value) {
+    if ((V % 8) == 0 && (E & 7) == 0) {
+#pragma unroll
+      for (int q = 0; q < V / 8; ++q) {
+        const int e0 = base + 8 * q;
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (e0 < E) load8_bf16(row + e0, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * q + i] = x[i];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = base + i < E ? load_logit(row + base + i) : 0.0f;
+    }
+  } else if ((V % 4) == 0 && (E & 3) == 0) {
 #pragma unroll
     for (int q = 0; q < V / 4; ++q) {
       const int e0 = base + 4 * q;
@@ -166,11 +197,27 @@ constexpr int kStageLd = kStageRows + 1;
 // Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into col[EP][kStageLd],
 // experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows); the
 // caller synchronises before reading.
-template <int EP>
-__device__ __forceinline__ void stage_rows(const float* __restrict__ logits, long t0, int nt, int E,
+template <int EP, typename In = float>
+__device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t0, int nt, int E,
                                            float* col, int tid, int nthr) {
-  const float* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
-  if ((E & 3) == 0) {
+  const In* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
+  if constexpr (!std::is_same<In, float>::value) {
+    if ((E & 7) == 0) {
+      const int n8 = nt * E / 8;
+      for (int f = tid; f < n8; f += nthr) {
+        float x[8];
+        load8_bf16(blk + 8 * f, x);
+        const int tl = (8 * f) / E, e0 = 8 * f - tl * E;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) col[(e0 + i) * kStageLd + tl] = x[i];
+      }
+    } else {
+      for (int f = tid; f < nt * E; f += nthr) {
+        const int tl = f / E;
+        col[(f - tl * E) * kStageLd + tl] = load_logit(blk + f);
+      }
+    }
+  } else if ((E & 3) == 0) {
     const int n4 = nt * E / 4;
     for (int f = tid; f < n4; f += nthr) {
       const float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);

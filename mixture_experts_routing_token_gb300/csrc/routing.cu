@@ -21,55 +21,55 @@ using gate::group_mask;
 using gate::kNone;
 
 constexpr int kBlock = 256;
-template <int L, int V>
-__global__ void __launch_bounds__(kBlock) gating_kernel(const float* __restrict__ logits, int T,
+template <int L, int V, typename In>
+__global__ void __launch_bounds__(kBlock) gating_kernel(const In* __restrict__ logits, int T,
                                                         int E, int k, int norm,
                                                         float* __restrict__ w_out,
                                                         int32_t* __restrict__ idx_out) {
   const long t = (long)blockIdx.x * (kBlock / L) + threadIdx.x / L;
   if (t >= T) return;   // whole groups leave together
-  gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
+  gate::gate_one_token<L, V, In>(logits, t, E, k, norm, w_out, idx_out);
 }
 
 // Gating for E <= 128, one thread per token: each CTA stages its 128 rows in
 // shared memory and runs gate::topk_staged_row on them (gating_device.cuh).
 constexpr int kSmemGateThreads = gate::kStageRows;
 
-template <int EP>
+template <int EP, typename In>
 __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
+    const In* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
     int32_t* __restrict__ idx_out) {
   extern __shared__ float col[];                   // [EP][kStageLd]
   const int tid = threadIdx.x;
   const long t0 = (long)blockIdx.x * kSmemGateThreads;
   const int nt = (int)min((long)kSmemGateThreads, (long)T - t0);
-  gate::stage_rows<EP>(logits, t0, nt, E, col, tid, kSmemGateThreads);
+  gate::stage_rows<EP, In>(logits, t0, nt, E, col, tid, kSmemGateThreads);
   __syncthreads();
   if (tid < nt) gate::topk_staged_row<EP>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
 }
 
-template <int EP>
-int launch_gating_smem(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+template <int EP, typename In>
+int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
   const size_t smem = (size_t)EP * gate::kStageLd * sizeof(float);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
-    cudaFuncSetAttribute(gating_smem_kernel<EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(gating_smem_kernel<EP, In>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr[dev] = true;
   }
-  gating_smem_kernel<EP><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
+  gating_smem_kernel<EP, In><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
       logits, T, E, k, norm, w, idx);
   return check_launch("gating_softmax_topk");
 }
 
-template <int L, int V>
-int launch_gating_t(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+template <int L, int V, typename In>
+int launch_gating_t(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                     cudaStream_t s) {
   const int tpb = kBlock / L;
   const int grid = (T + tpb - 1) / tpb;
-  gating_kernel<L, V><<<grid, kBlock, 0, s>>>(logits, T, E, k, norm, w, idx);
+  gating_kernel<L, V, In><<<grid, kBlock, 0, s>>>(logits, T, E, k, norm, w, idx);
   return check_launch("gating_softmax_topk");
 }
 
@@ -590,19 +590,34 @@ int launch_group_t(const float* scores, const float* bias, int T, int E, int k, 
   return check_launch("group_limited_topk");
 }
 
-}  // namespace
+// E <= 8: a thread per token, row in registers; E <= 128: the staged thread-per-token
+// kernel; wider rows: L lanes of 64 experts per token.
+template <typename In>
+int launch_gating_any(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                      cudaStream_t s, const char* name) {
+  if (T == 0) return MOE_OK;
+  ProfScope ps(name, s);
+  if (E <= 8) return launch_gating_t<1, 8, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 16) return launch_gating_smem<16, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 32) return launch_gating_smem<32, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 64) return launch_gating_smem<64, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 128) return launch_gating_smem<128, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 256) return launch_gating_t<4, 64, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 512) return launch_gating_t<8, 64, In>(logits, T, E, k, norm, w, idx, s);
+  return launch_gating_t<16, 64, In>(logits, T, E, k, norm, w, idx, s);
+}
 
+}  // namespace
 
 int launch_gating(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                   cudaStream_t s) {
-  if (T == 0) return MOE_OK;
-  ProfScope ps("gating_softmax_topk", s);
-  if (E <= 8) return launch_gating_t<1, 8>(logits, T, E, k, norm, w, idx, s);
-  if (E <= 16) return launch_gating_smem<16>(logits, T, E, k, norm, w, idx, s);
-  if (E <= 32) return launch_gating_smem<32>(logits, T, E, k, norm, w, idx, s);
-  if (E <= 64) return launch_gating_smem<64>(logits, T, E, k, norm, w, idx, s);
-  if (E <= 128) return launch_gating_smem<128>(logits, T, E, k, norm, w, idx, s);
-  MOE_DISPATCH_LV(E, launch_gating_t, logits, T, E, k, norm, w, idx, s);
+  return launch_gating_any(logits, T, E, k, norm, w, idx, s, "gating_softmax_topk");
+}
+
+int launch_gating_bf16(const void* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                       cudaStream_t s) {
+  return launch_gating_any(static_cast<const __nv_bfloat16*>(logits), T, E, k, norm, w, idx, s,
+                           "gating_softmax_topk_bf16");
 }
 
 int launch_indices_to_multihot(const int32_t* idx, const float* probs, int T, int k, int E,

@@ -21,12 +21,19 @@ What the page computes, restated:
 
 Arithmetic is float64, rounded once to float32 (the logits' dtype, the page
 casts back to it). Logits must be finite.
+
+``gating_softmax_topk`` is written for any logits dtype. For bf16 logits
+(``softmax_topk_bf16``) the reading is: each bf16 value is exactly a float32
+value (its 16 bits followed by 16 zero bits), and the result is the float32
+computation on those values, with the weights kept in float32 (the dtype the
+align and FFN steps take) rather than cast back to bf16.
 """
 from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["topk", "softmax_topk", "group_limited_topk", "FLOAT32_LOWEST"]
+__all__ = ["topk", "softmax_topk", "softmax_topk_bf16", "bf16_bits_as_float32", "group_limited_topk",
+           "FLOAT32_LOWEST"]
 
 FLOAT32_LOWEST = np.float32(np.finfo(np.float32).min)
 
@@ -60,6 +67,17 @@ def softmax_topk(logits: np.ndarray, k: int, norm_topk_prob: bool = True):
         prob = ex / ex.sum(axis=1, keepdims=True)
         w = np.take_along_axis(prob, idx, axis=1)
     return w.astype(np.float32), idx
+
+
+def bf16_bits_as_float32(bits: np.ndarray) -> np.ndarray:
+    """bf16 values given as uint16 bit patterns -> the equal float32 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def softmax_topk_bf16(logit_bits: np.ndarray, k: int, norm_topk_prob: bool = True):
+    """``gating_softmax_topk`` on bf16 logits (uint16 bits): float32 weights, int32 indices."""
+    return softmax_topk(bf16_bits_as_float32(logit_bits), k, norm_topk_prob)
 
 
 def group_limited_topk(scores: np.ndarray, k: int, n_group: int, topk_group: int,

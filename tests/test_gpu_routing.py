@@ -56,6 +56,26 @@ def test_gating_ties_go_to_lower_index(E, k):
     _gating_case(moe, x, k, False)
 
 
+# bf16 logits: same indices and bit-identical weights as the float32 entry on the widened
+# rows; both within 1e-6 of the oracle. Shapes cover every kernel of the dispatch, vector and
+# scalar row loads (E % 8), and heavy ties (8-bit mantissas).
+@pytest.mark.parametrize("E,k", [(8, 2), (6, 3), (16, 4), (36, 5), (64, 8), (100, 6), (128, 8),
+                                 (256, 8), (520, 16), (1024, 32)])
+@pytest.mark.parametrize("norm", [True, False])
+def test_gating_bf16_logits(E, k, norm):
+    moe = need_gpu()
+    x = gen_logits(np.random.SeedSequence(E * 77 + k), 300, E, "plain")
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    w_ref, i_ref = gating.softmax_topk_bf16(bits, k, norm)
+    w, i = moe.moe_gating_softmax_topk_bf16(xb, k, norm)
+    w32, i32 = moe.moe_gating_softmax_topk(xb.float(), k, norm)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(i.cpu().numpy(), i_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=W_RTOL, atol=0)
+    assert torch.equal(i, i32) and torch.equal(w.view(torch.int32), w32.view(torch.int32))
+
+
 def test_gating_empty_and_single():
     moe = need_gpu()
     w, i = moe.moe_gating_softmax_topk(torch.zeros((0, 8), device=DEV), 2)

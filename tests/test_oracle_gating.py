@@ -211,3 +211,26 @@ def test_group_limited_choice_stays_in_kept_groups():
         gating.group_limited_topk(x, 200, 8, 4, "noaux_tc", bias)
     with pytest.raises(ValueError):
         gating.group_limited_topk(x, 4, 256, 4, "noaux_tc", bias)      # one expert per group
+
+
+# ---- bf16 logits ------------------------------------------------------------------------
+
+def test_bf16_widening_matches_known_bit_patterns():
+    """bf16 bit patterns with textbook values: 1.0, -2.0, 0.5, the largest finite bf16,
+    the smallest normal, and a value whose float32 tail is zero by definition."""
+    bits = np.array([0x3F80, 0xC000, 0x3F00, 0x7F7F, 0x0080, 0x4049], np.uint16)
+    want = [1.0, -2.0, 0.5, 3.3895313892515355e38, 2.0 ** -126, 3.140625]
+    assert gating.bf16_bits_as_float32(bits).astype(np.float64).tolist() == want
+
+
+def test_bf16_topk_ties_follow_the_insertion_procedure():
+    """Coarse bf16 values tie often; the order must be the page's insertion procedure."""
+    rng = np.random.default_rng(4)
+    for E, k in [(8, 2), (16, 4), (12, 12)]:
+        x = (rng.integers(-4, 5, size=(30, E)) * 0.25).astype(np.float32)
+        bits = (x.view(np.uint32) >> 16).astype(np.uint16)          # exact: x has short mantissas
+        w, i = gating.softmax_topk_bf16(bits, k, True)
+        for r in range(x.shape[0]):
+            _, pi = insertion_topk(x[r].tolist(), k)
+            assert i[r].tolist() == pi
+        np.testing.assert_allclose(w.astype(np.float64).sum(1), 1.0, atol=1e-6)
