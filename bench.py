@@ -414,23 +414,21 @@ def main():
             graph.replay()
         torch.cuda.synchronize()
 
-    # per-kernel CUDA-event times: in the timed region itself when stepping eagerly,
-    # from a separate eager pass of the same length when the timed region replays a graph
-    kern = None
-    if use_graph:
-        moe.profiler_enable(True)
-        for _ in range(args.steps):
-            step()
-        torch.cuda.synchronize()
-        moe.profiler_enable(False)
-        kern = moe.profiler_report()
-
-    # ---- timed region: K steps, device events on the launching stream
+    # per-kernel CUDA-event times (each kernel bracketed on its own stream): a timed
+    # pass of K eager steps just before the timed region, under the clock sampler
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
-    if not use_graph:
-        moe.profiler_enable(True)
+    moe.profiler_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    moe.profiler_enable(False)
+    kern = moe.profiler_report()
+
+    # ---- timed region: K steps, device events on the launching stream. No events
+    # between the layer's kernels here: an event recorded between two launches
+    # serialises the programmatic dependent launch of the second one.
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -446,43 +444,66 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    if not use_graph:
-        moe.profiler_enable(False)
-        kern = moe.profiler_report()
     clocks = clk.stop()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
     ms = ms_total / args.steps
     value = whole_job_rate(T, world, args.steps, ms_total)
 
-    # ---- end to end through the public call: pinned host inputs in, output back to host
+    # ---- end to end through the public call: pinned host inputs in, output back to host.
+    # Every step copies its inputs in and its output back; with two buffer sets the
+    # copies of the neighbouring steps run on two copy streams while a step computes
+    # (H2D of step i+1 and D2H of step i-1 overlap step i, as a serving loop would).
     e2e = None
     if not args.no_e2e:
         h_hidden = hidden.cpu().pin_memory()
         h_logits = logits.cpu().pin_memory()
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_hidden = torch.empty_like(hidden)
-        d_logits = torch.empty_like(logits)
+        nb = 2
+        h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(nb)]
+        d_hidden = [torch.empty_like(hidden) for _ in range(nb)]
+        d_logits = [torch.empty_like(logits) for _ in range(nb)]
+        d_out = [torch.empty_like(out) for _ in range(nb)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(nb)]
+        ev_comp = [torch.cuda.Event() for _ in range(nb)]
+        ev_out = [torch.cuda.Event() for _ in range(nb)]
 
-        def e2e_step():
-            d_hidden.copy_(h_hidden, non_blocking=True)
-            d_logits.copy_(h_logits, non_blocking=True)
-            moe.moe_layer_forward(d_hidden, d_logits, w13, w2, k, wl.norm_topk_prob, out=out, workspace=ws,
-                                  stream=stream)
-            h_out.copy_(out, non_blocking=True)
+        def e2e_step(i):
+            b = i % nb
+            if i >= nb:
+                s_in.wait_event(ev_comp[b])        # step i-2 has consumed input set b
+            with torch.cuda.stream(s_in):
+                d_hidden[b].copy_(h_hidden, non_blocking=True)
+                d_logits[b].copy_(h_logits, non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= nb:
+                stream.wait_event(ev_out[b])       # step i-2's output has been read back
+            moe.moe_layer_forward(d_hidden[b], d_logits[b], w13, w2, k, wl.norm_topk_prob, out=d_out[b],
+                                  workspace=ws, stream=stream)
+            ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                h_out[b].copy_(d_out[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
-        for _ in range(3):
-            e2e_step()
+        for i in range(3):
+            e2e_step(i)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        s_in.wait_stream(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        stream.wait_stream(s_out)
         b.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(a.elapsed_time(b), dev)
+        h_out = h_out[0]
         e2e = {"value": whole_job_rate(T, world, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size() + h_logits.numel() * 4,
-               "d2h_bytes_per_step": h_out.numel() * h_out.element_size()}
+               "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
+               "copies": "pinned host buffers; the H2D of step i+1 and the D2H of step i-1 overlap step i "
+                         "on two copy streams (two device buffer sets)"}
 
     if rank != 0:
         if world > 1:
@@ -515,8 +536,10 @@ def main():
                        "l2": "inputs larger than L2 (weights %.2f GB read per step)" % (
                            (w13.numel() + w2.numel()) * w13.element_size() / 1e9),
                        "inputs": "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)))",
-                       "timing": ("CUDA graph replay of one layer step; per-kernel times from an eager pass"
-                                  if use_graph else "eager steps; per-kernel CUDA events inside the timed region")},
+                       "timing": ("CUDA graph replay of one layer step" if use_graph else "eager steps") +
+                                 "; per-kernel CUDA events (roofline, kernels) from a timed pass of K eager "
+                                 "steps just before, since events between launches serialise the "
+                                 "programmatic dependent launches"},
             "layer_tflops": ffn_flops / (ms / 1e3) / 1e12,
             "roofline": roofline, "kernels": per_kernel, "gpu_launches": launches * args.steps,
             "gpu_launches_per_step": launches, "clocks": clocks, "e2e": e2e, "lib": moe.version()}

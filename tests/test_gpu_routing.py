@@ -209,6 +209,7 @@ def _sigmoid_scores(T, E, seed):
     (64, 96, 4, 3, 1), (64, 32, 3, 16, 2),
     (300, 512, 8, 4, 2),       # groups of 128 experts: warp-per-token form
     (200, 320, 6, 10, 4),      # E > 256 with groups of 32: lane-per-group form
+    (70, 64, 4, 2, 1), (90, 128, 8, 4, 3), (33, 512, 16, 16, 5),   # more groups of 32
 ])
 @pytest.mark.parametrize("method", ["group_limited_greedy", "noaux_tc"])
 def test_group_limited_topk(T, E, k, n_group, topk_group, method):
@@ -225,6 +226,10 @@ def test_group_limited_topk_ties_and_golden(method, gold):
     x = (rng.integers(0, 4, size=(500, 48)) * 0.25).astype(np.float32)
     bias = (rng.integers(-1, 2, size=48) * 0.25).astype(np.float32)
     _group_case(moe, x, bias, 5, 6, 3, method)
+    # groups of 32 with ties inside groups, between group scores and between experts
+    x = (rng.integers(0, 4, size=(700, 256)) * 0.25).astype(np.float32)
+    bias = (rng.integers(-1, 2, size=256) * 0.25).astype(np.float32)
+    _group_case(moe, x, bias, 8, 8, 4, method)
     g = gold("group_limited_topk")
     x = np.array(g["scores"], np.float32)
     _group_case(moe, x, np.array(g["bias"], np.float32), g["k"], g["n_group"], g["topk_group"], method)
