@@ -173,6 +173,8 @@ int run_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int 
             cudaStream_t s) {
   FfnArgs a{hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, ids, sw, rev,
             out, w.act, w.staging, w.xs, status};
+  int rc = launch_zero_dropped(offsets, E, (long)T * k, H, w.staging, s);
+  if (rc) return rc;
   return ffn_uses_tensor_cores(dtype, H, I) ? launch_ffn_tc(a, s) : launch_ffn_simt(a, s);
 }
 

@@ -67,6 +67,30 @@ __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __rest
   }
 }
 
+// Slots dropped by the align step (expert index outside [0, E)) are in no
+// expert's rows, so no FFN epilogue writes their staging rows. When any slot
+// was dropped (offsets[E] < S) the whole staging buffer is zeroed before the
+// FFN writes the routed rows; otherwise the kernel exits at once.
+__global__ void __launch_bounds__(256) zero_dropped_kernel(const int32_t* __restrict__ offsets, int E, long S,
+                                                           int H4, float4* __restrict__ staging) {
+  pdl_wait();
+  pdl_trigger();
+  if (__ldg(offsets + E) >= S) return;
+  const long n = S * H4;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
+    staging[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void __launch_bounds__(256) zero_dropped_scalar_kernel(const int32_t* __restrict__ offsets, int E,
+                                                                  long S, int H, float* __restrict__ staging) {
+  pdl_wait();
+  pdl_trigger();
+  if (__ldg(offsets + E) >= S) return;
+  const long n = S * H;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
+    staging[i] = 0.0f;
+}
+
 template <class OutT>
 int launch_t(const float* staging, int T, int k, int H, OutT* out, cudaStream_t s) {
   ProfScope ps("combine", s);
@@ -84,6 +108,19 @@ int launch_t(const float* staging, int T, int k, int H, OutT* out, cudaStream_t 
 }
 
 }  // namespace
+
+int launch_zero_dropped(const int32_t* offsets, int E, long S, int H, float* staging, cudaStream_t s) {
+  if (S * H == 0) return MOE_OK;
+  ProfScope ps("zero_dropped", s);
+  const long units = S * (H % 4 == 0 ? H / 4 : H);
+  const int grid = (int)std::max(1L, std::min((long)num_sms() * 4, (units + 255) / 256));
+  const cudaError_t e =
+      H % 4 == 0 ? launch_pdl(zero_dropped_kernel, grid, 256, 0, s, offsets, E, S, H / 4,
+                              reinterpret_cast<float4*>(staging))
+                 : launch_pdl(zero_dropped_scalar_kernel, grid, 256, 0, s, offsets, E, S, H, staging);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "zero_dropped: %s", cudaGetErrorString(e));
+  return check_launch("zero_dropped");
+}
 
 int launch_combine(const float* staging, int T, int k, int H, int dtype, void* out, cudaStream_t s) {
   if ((long)T * H == 0) return MOE_OK;

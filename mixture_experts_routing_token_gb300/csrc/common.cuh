@@ -107,6 +107,8 @@ bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
 int launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
+// Zeroes the staging rows when the align step dropped slots (offsets[E] < S).
+int launch_zero_dropped(const int32_t* offsets, int E, long S, int H, float* staging, cudaStream_t s);
 int launch_combine(const float* staging, int T, int k, int H, int dtype, void* out,
                    cudaStream_t s);
 

@@ -139,6 +139,33 @@ def test_grouped_ffn_every_last_tile_kind(H, I):
     assert_close_rel_max(to_np64(out), ref, 2e-2, "grouped ffn, every last-tile kind")
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [(300, 256, 256, 8, 2), (40, 128, 128, 16, 4), (90, 40, 24, 5, 2)])
+def test_grouped_ffn_dropped_slots_contribute_nothing(T, H, I, E, k):
+    """Slots whose expert index is outside [0, E) are dropped by the align step; the FFN must
+    ignore them even when the workspace holds stale data (filled with NaN bytes here)."""
+    moe = need_gpu()
+    dt = "bf16" if H % 64 == 0 else "f32"
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, dtype=dt, logits="distinct", seed=T + k)
+    w, idx = gating.softmax_topk(d["logits"], k, True)
+    idx = idx.copy()
+    rng = np.random.default_rng(T)
+    drop = rng.random(idx.shape) < 0.2
+    idx[drop] = np.where(rng.random(int(drop.sum())) < 0.5, -1, E + 3)
+    al = align.align_by_expert(idx, w, E)
+    assert al["valid_slots"] < T * k
+    t = {k_: torch.from_numpy(np.ascontiguousarray(al[k_])).to(DEV)
+         for k_ in ("counts", "offsets", "sorted_token_ids", "sorted_weights", "reverse_indices")}
+    code = moe.MOE_BF16 if dt == "bf16" else moe.MOE_F32
+    ws = torch.full((moe.moe_grouped_ffn_workspace_size(code, T, H, I, E, k),), 0xFF, dtype=torch.uint8, device=DEV)
+    out = moe.moe_grouped_ffn(to_dev(d["hidden"], dt), to_dev(d["w13"], dt), to_dev(d["w2"], dt), k,
+                              t["counts"], t["offsets"], t["sorted_token_ids"], t["sorted_weights"],
+                              t["reverse_indices"], workspace=ws)
+    torch.cuda.synchronize()
+    ref = ffn.grouped_ffn(d["hidden"], d["w13"], d["w2"], dt, k, al["counts"], al["offsets"],
+                          al["sorted_token_ids"], al["sorted_weights"], al["reverse_indices"])
+    assert_close_rel_max(to_np64(out), ref, layer_tolerance(dt), "grouped ffn with dropped slots")
+
+
 def test_layer_repeated_calls_are_identical():
     moe = need_gpu()
     d = make_layer_inputs(T=600, H=256, I=256, E=8, k=2, dtype="bf16", logits="distinct", seed=9)
