@@ -222,6 +222,38 @@ MOE_API int moe_grouped_ffn(const void* hidden, const void* w13, const void* w2,
                             void* out, void* ws, size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * Backward of the grouped expert FFN and the weighted combine (the training
+ * side of moe_grouped_ffn). The pages print the forward ([p6]
+ * moe_prefill_experts; [mlc] scatter_output, moe_sum) and name the training
+ * use ([mgt] IndicesToMultihot has a backward); this is the derivative of that
+ * forward. Per routed slot p (token t, expert e, weight w_p; g, u the gate and
+ * up pre-activations, s = sigmoid(g), a = g s u rounded to bf16 as in the
+ * forward, y = a W2[e]^T):
+ *   d_weights[t, j] = <d_out[t], y_p>                  (slot p = (t, j))
+ *   d_w2[e]         = sum_p (w_p d_out[t]) a_p^T        [H, I]
+ *   da_p = w_p d_out[t] W2[e];  dg = da u s (1 + g (1 - s));  du = da g s
+ *   d_w13[e]        = sum_p [dg du]_p^T x_t             [2I, H]
+ *   d_hidden[t]     = sum_j [dg du]_p W13[e]            [H]
+ * The bf16 rounding of a is differentiated as the identity. FC1 is
+ * recomputed (nothing from the forward call is needed besides its inputs and
+ * its routing). Inputs as moe_grouped_ffn plus d_out [T, H] bf16; outputs
+ * d_hidden [T, H], d_w13 [E, 2I, H], d_w2 [E, H, I] (bf16, float32
+ * accumulation, one rounding) and d_weights_or_null [T, k] float32 (0 for
+ * dropped slots). Experts without rows get zero weight gradients.
+ * bf16 with H % 64 == 0 and I % 64 == 0 only (MOE_ERR_UNSUPPORTED otherwise).
+ * ws / ws_bytes: at least moe_grouped_ffn_backward_workspace_size(...) bytes
+ * (0 for an unsupported dtype).
+ */
+MOE_API size_t moe_grouped_ffn_backward_workspace_size(int dtype, int T, int H, int I, int E, int k);
+MOE_API int moe_grouped_ffn_backward(const void* hidden, const void* w13, const void* w2, int dtype, int T,
+                                     int H, int I, int E, int k, const int32_t* counts,
+                                     const int32_t* offsets, const int32_t* sorted_token_ids,
+                                     const float* sorted_weights, const int32_t* reverse_indices,
+                                     const void* d_out, void* d_hidden, void* d_w13, void* d_w2,
+                                     float* d_weights_or_null, void* ws, size_t ws_bytes, int32_t* status,
+                                     void* stream);
+
+/*
  * Whole layer: gating -> align -> grouped FFN -> combine, in one call, on one
  * stream, without host synchronisation.
  *   hidden [T, H] dtype, router_logits [T, E] float32, w13, w2 as above.

@@ -8,7 +8,8 @@ from ._binding import (  # noqa: F401
     MOE_BF16, MOE_F32, MOE_GROUP_TOPK_GREEDY, MOE_GROUP_TOPK_NOAUX_TC, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_STATUS_BAD_INDEX, MOE_STATUS_TIMEOUT,
     MoeError, SIGNATURES, LIB_PATH, MOE_ALIGN_NOALLOC_SCRATCH_INTS, lib, moe_align_by_expert,
     moe_align_by_expert_noalloc, moe_align_workspace_size,
-    moe_gating_softmax_topk, moe_gating_softmax_topk_bf16, moe_group_limited_topk, moe_grouped_ffn, moe_grouped_ffn_workspace_size,
+    moe_gating_softmax_topk, moe_gating_softmax_topk_bf16, moe_group_limited_topk,
+    moe_grouped_ffn_backward, moe_grouped_ffn_backward_workspace_size, moe_grouped_ffn, moe_grouped_ffn_workspace_size,
     moe_indices_to_multihot, moe_layer_forward, moe_layer_workspace_size, moe_multihot_to_indices,
     profiler_enable, profiler_report, version,
 )

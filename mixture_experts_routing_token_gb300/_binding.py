@@ -38,6 +38,9 @@ SIGNATURES = {
     "moe_align_by_expert_noalloc": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p]),
     "moe_grouped_ffn_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_grouped_ffn": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p, _p]),
+    "moe_grouped_ffn_backward_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "moe_grouped_ffn_backward": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                      _p, _p, _sz, _p, _p]),
     "moe_layer_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_layer_forward": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p, _p]),
     "moe_profiler_enable": (_i, [_i]),
@@ -280,6 +283,41 @@ def moe_grouped_ffn(hidden, w13, w2, k, counts, offsets, sorted_token_ids, sorte
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream, d)))
     return out
+
+
+def moe_grouped_ffn_backward_workspace_size(dtype_code, T, H, I, E, k) -> int:
+    return int(lib().moe_grouped_ffn_backward_workspace_size(dtype_code, T, H, I, E, k))
+
+
+def moe_grouped_ffn_backward(hidden, w13, w2, k, counts, offsets, sorted_token_ids, sorted_weights,
+                             reverse_indices, d_out, d_hidden=None, d_w13=None, d_w2=None, d_weights=None,
+                             workspace=None, status=None, stream=None, want_d_weights=True):
+    """Backward of moe_grouped_ffn (bf16) -> (d_hidden [T,H], d_w13 [E,2I,H], d_w2 [E,H,I], d_weights [T,k] f32)."""
+    _dev(hidden, "hidden")
+    dt = _dtype_code(hidden)
+    T, H = hidden.shape
+    E, I2, H2 = w13.shape
+    I = I2 // 2
+    _dev(w13, "w13", hidden.dtype)
+    _dev(w2, "w2", hidden.dtype)
+    _dev(d_out, "d_out", hidden.dtype)
+    if H2 != H or tuple(w2.shape) != (E, H, I) or tuple(d_out.shape) != (T, H):
+        raise ValueError("shape mismatch")
+    d = hidden.device
+    d_hidden = _out(d_hidden, (T, H), hidden.dtype, d, "d_hidden")
+    d_w13 = _out(d_w13, (E, 2 * I, H), hidden.dtype, d, "d_w13")
+    d_w2 = _out(d_w2, (E, H, I), hidden.dtype, d, "d_w2")
+    if want_d_weights:
+        d_weights = _out(d_weights, (T, k), torch.float32, d, "d_weights")
+    need = moe_grouped_ffn_backward_workspace_size(dt, T, H, I, E, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d)
+    _check("moe_grouped_ffn_backward", lib().moe_grouped_ffn_backward(
+        _ptr(hidden), _ptr(w13), _ptr(w2), dt, T, H, I, E, k, _ptr(counts), _ptr(offsets),
+        _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(reverse_indices), _ptr(d_out), _ptr(d_hidden),
+        _ptr(d_w13), _ptr(d_w2), _ptr(d_weights) if want_d_weights else None, _ptr(workspace),
+        workspace.numel(), _ptr(status), _stream(stream, d)))
+    return d_hidden, d_w13, d_w2, (d_weights if want_d_weights else None)
 
 
 def moe_layer_workspace_size(dtype_code, T, H, I, E, k) -> int:

@@ -341,6 +341,99 @@ MOE_API int moe_grouped_ffn(const void* hidden, const void* w13, const void* w2,
                  sorted_weights, reverse_indices, out, w, status, (cudaStream_t)stream);
 }
 
+namespace moe {
+namespace {
+
+size_t carve_bwd(Carver& c, FfnBwdArgs* a, long S, int H, int I, int E) {
+  const long P = bwd_padded_rows(S, E);
+  int32_t* poff = c.take<int32_t>((size_t)E + 1);
+  void* xs = c.take<uint16_t>((size_t)P * H);
+  void* dos = c.take<uint16_t>((size_t)P * H);
+  void* dys = c.take<uint16_t>((size_t)P * H);
+  float* gu = c.take<float>((size_t)P * 2 * I);
+  void* act = c.take<uint16_t>((size_t)P * I);
+  void* dgu = c.take<uint16_t>((size_t)P * 2 * I);
+  float* dwp = c.take<float>((size_t)P * ((I + 255) / 256));
+  float* staging = c.take<float>((size_t)S * H);
+  if (a) {
+    a->poff = poff;
+    a->xs = xs;
+    a->dos = dos;
+    a->dys = dys;
+    a->gu = gu;
+    a->act = act;
+    a->dgu = dgu;
+    a->dwp = dwp;
+    a->staging = staging;
+  }
+  return align_up(c.used, 256);
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_API size_t moe_grouped_ffn_backward_workspace_size(int dtype, int T, int H, int I, int E, int k) {
+  if (dtype != MOE_BF16 || T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
+  Carver c(nullptr);
+  return carve_bwd(c, nullptr, (long)T * k, H, I, E);
+}
+
+MOE_API int moe_grouped_ffn_backward(const void* hidden, const void* w13, const void* w2, int dtype, int T,
+                                     int H, int I, int E, int k, const int32_t* counts,
+                                     const int32_t* offsets, const int32_t* sorted_token_ids,
+                                     const float* sorted_weights, const int32_t* reverse_indices,
+                                     const void* d_out, void* d_hidden, void* d_w13, void* d_w2,
+                                     float* d_weights_or_null, void* ws, size_t ws_bytes, int32_t* status,
+                                     void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  if ((rc = check_ffn_dims(dtype, H, I))) return rc;
+  if (dtype != MOE_BF16 || !ffn_uses_tensor_cores(dtype, H, I))
+    return fail(MOE_ERR_UNSUPPORTED, "the FFN backward runs bf16 with H %% 64 == 0 and I %% 64 == 0 only");
+  const long S = (long)T * k;
+  if ((rc = check_tensor(hidden, (long)T * H, "hidden"))) return rc;
+  if ((rc = check_tensor(w13, (long)E * 2 * I * H, "w13"))) return rc;
+  if ((rc = check_tensor(w2, (long)E * H * I, "w2"))) return rc;
+  if ((rc = check_tensor(counts, E, "counts"))) return rc;
+  if ((rc = check_tensor(offsets, E + 1, "offsets"))) return rc;
+  if ((rc = check_tensor(sorted_token_ids, S, "sorted_token_ids"))) return rc;
+  if ((rc = check_tensor(sorted_weights, S, "sorted_weights"))) return rc;
+  if ((rc = check_tensor(reverse_indices, S, "reverse_indices"))) return rc;
+  if ((rc = check_tensor(d_out, (long)T * H, "d_out"))) return rc;
+  if ((rc = check_tensor(d_hidden, (long)T * H, "d_hidden"))) return rc;
+  if ((rc = check_tensor(d_w13, (long)E * 2 * I * H, "d_w13"))) return rc;
+  if ((rc = check_tensor(d_w2, (long)E * H * I, "d_w2"))) return rc;
+  if (d_weights_or_null && (rc = check_tensor(d_weights_or_null, S, "d_weights"))) return rc;
+  if (status && (rc = check_tensor(status, 1, "status"))) return rc;
+  const size_t need = moe_grouped_ffn_backward_workspace_size(dtype, T, H, I, E, k);
+  if ((rc = check_ws(ws, ws_bytes, need))) return rc;
+  if (T == 0) return MOE_OK;
+  FfnBwdArgs a{};
+  a.hidden = hidden;
+  a.w13 = w13;
+  a.w2 = w2;
+  a.d_out = d_out;
+  a.T = T;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.k = k;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.sorted_ids = sorted_token_ids;
+  a.sorted_w = sorted_weights;
+  a.reverse = reverse_indices;
+  a.d_hidden = d_hidden;
+  a.d_w13 = d_w13;
+  a.d_w2 = d_w2;
+  a.d_weights = d_weights_or_null;
+  a.status = status;
+  Carver c(ws);
+  carve_bwd(c, &a, S, H, I, E);
+  return launch_ffn_backward(a, (cudaStream_t)stream);
+}
+
 MOE_API size_t moe_layer_workspace_size(int dtype, int T, int H, int I, int E, int k) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
   const long S = (long)T * k;

@@ -103,6 +103,37 @@ int launch_ffn_pair_gemms(const FfnArgs& a, const CUtensorMap& tA1, const CUtens
                           const CUtensorMap& tA2, const CUtensorMap& tB2, const CUtensorMap& tS2,
                           cudaStream_t s);
 
+// Backward of the grouped FFN and the k-sum (bf16, tensor cores; ffn_bwd.cu).
+struct FfnBwdArgs {
+  const void* hidden;
+  const void* w13;
+  const void* w2;
+  const void* d_out;
+  int T, H, I, E, k;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* sorted_ids;
+  const float* sorted_w;
+  const int32_t* reverse;
+  void* d_hidden;   // [T, H] bf16
+  void* d_w13;      // [E, 2I, H] bf16
+  void* d_w2;       // [E, H, I] bf16
+  float* d_weights; // [T, k] or null
+  // workspace
+  int32_t* poff;    // [E + 1]
+  void* xs;         // [P, H] bf16, P = bwd_padded_rows(S, E)
+  void* dos;        // [P, H] bf16
+  void* dys;        // [P, H] bf16
+  float* gu;        // [P, 2I]
+  void* act;        // [P, I] bf16
+  void* dgu;        // [P, 2I] bf16
+  float* dwp;       // [P, ceil(I / 256)]
+  float* staging;   // [S, H]
+  int32_t* status;
+};
+long bwd_padded_rows(long S, int E);
+int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s);
+
 bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
