@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-routing", action="store_true", help="skip the large-T routing bandwidth section")
+    ap.add_argument("--no-backward", action="store_true", help="skip the FFN backward section")
     ap.add_argument("--routing-only", action="store_true",
                     help="only the large-T routing bandwidth section (prints it as JSON; for profiling)")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
@@ -229,6 +230,54 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
         (4 * Eg + 8 * kg) * Tg)
     res["group_limited_topk"]["shape"] = "E=256, n_group=8, topk_group=4, k=8, noaux_tc"
     return res
+
+
+def backward_bench(moe, wl, dev, hidden, logits, w13, w2, peaks, steps):
+    """FFN backward (moe_grouped_ffn_backward) on the workload's own routing and a seeded
+    N(0,1) upstream gradient: CUDA-event time per step (no per-kernel events), then a
+    separate pass with per-kernel events. Routed flops per step: FC1 recomputed
+    (2 S H 2I), dA (2 S H I), dX (2 S 2I H), dW2 (2 S H I), dW13 (2 S 2I H) = 16 S H I."""
+    import torch
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    w, idx = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
+    aws = torch.empty(max(1, moe.moe_align_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+    al = moe.moe_align_by_expert(idx, w, E, workspace=aws)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    d_out = torch.randn((T, H), generator=g, device=dev).to(hidden.dtype)
+    ws = torch.empty(moe.moe_grouped_ffn_backward_workspace_size(moe.MOE_BF16, T, H, I, E, k), dtype=torch.uint8,
+                     device=dev)
+    outs = dict(d_hidden=torch.empty_like(hidden), d_w13=torch.empty_like(w13), d_w2=torch.empty_like(w2),
+                d_weights=torch.empty((T, k), dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        moe.moe_grouped_ffn_backward(hidden, w13, w2, k, al["counts"], al["offsets"], al["sorted_token_ids"],
+                                     al["sorted_weights"], al["reverse_indices"], d_out, workspace=ws,
+                                     stream=stream, **outs)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    moe.profiler_enable(True)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    moe.profiler_enable(False)
+    kern = {n: round(v["total_ms"] / steps, 4) for n, v in moe.profiler_report().items()}
+    flops = 16.0 * T * k * H * I
+    tf = flops / (ms / 1e3) / 1e12
+    return {"ms_per_step": ms, "tflops": tf, "peak_tflops": peaks["bf16_tflops"],
+            "frac": tf / peaks["bf16_tflops"], "flops_per_step": flops,
+            "flops": "routed work 16*S*H*I (FC1 recomputed, dA, dX, dW2, dW13)", "kernels_ms": kern,
+            "timing": "CUDA events over %d steps after 3 warm-up steps; kernels_ms from a second pass" % steps}
 
 
 def kernel_traffic(kernel, workload):
@@ -545,6 +594,8 @@ def main():
             "gpu_launches_per_step": launches, "clocks": clocks, "e2e": e2e, "lib": moe.version()}
     if not args.no_routing:
         line["routing"] = routing_bandwidth(moe, wl, dev, peaks)
+    if not args.no_backward and wl.dtype == "bf16" and H % 64 == 0 and I % 64 == 0:
+        line["backward"] = backward_bench(moe, wl, dev, hidden, logits, w13, w2, peaks, max(3, min(args.steps, 10)))
     if not args.no_cpu_baseline:
         try:
             line["cpu_baseline"] = cpu_baseline(wl, hidden, logits, w13, w2)
