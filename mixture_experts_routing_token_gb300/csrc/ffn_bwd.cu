@@ -108,8 +108,15 @@ __device__ __forceinline__ BTile btile(int t, const int* tile_start, const BwdPa
   BTile d;
   d.e = lo;
   if (KIND == WGRAD) {
-    d.n_tile = local / P.MT;
-    d.m_tile = local - d.n_tile * P.MT;
+    // the operand with more columns is walked once (outer), the other one sweeps
+    // past it (inner) and stays in L2 across the concurrently running tiles
+    if (P.M_dim >= P.N_dim) {
+      d.m_tile = local / P.NT;
+      d.n_tile = local - d.m_tile * P.NT;
+    } else {
+      d.n_tile = local / P.MT;
+      d.m_tile = local - d.n_tile * P.MT;
+    }
     d.ksteps = (__ldg(P.poff + lo + 1) - __ldg(P.poff + lo)) / BK;
   } else {
     const int mt = (__ldg(P.counts + lo) + 2 * BM - 1) / (2 * BM);

@@ -56,8 +56,13 @@ __device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
+// Arrive on an mbarrier of another CTA of the cluster. Used by the epilogue warps to
+// hand a TMEM accumulator back to the MMA issuer: the tcgen05 loads are complete
+// (tcgen05.wait::ld) and ordered by tcgen05.fence::before_thread_sync, so only
+// CTA-scope release is needed; a cluster-scope release would also wait for the
+// epilogue's global stores to drain before every hand-back.
 __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 
