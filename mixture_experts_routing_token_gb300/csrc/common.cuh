@@ -124,14 +124,16 @@ struct FfnBwdArgs {
   void* xs;         // [P, H] bf16, P = bwd_padded_rows(S, E)
   void* dos;        // [P, H] bf16
   void* dys;        // [P, H] bf16
-  float* gu;        // [P, 2I]
+  float* gu;        // [P, 2I] (separate recompute / dA path only, else null)
   void* act;        // [P, I] bf16
   void* dgu;        // [P, 2I] bf16
-  float* dwp;       // [P, ceil(I / 256)]
+  float* dwp;       // [P, ceil(I / 128)]
   float* staging;   // [S, H]
   int32_t* status;
 };
 long bwd_padded_rows(long S, int E);
+// FC1 recompute and dA in one kernel (no gu buffer) for this H.
+bool bwd_uses_fused(int H);
 int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s);
 
 bool ffn_uses_tensor_cores(int dtype, int H, int I);

@@ -21,9 +21,13 @@
 // dependency, as in the forward):
 //   bwd_pad         poff from counts;
 //   bwd_gather      xs = hidden rows, dos = dO rows, dys = w_p dO rows (bf16);
+// then, for H above kFusedMaxH:
 //   RECOMPUTE       [g u] = xs W13^T -> gu (f32), act = bf16(silu(g) u);
 //   DGRAD_A         G = dos W2 (B MN-major) -> dgu = bf16([dg du]) with
 //                   da = w_p G, and per-tile partials of d w_p = <G, act>;
+// or, for H up to kFusedMaxH, both in one kernel:
+//   FUSED_A         per tile G and [g u] into TMEM, the same epilogue outputs
+//                   without the f32 gu round trip through HBM;
 //   zero_dropped    (staging rows of dropped slots);
 //   DGRAD_X         dgu W13 (B MN-major) -> staging[reverse[p]] (f32);
 //   combine         d_hidden[t] = sum_j staging[t k + j];
@@ -57,6 +61,7 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int kRowPad = 64;
 constexpr uint32_t kMnBlock = 64 * BK * 2;   // bytes between the two 64-column MN boxes
+constexpr int kFusedMaxH = 3072;
 
 enum { RECOMPUTE = 0, DGRAD_A = 1, DGRAD_X = 2, WGRAD = 3 };
 
@@ -438,6 +443,251 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (tid == 0 && abort_flag && P.status) atomicOr(P.status, MOE_STATUS_TIMEOUT);
 }
 
+// ---- FC1 recomputed and dA, fused ----------------------------------------------
+//
+// One tile = 256 padded rows x 128 features of expert e. The leader issues two
+// MMA phases per tile:
+//   G phase:  G = dO rows . W2[e][:, features]      N = 128, W2 as an MN-major
+//             B operand (each SM holds 64 of the 128 columns);
+//   gu phase: [g | u] = x rows . [W1; W3][e]^T      N = 256, gate rows of the
+//             128 features on SM 0, the matching up rows on SM 1 (as FC1).
+// TMEM: [g | u] in columns 0..255 (one buffer), G in 256..383 and 384..511
+// (two buffers), so the next tile's G phase runs while the epilogue drains the
+// current tile. The epilogue forms s = sigmoid(g), a = bf16(g s u) (written:
+// the dW2 operand), the partial <G, a> of d w_p, da = w_p G, and writes
+// dg = da u s (1 + g (1 - s)), du = da g s as bf16.
+constexpr int FA_FEAT = 128;
+constexpr int FA_G_BYTES = (FA_FEAT / 2) * BK * 2;   // this SM's 64 columns of W2 per k-step
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    bwd_fused_a_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2,
+                       const BwdParams P) {
+  constexpr uint32_t IDESC_G = idesc_bf16_f32_major(2 * BM, FA_FEAT, 0, 1);
+  constexpr uint32_t IDESC_GU = idesc_bf16_f32_major(2 * BM, BN, 0, 0);
+  __shared__ __align__(8) uint64_t full_bar[NSTAGE], empty_bar[NSTAGE];
+  __shared__ __align__(8) uint64_t tfull_bar, gu_empty_bar, g_empty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int tile_start[MOE_MAX_EXPERTS + 1];
+  extern __shared__ uint8_t dsmem_raw[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const uint32_t dsmem = (ptx::smem_u32(dsmem_raw) + 1023u) & ~1023u;
+  auto sA = [&](int s) { return dsmem + (uint32_t)(s * STAGE); };
+  auto sB = [&](int s) { return dsmem + (uint32_t)(s * STAGE + A_BYTES); };
+  volatile int* abort_p = &abort_flag;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&tfull_bar), 1);
+    ptx::mbar_init(ptx::smem_u32(&gu_empty_bar), 8);
+    ptx::mbar_init(ptx::smem_u32(&g_empty_bar[0]), 8);
+    ptx::mbar_init(ptx::smem_u32(&g_empty_bar[1]), 8);
+    ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmX);
+    ptx::prefetch_tmap(&tmDO);
+    ptx::prefetch_tmap(&tmW13);
+    ptx::prefetch_tmap(&tmW2);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     ptx::smem_u32(&tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  ptx::tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  if (warp == 2) {     // tile_start[e] = tiles of the experts before e
+    const int per = (P.E + 31) / 32;
+    const int e0 = min(P.E, lane * per), e1 = min(P.E, e0 + per);
+    int run = 0;
+    for (int e = e0; e < e1; ++e) run += expert_tiles<DGRAD_X>(__ldg(P.counts + e), P);
+    int incl = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int acc = incl - run;
+    for (int e = e0; e < e1; ++e) {
+      tile_start[e] = acc;
+      acc += expert_tiles<DGRAD_X>(__ldg(P.counts + e), P);
+    }
+    if (lane == 31) tile_start[P.E] = incl;
+  }
+  __syncthreads();
+  const uint32_t tmem_base = tmem_slot;
+  const int total = tile_start[P.E];
+  const int KB = P.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int t = cluster_id; t < total; t += nclusters) {
+        const BTile ti = btile<DGRAD_X>(t, tile_start, P);
+        const int a_row = __ldg(P.poff + ti.e) + ti.m_tile * (2 * BM) + (int)rank * BM;
+        for (int step = 0; step < 2 * KB; ++step) {
+          const bool gphase = step < KB;
+          const int kb = gphase ? step : step - KB;
+          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, WAIT_NS)) goto producer_done;
+          const uint32_t fb_local = ptx::smem_u32(&full_bar[stage]);
+          if (leader) ptx::mbar_arrive_expect_tx(fb_local, gphase ? 2 * (A_BYTES + FA_G_BYTES) : 2 * STAGE);
+          const uint32_t fb = map_to_rank(fb_local, 0);
+          if (gphase) {
+            tma_load_2d_pair(sA(stage), &tmDO, kb * BK, a_row, fb);
+            tma_load_2d_pair(sB(stage), &tmW2, ti.n_tile * FA_FEAT + (int)rank * (FA_FEAT / 2), ti.e * P.H + kb * BK,
+                             fb);
+          } else {
+            tma_load_2d_pair(sA(stage), &tmX, kb * BK, a_row, fb);
+            tma_load_2d_pair(sB(stage), &tmW13, kb * BK,
+                             ti.e * 2 * P.I + ti.n_tile * FA_FEAT + (leader ? 0 : P.I), fb);
+          }
+          if (++stage == NSTAGE) { stage = 0; ph ^= 1u; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < total && ok; t += nclusters, ++it) {
+        const uint32_t gb = it & 1u;
+        for (int phase = 0; phase < 2 && ok; ++phase) {
+          uint32_t d_tmem;
+          if (phase == 0) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&g_empty_bar[gb]), ((it >> 1) & 1u) ^ 1u, abort_p, WAIT_NS)) {
+              ok = false;
+              break;
+            }
+            d_tmem = tmem_base + (uint32_t)(BN + gb * FA_FEAT);
+          } else {
+            if (!ptx::mbar_wait(ptx::smem_u32(&gu_empty_bar), (it & 1u) ^ 1u, abort_p, WAIT_NS)) {
+              ok = false;
+              break;
+            }
+            d_tmem = tmem_base;
+          }
+          ptx::tc_fence_after();
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, WAIT_NS)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a0 = sA(stage), b0 = sB(stage);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if (phase == 0)
+                mma_pair(d_tmem, ptx::sdesc_k128(a0 + kk * 32), sdesc_mn128(b0 + kk * 2048, kMnBlock), IDESC_G,
+                         (kb | kk) != 0);
+              else
+                mma_pair(d_tmem, ptx::sdesc_k128(a0 + kk * 32), ptx::sdesc_k128(b0 + kk * 32), IDESC_GU,
+                         (kb | kk) != 0);
+            }
+            commit_pair(ptx::smem_u32(&empty_bar[stage]), 0x3);
+            if (++stage == NSTAGE) { stage = 0; ph ^= 1u; }
+          }
+        }
+        if (ok) commit_pair(ptx::smem_u32(&tfull_bar), 0x3);
+      }
+      commit_pair(ptx::smem_u32(&drain_bar), 0x1);
+      int dummy = 0;
+      ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, &dummy, WAIT_NS);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    uint32_t it = 0;
+    for (int t = cluster_id; t < total; t += nclusters, ++it) {
+      const BTile ti = btile<DGRAD_X>(t, tile_start, P);
+      if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar), it & 1u, abort_p, WAIT_NS)) break;
+      ptx::tc_fence_after();
+      const uint32_t gb = it & 1u;
+      const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+      const int cnt = __ldg(P.counts + ti.e);
+      const int pcnt = __ldg(P.poff + ti.e + 1) - __ldg(P.poff + ti.e);
+      const int r = ti.m_tile * (2 * BM) + (int)rank * BM + row;
+      const bool in_seg = r < pcnt;
+      const bool real = r < cnt;
+      const long pp = (long)__ldg(P.poff + ti.e) + r;
+      const int I = P.I;
+      const float wp = real ? __ldg(P.sorted_w + __ldg(P.offsets + ti.e) + r) : 0.0f;
+      float dot = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < FA_FEAT / 32; ++c) {
+        uint32_t G[32], g[32], u[32];
+        ptx::tmem_ld32(lane_base + BN + gb * FA_FEAT + c * 32, G);
+        ptx::tmem_ld32(lane_base + c * 32, g);
+        ptx::tmem_ld32(lane_base + 128 + c * 32, u);
+        ptx::tmem_ld_wait();
+        const int i0 = ti.n_tile * FA_FEAT + c * 32;
+        if (in_seg && i0 < I) {
+          float av[32], dg[32], du[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]), Gv = __uint_as_float(G[i]);
+            const float s = 1.0f / (1.0f + expf(-gv));
+            const float a = __bfloat162float(__float2bfloat16_rn(gv * s * uv));
+            av[i] = a;
+            dot = fmaf(Gv, a, dot);
+            const float da = wp * Gv;
+            dg[i] = da * uv * s * (1.0f + gv * (1.0f - s));
+            du[i] = da * gv * s;
+          }
+          store_bf16x32(P.act + pp * I + i0, av);
+          store_bf16x32(P.dgu + pp * 2 * I + i0, dg);
+          store_bf16x32(P.dgu + pp * 2 * I + I + i0, du);
+        }
+      }
+      if (in_seg) P.dwp[pp * P.NT + ti.n_tile] = dot;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        arrive_remote(map_to_rank(ptx::smem_u32(&gu_empty_bar), 0));
+        arrive_remote(map_to_rank(ptx::smem_u32(&g_empty_bar[gb]), 0));
+      }
+    }
+  }
+
+  if (*abort_p) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 1000000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+  if (tid == 0 && abort_flag && P.status) atomicOr(P.status, MOE_STATUS_TIMEOUT);
+}
+
 // ---- small kernels ------------------------------------------------------------
 
 // poff[e] = sum over e' < e of counts[e'] rounded up to kRowPad; one CTA of 1024 threads.
@@ -518,7 +768,7 @@ __global__ void __launch_bounds__(256) bwd_gather_kernel(
   }
 }
 
-// d_weights[reverse[p]] = sum over the DGRAD_A N tiles of the row's partial dot.
+// d_weights[reverse[p]] = sum over the row's partial dots (one per feature tile of dA).
 __global__ void __launch_bounds__(256) bwd_dw_reduce_kernel(const int32_t* __restrict__ offsets,
                                                             const int32_t* __restrict__ poff,
                                                             const int32_t* __restrict__ reverse,
@@ -578,6 +828,25 @@ int launch_bwd_pair(const CUtensorMap& a, const CUtensorMap& b, const BwdParams&
   return check_launch(name);
 }
 
+int launch_fused_a(const CUtensorMap& x, const CUtensorMap& dO, const CUtensorMap& w13, const CUtensorMap& w2,
+                   const BwdParams& p, long max_tiles, cudaStream_t s) {
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    if (cudaFuncSetAttribute(bwd_fused_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DSMEM) !=
+        cudaSuccess)
+      return check_launch("bwd_fc1_dact");
+    attr[dev] = true;
+  }
+  const int grid = 2 * (int)std::min(max_tiles, (long)(num_sms() / 2));
+  if (grid <= 0) return MOE_OK;
+  ProfScope ps("bwd_fc1_dact", s);
+  const cudaError_t e = launch_pdl(bwd_fused_a_kernel, grid, THREADS, DSMEM, s, x, dO, w13, w2, p);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "bwd_fc1_dact: %s", cudaGetErrorString(e));
+  return check_launch("bwd_fc1_dact");
+}
+
 template <typename... KArgs, typename... Args>
 int launch_small(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                  Args&&... args) {
@@ -590,6 +859,11 @@ int launch_small(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 blo
 }  // namespace
 
 long bwd_padded_rows(long S, int E) { return S + (long)kRowPad * E; }
+
+// FC1 recompute and dA in one kernel for H up to this (measured: H = 2048 layers
+// gain, where the separate dA epilogue's gu / act reads outweigh its MMAs; at
+// H = 4096 the fused kernel's N = 128 G phase costs more than the round trip).
+bool bwd_uses_fused(int H) { return H <= kFusedMaxH; }
 
 int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
   const long S = (long)a.T * a.k;
@@ -627,23 +901,35 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
   p.dwp = a.dwp;
   p.staging = a.staging;
   p.status = a.status;
-  const int nt_a = (I + BN - 1) / BN;
+  const bool fused = bwd_uses_fused(H);
+  const int nt_a = fused ? (I + FA_FEAT - 1) / FA_FEAT : (I + BN - 1) / BN;
 
-  // FC1 recomputed: gate / up pre-activations and the bf16 activation
-  if ((rc = make_tmap(&ta, a.xs, (uint64_t)Pmax, (uint64_t)H, 128))) return rc;
-  if ((rc = make_tmap(&tb, a.w13, (uint64_t)E * 2 * I, (uint64_t)H, 128))) return rc;
-  p.K = H;
-  p.NT = (I + 127) / 128;
-  p.b_rows = 2 * I;
-  if ((rc = launch_bwd_pair<RECOMPUTE>(ta, tb, p, row_tiles * p.NT, s, "bwd_fc1_recompute"))) return rc;
+  if (fused) {   // FC1 recomputed and G = dO W2 in one kernel
+    CUtensorMap tx, tdo, tw13, tw2;
+    if ((rc = make_tmap(&tx, a.xs, (uint64_t)Pmax, (uint64_t)H, 128))) return rc;
+    if ((rc = make_tmap(&tdo, a.dos, (uint64_t)Pmax, (uint64_t)H, 128))) return rc;
+    if ((rc = make_tmap(&tw13, a.w13, (uint64_t)E * 2 * I, (uint64_t)H, 128))) return rc;
+    if ((rc = make_tmap(&tw2, a.w2, (uint64_t)E * H, (uint64_t)I, 64))) return rc;
+    p.K = H;
+    p.NT = nt_a;
+    if ((rc = launch_fused_a(tx, tdo, tw13, tw2, p, row_tiles * p.NT, s))) return rc;
+  } else {
+    // FC1 recomputed: gate / up pre-activations and the bf16 activation
+    if ((rc = make_tmap(&ta, a.xs, (uint64_t)Pmax, (uint64_t)H, 128))) return rc;
+    if ((rc = make_tmap(&tb, a.w13, (uint64_t)E * 2 * I, (uint64_t)H, 128))) return rc;
+    p.K = H;
+    p.NT = (I + 127) / 128;
+    p.b_rows = 2 * I;
+    if ((rc = launch_bwd_pair<RECOMPUTE>(ta, tb, p, row_tiles * p.NT, s, "bwd_fc1_recompute"))) return rc;
 
-  // G = dO W2; dgu and the d w_p partials
-  if ((rc = make_tmap(&ta, a.dos, (uint64_t)Pmax, (uint64_t)H, 128))) return rc;
-  if ((rc = make_tmap(&tb, a.w2, (uint64_t)E * H, (uint64_t)I, 64))) return rc;
-  p.K = H;
-  p.NT = nt_a;
-  p.b_rows = H;
-  if ((rc = launch_bwd_pair<DGRAD_A>(ta, tb, p, row_tiles * p.NT, s, "bwd_dgrad_act"))) return rc;
+    // G = dO W2; dgu and the d w_p partials
+    if ((rc = make_tmap(&ta, a.dos, (uint64_t)Pmax, (uint64_t)H, 128))) return rc;
+    if ((rc = make_tmap(&tb, a.w2, (uint64_t)E * H, (uint64_t)I, 64))) return rc;
+    p.K = H;
+    p.NT = nt_a;
+    p.b_rows = H;
+    if ((rc = launch_bwd_pair<DGRAD_A>(ta, tb, p, row_tiles * p.NT, s, "bwd_dgrad_act"))) return rc;
+  }
 
   // dx = dgu W13 into the slot rows, then the sum over k
   if ((rc = launch_zero_dropped(a.offsets, E, S, H, a.staging, s))) return rc;

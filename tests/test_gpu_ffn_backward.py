@@ -48,6 +48,9 @@ def _check(moe, d, al, k, seed, workspace=None):
     (513, 320, 640, 5, 3),       # H % 256 == 64: partial dx / dW tiles
     (40, 128, 128, 256, 2),      # 80 slots over 256 experts: most experts have no rows
     (5, 128, 192, 8, 2),         # a few tokens
+    # H above 3072: FC1 recompute and dA as two kernels (f32 gate/up buffer) instead of one
+    (300, 4096, 256, 8, 2),
+    (200, 3200, 384, 4, 3),      # H % 256 == 128
 ])
 def test_backward_shapes(T, H, I, E, k):
     moe = need_gpu()
