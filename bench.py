@@ -41,6 +41,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-routing", action="store_true", help="skip the large-T routing bandwidth section")
     ap.add_argument("--no-backward", action="store_true", help="skip the FFN backward section")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="only the FFN backward section (for profiling captures)")
+    ap.add_argument("--tokens", type=int, default=None, help="override the workload's T (profiling captures)")
+    ap.add_argument("--experts", type=int, default=None, help="override the workload's E (profiling captures)")
+    ap.add_argument("--topk", type=int, default=None, help="override the workload's k (profiling captures)")
     ap.add_argument("--routing-only", action="store_true",
                     help="only the large-T routing bandwidth section (prints it as JSON; for profiling)")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
@@ -406,6 +411,10 @@ def run_reference(args, wl, rank, world):
 def main():
     args = parse()
     wl = WORKLOADS[args.workload]
+    if args.tokens or args.experts or args.topk:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=wl.name + "_reduced", T=args.tokens or wl.T, E=args.experts or wl.E,
+                                 k=args.topk or wl.k)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, wl, rank, world)
@@ -431,6 +440,12 @@ def main():
         return
     hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=rank)
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    if args.backward_only:
+        if rank == 0:
+            print(json.dumps({"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
+                              "backward": backward_bench(moe, wl, dev, hidden, logits, w13, w2, measured_peaks(),
+                                                         max(3, min(args.steps, 10)))}), flush=True)
+        return
     dcode = moe.MOE_BF16 if wl.dtype == "bf16" else moe.MOE_F32
     ws = torch.empty(moe.moe_layer_workspace_size(dcode, T, H, I, E, k), dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=hidden.dtype, device=dev)

@@ -96,12 +96,18 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t* __restrict__ 
   }
 }
 
-// Loads of the routing (indices, weights): through the read-only path normally,
-// through L2 when the same kernel has just written them (fused small batches).
-template <bool FRESH>
-__device__ __forceinline__ int load_i(const int32_t* p) { return FRESH ? __ldcg(p) : __ldg(p); }
-template <bool FRESH>
-__device__ __forceinline__ float load_f(const float* p) { return FRESH ? __ldcg(p) : __ldg(p); }
+// Where align_chunk reads the routing (indices, weights) from: global memory
+// through the read-only path, global memory through L2 (the same kernel has
+// just written it), or a shared-memory copy made by the same CTA.
+enum { kSrcGlobal = 0, kSrcFresh = 1, kSrcShared = 2 };
+template <int SRC>
+__device__ __forceinline__ int load_i(const int32_t* p) {
+  return SRC == kSrcShared ? *p : (SRC == kSrcFresh ? __ldcg(p) : __ldg(p));
+}
+template <int SRC>
+__device__ __forceinline__ float load_f(const float* p) {
+  return SRC == kSrcShared ? *p : (SRC == kSrcFresh ? __ldcg(p) : __ldg(p));
+}
 
 // Exclusive scan of v[0..n) in place by warp 0 (lane l owns a run of entries);
 // returns the total in lane 31.
@@ -134,7 +140,7 @@ __device__ __forceinline__ int warp0_exclusive_scan(int* v, int n) {
 // e's slots. Slots are ranked into the staging arrays in expert-sorted order,
 // then each expert's run is copied to its global positions by consecutive
 // threads (coalesced stores).
-template <bool FRESH>
+template <int SRC>
 __device__ __forceinline__ void align_chunk(
     int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
     const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -179,7 +185,7 @@ __device__ __forceinline__ void align_chunk(
     __syncthreads();
     bool bad = false;
     for (long s = lo + tid; s < hi; s += kThreads) {
-      const int e = load_i<FRESH>(idx + s);
+      const int e = load_i<SRC>(idx + s);
       if (e >= 0 && e < E) atomicAdd(&off[e], 1);
       else bad = true;
     }
@@ -223,8 +229,8 @@ __device__ __forceinline__ void align_chunk(
 #pragma unroll
     for (int u = 0; u < kSpt; ++u) {
       const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
-      eu[u] = s < hi ? load_i<FRESH>(idx + s) : -1;
-      wu[u] = s < hi ? load_f<FRESH>(wts + s) : 0.0f;
+      eu[u] = s < hi ? load_i<SRC>(idx + s) : -1;
+      wu[u] = s < hi ? load_f<SRC>(wts + s) : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < kSpt; ++u) {
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
   extern __shared__ int sm[];
-  align_chunk<false>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
+  align_chunk<kSrcGlobal>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
                      sorted_ids, sorted_w, reverse, status, sm);
 }
 
@@ -303,12 +309,16 @@ __global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
   extern __shared__ int sm[];
   pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
   float* col = reinterpret_cast<float*>(sm);
+  int* asm_ = sm + EP * gate::kStageLd;                       // align_chunk's shared memory
+  int32_t* s_idx = asm_ + align_smem_bytes(E) / sizeof(int);  // shared copies of the routing
+  float* s_w = reinterpret_cast<float*>(s_idx + T * k);
   gate::stage_rows<EP>(logits, 0, T, E, col, threadIdx.x, kThreads);
   __syncthreads();
-  if ((int)threadIdx.x < T) gate::topk_staged_row<EP>(col, threadIdx.x, threadIdx.x, E, k, norm, w_out, idx_out);
+  if ((int)threadIdx.x < T)
+    gate::topk_staged_row<EP>(col, threadIdx.x, threadIdx.x, E, k, norm, w_out, idx_out, s_w, s_idx);
   __syncthreads();
-  align_chunk<true>(0, idx_out, w_out, (long)T * k, k, E, 1, 0, nullptr, counts, offsets, sorted_ids,
-                    sorted_w, reverse, status, sm + EP * gate::kStageLd);
+  align_chunk<kSrcShared>(0, s_idx, s_w, (long)T * k, k, E, 1, 0, nullptr, counts, offsets, sorted_ids,
+                          sorted_w, reverse, status, asm_);
 }
 
 template <int L, int V>
@@ -322,7 +332,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(
   for (long t = threadIdx.x / L; t < T; t += groups)
     gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
   __syncthreads();
-  align_chunk<true>(0, idx_out, w_out, (long)T * k, k, E, 1, 0, nullptr, counts, offsets, sorted_ids,
+  align_chunk<kSrcFresh>(0, idx_out, w_out, (long)T * k, k, E, 1, 0, nullptr, counts, offsets, sorted_ids,
                     sorted_w, reverse, status, sm);
 }
 
@@ -349,9 +359,10 @@ int launch_route_staged(const float* logits, int T, int E, int k, int norm, floa
                         int32_t* reverse, int32_t* status, cudaStream_t s) {
   static bool attr[64] = {};
   const size_t stage = (size_t)EP * gate::kStageLd * sizeof(float);
-  return launch_route_small_k(route_small_staged_kernel<EP>, stage + align_smem_bytes(E),
-                              stage + align_smem_bytes(EP), logits, T, E, k, norm, w, idx, counts, offsets,
-                              sorted_ids, sorted_w, reverse, status, s, attr);
+  const size_t copies = (size_t)T * k * (sizeof(int32_t) + sizeof(float));
+  return launch_route_small_k(route_small_staged_kernel<EP>, stage + align_smem_bytes(E) + copies,
+                              stage + align_smem_bytes(EP) + (size_t)kChunk * 8, logits, T, E, k, norm, w, idx,
+                              counts, offsets, sorted_ids, sorted_w, reverse, status, s, attr);
 }
 
 template <int V>

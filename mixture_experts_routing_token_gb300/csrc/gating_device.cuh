@@ -237,10 +237,13 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
     for (int e = E; e < EP; ++e) col[e * kStageLd + tid] = -INFINITY;
 }
 
-// Top-k and softmax of staged row r (called by one thread), written as token t.
+// Top-k and softmax of staged row r (called by one thread), written as token t. With
+// s_w / s_idx (shared memory, indexed like the outputs) the results are also kept
+// there, and the finishing pass reads the raw logits back from s_w instead of w_out.
 template <int EP>
 __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E, int k, int norm,
-                                                float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+                                                float* __restrict__ w_out, int32_t* __restrict__ idx_out,
+                                                float* s_w = nullptr, int32_t* s_idx = nullptr) {
   constexpr int G = EP / 8;
   auto at = [&](int i) -> float& { return col[i * kStageLd + r]; };
   float gv[G];
@@ -283,10 +286,20 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
       if (g == bg) { gv[g] = nv; gi[g] = ni; }
     if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
     idx_out[t * k + j] = bi;
-    w_out[t * k + j] = bv;
+    if (s_w) {
+      s_idx[t * k + j] = bi;
+      s_w[t * k + j] = bv;
+    } else {
+      w_out[t * k + j] = bv;
+    }
   }
   const float denom = hi + lo;
-  for (int j = 0; j < k; ++j) w_out[t * k + j] = __fdiv_rn(exp_diff(w_out[t * k + j], m), denom);
+  for (int j = 0; j < k; ++j) {
+    const float x = s_w ? s_w[t * k + j] : w_out[t * k + j];
+    const float wj = __fdiv_rn(exp_diff(x, m), denom);
+    w_out[t * k + j] = wj;
+    if (s_w) s_w[t * k + j] = wj;
+  }
 }
 
 }  // namespace gate
