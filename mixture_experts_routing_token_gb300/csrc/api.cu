@@ -355,7 +355,7 @@ size_t carve_bwd(Carver& c, FfnBwdArgs* a, long S, int H, int I, int E) {
   float* gu = bwd_uses_fused(H) ? nullptr : c.take<float>((size_t)P * 2 * I);
   void* act = c.take<uint16_t>((size_t)P * I);
   void* dgu = c.take<uint16_t>((size_t)P * 2 * I);
-  float* dwp = c.take<float>((size_t)P * ((I + 127) / 128));
+  float* dwp = c.take<float>((size_t)P * 2 * ((I + 127) / 128));
   float* staging = c.take<float>((size_t)S * H);
   if (a) {
     a->poff = poff;

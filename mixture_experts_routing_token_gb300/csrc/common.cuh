@@ -127,7 +127,7 @@ struct FfnBwdArgs {
   float* gu;        // [P, 2I] (separate recompute / dA path only, else null)
   void* act;        // [P, I] bf16
   void* dgu;        // [P, 2I] bf16
-  float* dwp;       // [P, ceil(I / 128)]
+  float* dwp;       // [P, 2 ceil(I / 128)]: one partial per feature tile and epilogue half
   float* staging;   // [S, H]
   int32_t* status;
 };

@@ -56,14 +56,23 @@ constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE = A_BYTES + B_BYTES;
 constexpr int DSMEM = NSTAGE * STAGE + 1024;
-constexpr int THREADS = 192;
+// Epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter, each
+// draining every other 32-column chunk). The recompute / dA epilogues, which
+// move several values per output element, measured faster with 8; the dX and
+// weight-gradient ones with 4.
+constexpr int MAX_THREADS = (2 + 8) * 32;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int kRowPad = 64;
 constexpr uint32_t kMnBlock = 64 * BK * 2;   // bytes between the two 64-column MN boxes
 constexpr int kFusedMaxH = 3072;
 
-enum { RECOMPUTE = 0, DGRAD_A = 1, DGRAD_X = 2, WGRAD = 3 };
+enum { RECOMPUTE = 0, DGRAD_A = 1, DGRAD_X = 2, WGRAD = 3, FUSED_A = 4 };
+
+template <int KIND>
+constexpr int epi_warps() { return (KIND == RECOMPUTE || KIND == DGRAD_A || KIND == FUSED_A) ? 8 : 4; }
+template <int KIND>
+constexpr int kind_threads() { return (2 + epi_warps<KIND>()) * 32; }
 
 template <int KIND>
 struct Major {
@@ -174,7 +183,7 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[
 }
 
 template <int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAX_THREADS, 1)
     bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const BwdParams P) {
   constexpr int A_MN = Major<KIND>::a_mn, B_MN = Major<KIND>::b_mn;
@@ -202,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
-      ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 8);
+      ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 2 * epi_warps<KIND>());
     }
     ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
     abort_flag = 0;
@@ -318,7 +327,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    constexpr int NH = epi_warps<KIND>() / 4;   // warps per lane quarter
+    const int half = (warp - 2) >> 2;           // which 32-column chunks it drains
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
@@ -331,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int m = ti.m_tile * (2 * BM) + (int)rank * BM + row;
         __nv_bfloat16* dst = P.dw + ((long)ti.e * P.M_dim + m) * P.N_dim;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half; c < BN / 32; c += NH) {
           uint32_t y[32];
           ptx::tmem_ld32(taddr + c * 32, y);
           ptx::tmem_ld_wait();
@@ -353,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int I = P.I, H = P.H;
         if (KIND == RECOMPUTE) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = half; c < 4; c += NH) {
             uint32_t g[32], u[32];
             ptx::tmem_ld32(taddr + c * 32, g);
             ptx::tmem_ld32(taddr + 128 + c * 32, u);
@@ -376,7 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const float wp = real ? __ldg(P.sorted_w + __ldg(P.offsets + ti.e) + r) : 0.0f;
           float dot = 0.0f;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = half; c < BN / 32; c += NH) {
             uint32_t G[32];
             ptx::tmem_ld32(taddr + c * 32, G);
             ptx::tmem_ld_wait();
@@ -402,11 +413,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               store_bf16x32(P.dgu + pp * 2 * I + I + i0, uv);
             }
           }
-          if (in_seg) P.dwp[pp * P.NT + ti.n_tile] = dot;
+          if (in_seg) P.dwp[(pp * P.NT + ti.n_tile) * 2 + half] = dot;
         } else {   // DGRAD_X
           const long dst_row = real ? (long)__ldg(P.reverse + __ldg(P.offsets + ti.e) + r) : 0;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = half; c < BN / 32; c += NH) {
             uint32_t y[32];
             ptx::tmem_ld32(taddr + c * 32, y);
             ptx::tmem_ld_wait();
@@ -459,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 constexpr int FA_FEAT = 128;
 constexpr int FA_G_BYTES = (FA_FEAT / 2) * BK * 2;   // this SM's 64 columns of W2 per k-step
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAX_THREADS, 1)
     bwd_fused_a_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2,
                        const BwdParams P) {
@@ -487,9 +498,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&tfull_bar), 1);
-    ptx::mbar_init(ptx::smem_u32(&gu_empty_bar), 8);
-    ptx::mbar_init(ptx::smem_u32(&g_empty_bar[0]), 8);
-    ptx::mbar_init(ptx::smem_u32(&g_empty_bar[1]), 8);
+    ptx::mbar_init(ptx::smem_u32(&gu_empty_bar), 2 * epi_warps<FUSED_A>());
+    ptx::mbar_init(ptx::smem_u32(&g_empty_bar[0]), 2 * epi_warps<FUSED_A>());
+    ptx::mbar_init(ptx::smem_u32(&g_empty_bar[1]), 2 * epi_warps<FUSED_A>());
     ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
     abort_flag = 0;
     ptx::fence_mbar_init();
@@ -618,7 +629,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2;    // which 32-column chunks it drains (every other one)
     const int row = q * 32 + lane;
     uint32_t it = 0;
     for (int t = cluster_id; t < total; t += nclusters, ++it) {
@@ -637,7 +649,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const float wp = real ? __ldg(P.sorted_w + __ldg(P.offsets + ti.e) + r) : 0.0f;
       float dot = 0.0f;
 #pragma unroll 1
-      for (int c = 0; c < FA_FEAT / 32; ++c) {
+      for (int c = half; c < FA_FEAT / 32; c += 2) {
         uint32_t G[32], g[32], u[32];
         ptx::tmem_ld32(lane_base + BN + gb * FA_FEAT + c * 32, G);
         ptx::tmem_ld32(lane_base + c * 32, g);
@@ -662,7 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           store_bf16x32(P.dgu + pp * 2 * I + I + i0, du);
         }
       }
-      if (in_seg) P.dwp[pp * P.NT + ti.n_tile] = dot;
+      if (in_seg) P.dwp[(pp * P.NT + ti.n_tile) * 2 + half] = dot;
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -823,7 +835,7 @@ int launch_bwd_pair(const CUtensorMap& a, const CUtensorMap& b, const BwdParams&
   const int grid = 2 * (int)std::min(max_tiles, pairs);
   if (grid <= 0) return MOE_OK;
   ProfScope ps(name, s);
-  const cudaError_t e = launch_pdl(bwd_pair_kernel<KIND>, grid, THREADS, DSMEM, s, a, b, p);
+  const cudaError_t e = launch_pdl(bwd_pair_kernel<KIND>, grid, kind_threads<KIND>(), DSMEM, s, a, b, p);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
   return check_launch(name);
 }
@@ -842,7 +854,7 @@ int launch_fused_a(const CUtensorMap& x, const CUtensorMap& dO, const CUtensorMa
   const int grid = 2 * (int)std::min(max_tiles, (long)(num_sms() / 2));
   if (grid <= 0) return MOE_OK;
   ProfScope ps("bwd_fc1_dact", s);
-  const cudaError_t e = launch_pdl(bwd_fused_a_kernel, grid, THREADS, DSMEM, s, x, dO, w13, w2, p);
+  const cudaError_t e = launch_pdl(bwd_fused_a_kernel, grid, kind_threads<FUSED_A>(), DSMEM, s, x, dO, w13, w2, p);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "bwd_fc1_dact: %s", cudaGetErrorString(e));
   return check_launch("bwd_fc1_dact");
 }
@@ -965,7 +977,7 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
   if (a.d_weights) {
     const int grid = (int)std::max(1L, std::min((long)num_sms() * 4, (S + 255) / 256));
     if ((rc = launch_small("bwd_dw_reduce", bwd_dw_reduce_kernel, grid, 256, (E + 1) * sizeof(int), s, a.offsets,
-                           a.poff, a.reverse, a.dwp, E, nt_a, a.d_weights)))
+                           a.poff, a.reverse, a.dwp, E, 2 * nt_a, a.d_weights)))
       return rc;
   }
   return MOE_OK;
