@@ -262,7 +262,7 @@ __device__ __forceinline__ void align_chunk(
       if (e >= 0) {
         const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
         const int q = cpre[e] + wcnt[warp * E + e] + ru[u] - cb[e];   // chunk-local, expert-sorted
-        s_tok[q] = (int)(s / k);
+        s_tok[q] = s <= 0x7fffffffL ? (int)((uint32_t)s / (uint32_t)k) : (int)(s / k);
         s_rev[q] = (int)s;
         s_w[q] = wu[u];
       }

@@ -32,12 +32,12 @@ struct Out4<__nv_bfloat16> {
 
 template <class OutT>
 __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restrict__ staging, long T,
-                                                          int k, int H4, OutT* __restrict__ out) {
+                                                          int k, int H4, OutT* __restrict__ out, int sh) {
   pdl_wait();
   pdl_trigger();
   const long n = T * H4;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const long t = i / H4;
+    const long t = div_idx(i, H4, sh);
     const int c = (int)(i - t * H4);
     const float4* src = staging + t * k * H4 + c;
     float4 acc = __ldcs(src);
@@ -54,12 +54,12 @@ __global__ void __launch_bounds__(256) combine_vec_kernel(const float4* __restri
 
 template <class OutT>
 __global__ void __launch_bounds__(256) combine_scalar_kernel(const float* __restrict__ staging, long T,
-                                                             int k, int H, OutT* __restrict__ out) {
+                                                             int k, int H, OutT* __restrict__ out, int sh) {
   pdl_wait();
   pdl_trigger();
   const long n = T * H;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const long t = i / H;
+    const long t = div_idx(i, H, sh);
     const int h = (int)(i - t * H);
     float acc = staging[t * k * H + h];
     for (int j = 1; j < k; ++j) acc += staging[(t * k + j) * H + h];
@@ -100,9 +100,9 @@ int launch_t(const float* staging, int T, int k, int H, OutT* out, cudaStream_t 
   cudaError_t e;
   if (H % 4 == 0)
     e = launch_pdl(combine_vec_kernel<OutT>, grid, 256, 0, s, reinterpret_cast<const float4*>(staging), (long)T, k,
-                   H / 4, out);
+                   H / 4, out, pow2_shift(H / 4));
   else
-    e = launch_pdl(combine_scalar_kernel<OutT>, grid, 256, 0, s, staging, (long)T, k, H, out);
+    e = launch_pdl(combine_scalar_kernel<OutT>, grid, 256, 0, s, staging, (long)T, k, H, out, pow2_shift(H));
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "combine: %s", cudaGetErrorString(e));
   return check_launch("combine");
 }

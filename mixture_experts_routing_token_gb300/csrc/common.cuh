@@ -20,6 +20,16 @@ int check_launch(const char* what);
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
 
+// Row of a flat grid-stride index: i / d for d > 0. A shift when d is a power of
+// two (sh = log2(d), from pow2_shift on the host), else an unsigned 32-bit
+// division while i fits, else the 64-bit division (a long instruction sequence).
+__device__ __forceinline__ long div_idx(long i, long d, int sh) {
+  if (sh >= 0) return i >> sh;
+  if (i <= 0x7fffffffL && d <= 0x7fffffffL) return (long)((uint32_t)i / (uint32_t)d);
+  return i / d;
+}
+inline int pow2_shift(long d) { return (d > 0 && (d & (d - 1)) == 0) ? __builtin_ctzl((unsigned long)d) : -1; }
+
 // Kernel timing hooks (no-ops unless moe_profiler_enable(1)).
 struct ProfScope {
   ProfScope(const char* name, cudaStream_t s);

@@ -747,8 +747,8 @@ __device__ __forceinline__ int find_segment(const int* seg, int E, int q) {   //
 __global__ void __launch_bounds__(256) bwd_gather_kernel(
     const uint4* __restrict__ hidden, const uint4* __restrict__ dout, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ poff, const int32_t* __restrict__ ids,
-    const float* __restrict__ sw, int E, int H8, long Pmax, uint4* __restrict__ xs, uint4* __restrict__ dos,
-    uint4* __restrict__ dys) {
+    const float* __restrict__ sw, int E, int H8, int sh, long Pmax, uint4* __restrict__ xs,
+    uint4* __restrict__ dos, uint4* __restrict__ dys) {
   extern __shared__ int s_poff[];
   pdl_wait();
   pdl_trigger();
@@ -756,7 +756,7 @@ __global__ void __launch_bounds__(256) bwd_gather_kernel(
   __syncthreads();
   const long n = min(Pmax, (long)s_poff[E]) * H8;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const int q = (int)(i / H8);
+    const int q = (int)div_idx(i, H8, sh);
     const int c = (int)(i - (long)q * H8);
     const int e = find_segment(s_poff, E, q);
     const int r = q - s_poff[e];
@@ -892,7 +892,7 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
     const int grid = (int)std::max(1L, std::min((long)num_sms() * 8, (units + 255) / 256));
     if ((rc = launch_small("bwd_gather", bwd_gather_kernel, grid, 256, (E + 1) * sizeof(int), s,
                            static_cast<const uint4*>(a.hidden), static_cast<const uint4*>(a.d_out), a.counts,
-                           a.offsets, a.poff, a.sorted_ids, a.sorted_w, E, H / 8, Pmax,
+                           a.offsets, a.poff, a.sorted_ids, a.sorted_w, E, H / 8, pow2_shift(H / 8), Pmax,
                            static_cast<uint4*>(a.xs), static_cast<uint4*>(a.dos), static_cast<uint4*>(a.dys))))
       return rc;
   }

@@ -24,14 +24,14 @@ namespace {
 // Copies the expert-sorted token rows of `hidden` into x_sorted, the FC1 A operand
 // (16-byte vectors; rows p < offsets[E]).
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
-                                   const int32_t* __restrict__ offsets, int E, int H16,
+                                   const int32_t* __restrict__ offsets, int E, int H16, int sh,
                                    uint4* __restrict__ xs) {
   pdl_wait();
   pdl_trigger();
   const int n = __ldg(offsets + E);
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < (long)n * H16;
        i += (long)gridDim.x * blockDim.x) {
-    const long p = i / H16;
+    const long p = div_idx(i, H16, sh);
     const int c = (int)(i - p * H16);
     xs[i] = __ldg(hidden + (long)__ldg(ids + p) * H16 + c);
   }
@@ -90,7 +90,7 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
     ProfScope ps("gather_rows", s);
     const cudaError_t e = launch_pdl(gather_rows_kernel, num_sms() * 4, 256, 0, s,
                                      static_cast<const uint4*>(a.hidden), a.sorted_ids, a.offsets, a.E,
-                                     a.H / 8, static_cast<uint4*>(a.xs));
+                                     a.H / 8, pow2_shift(a.H / 8), static_cast<uint4*>(a.xs));
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gather_rows: %s", cudaGetErrorString(e));
     if ((rc = check_launch("gather_rows"))) return rc;
   }

@@ -111,11 +111,11 @@ __device__ __forceinline__ void load_row(const int32_t* __restrict__ idx, const 
 template <int K>
 __global__ void __launch_bounds__(kBlock) indices_to_multihot_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ probs, int T, int k, int E,
-    uint8_t* __restrict__ mh, float* __restrict__ pm, int32_t* __restrict__ pos) {
+    uint8_t* __restrict__ mh, float* __restrict__ pm, int32_t* __restrict__ pos, int e4_shift) {
   const int E4 = (E + 3) >> 2;
   const long n = (long)T * E4;
   for (long tid = (long)blockIdx.x * blockDim.x + threadIdx.x; tid < n; tid += (long)gridDim.x * blockDim.x) {
-    const long t = tid / E4;
+    const long t = div_idx(tid, E4, e4_shift);
     const int e0 = (int)(tid - t * E4) * 4;
     unsigned m[4] = {0, 0, 0, 0};
     float p[4] = {0.f, 0.f, 0.f, 0.f};
@@ -260,7 +260,7 @@ int launch_i2m(const int32_t* idx, const float* probs, int T, int k, int E, uint
   long blocks = (n + kBlock - 1) / kBlock;
   const long cap = (long)num_sms() * 16;
   indices_to_multihot_kernel<K><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
-      idx, probs, T, k, E, mh, pm, pos);
+      idx, probs, T, k, E, mh, pm, pos, pow2_shift((E + 3) / 4));
   return check_launch("indices_to_multihot");
 }
 
