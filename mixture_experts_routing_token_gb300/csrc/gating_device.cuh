@@ -264,8 +264,19 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
 #pragma unroll
   for (int g = 1; g < G; ++g) m = fmaxf(m, gv[g]);
   float hi = 0.0f, lo = 0.0f;
-  if (!norm) {
-    for (int i = 0; i < E; ++i) two_sum_add(hi, lo, exp_diff(at(i), m));
+  if (!norm) {   // four independent compensated sums (a quarter of the dependent chain), then merged
+    float h[4] = {0.0f, 0.0f, 0.0f, 0.0f}, l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int i = 0;
+    for (; i + 4 <= E; i += 4) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a) two_sum_add(h[a], l[a], exp_diff(at(i + a), m));
+    }
+    for (; i < E; ++i) two_sum_add(h[0], l[0], exp_diff(at(i), m));
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      two_sum_add(hi, lo, h[a]);
+      lo += l[a];
+    }
   }
   for (int j = 0; j < k; ++j) {
     float bv = gv[0];
