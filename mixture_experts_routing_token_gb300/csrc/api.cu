@@ -410,7 +410,11 @@ MOE_API int moe_grouped_ffn_backward(const void* hidden, const void* w13, const 
   if (status && (rc = check_tensor(status, 1, "status"))) return rc;
   const size_t need = moe_grouped_ffn_backward_workspace_size(dtype, T, H, I, E, k);
   if ((rc = check_ws(ws, ws_bytes, need))) return rc;
-  if (T == 0) return MOE_OK;
+  if (T == 0) {   // no rows: the weight gradients are zero
+    cudaError_t e = cudaMemsetAsync(d_w13, 0, (size_t)E * 2 * I * H * 2, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_w2, 0, (size_t)E * H * I * 2, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : fail(MOE_ERR_CUDA, "zeroing weight gradients: %s", cudaGetErrorString(e));
+  }
   FfnBwdArgs a{};
   a.hidden = hidden;
   a.w13 = w13;

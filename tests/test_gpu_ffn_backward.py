@@ -60,6 +60,45 @@ def test_backward_shapes(T, H, I, E, k):
     _check(moe, d, al, k, seed=T * 3)
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (50, 64, 64, 1, 1),          # one expert, the smallest tensor-core shape
+    (33, 128, 128, 4, 4),        # k = E: every token on every expert
+    (70, 192, 320, 3, 1),        # odd expert count, I % 256 == 64
+])
+def test_backward_edge_shapes(T, H, I, E, k):
+    moe = need_gpu()
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, dtype="bf16", logits="distinct", seed=T + E)
+    w, idx = gating.softmax_topk(d["logits"], k, True)
+    _check(moe, d, align.align_by_expert(idx, w, E), k, seed=E)
+
+
+def test_backward_all_rows_on_one_expert():
+    moe = need_gpu()
+    T, H, I, E, k = 300, 128, 192, 8, 1
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, dtype="bf16", logits="distinct", seed=4)
+    idx = np.full((T, 1), 5, np.int32)
+    w = np.random.default_rng(1).uniform(0.1, 1.0, (T, 1)).astype(np.float32)
+    _, dw13, dw2, _ = _check(moe, d, align.align_by_expert(idx, w, E), k, seed=3)
+    assert not dw13[torch.arange(E, device=DEV) != 5].any() and not dw2[torch.arange(E, device=DEV) != 5].any()
+
+
+def test_backward_zero_tokens():
+    moe = need_gpu()
+    z = torch.zeros(0, dtype=torch.int32, device=DEV)
+    h = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    w13 = torch.zeros((2, 128, 64), dtype=torch.bfloat16, device=DEV)
+    w2 = torch.zeros((2, 64, 64), dtype=torch.bfloat16, device=DEV)
+    counts = torch.zeros(2, dtype=torch.int32, device=DEV)
+    offsets = torch.zeros(3, dtype=torch.int32, device=DEV)
+    dw13_out = torch.full_like(w13, 3.0)   # must be overwritten with zeros
+    dw2_out = torch.full_like(w2, 3.0)
+    dh, dw13, dw2, dwt = moe.moe_grouped_ffn_backward(h, w13, w2, 1, counts, offsets, z, z.float(), z, h,
+                                                     d_w13=dw13_out, d_w2=dw2_out)
+    torch.cuda.synchronize()
+    assert dh.shape == (0, 64) and dwt.shape == (0, 1)
+    assert not dw13.any() and not dw2.any()   # no rows: zero weight gradients
+
+
 def test_backward_dropped_slots_and_stale_workspace():
     """Dropped slots get d_weights 0 and contribute nothing, whatever the workspace held."""
     moe = need_gpu()
