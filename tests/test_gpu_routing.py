@@ -118,9 +118,9 @@ def test_multihot_page_examples(gold):
 
 def test_multihot_invalid_and_duplicate_indices():
     moe = need_gpu()
-    idx = np.array([[-1, 2], [5, -7], [1, 1], [3, 0]], np.int32)
-    pr = np.array([[0.5, 0.25], [0.1, 0.2], [0.3, 0.4], [0.6, 0.7]], np.float32)
-    for E in (4, 5):   # vector and scalar store paths
+    idx = np.array([[-1, 2], [5, -7], [1, 1], [3, 0], [9, 6]], np.int32)
+    pr = np.array([[0.5, 0.25], [0.1, 0.2], [0.3, 0.4], [0.6, 0.7], [0.8, 0.9]], np.float32)
+    for E in (4, 5, 8, 16):   # four-wide vector, scalar and eight-wide store paths
         ref = multihot.indices_to_multihot(idx, pr, E)
         got = moe.moe_indices_to_multihot(torch.from_numpy(idx).to(DEV), torch.from_numpy(pr).to(DEV), E)
         for r, g_ in zip(ref, got):
@@ -129,6 +129,27 @@ def test_multihot_invalid_and_duplicate_indices():
         gp, gi = moe.moe_multihot_to_indices(got[1], got[2], 2)
         np.testing.assert_array_equal(gp.cpu().numpy(), rp)
         np.testing.assert_array_equal(gi.cpu().numpy(), ri)
+
+
+@pytest.mark.parametrize("E,k", [(64, 8), (320, 6)])
+def test_multihot_outputs_16_byte_aligned_only(E, k):
+    """Outputs on a 16- but not 32-byte boundary take the 128-bit store form."""
+    moe = need_gpu()
+    T = 777
+    x = gen_logits(np.random.SeedSequence(E), T, E, "distinct")
+    w_ref, i_ref = gating.softmax_topk(x, k, True)
+    ref = multihot.indices_to_multihot(i_ref, w_ref, E)
+    bufs = [torch.full((T * E + 16,), 7, dtype=dt, device=DEV) for dt in (torch.uint8, torch.float32, torch.int32)]
+    n = T * E
+    mh, pm, pos = (bufs[0][16:16 + n].view(T, E), bufs[1][4:4 + n].view(T, E), bufs[2][4:4 + n].view(T, E))
+    assert pm.data_ptr() % 32 == 16 and pos.data_ptr() % 32 == 16
+    moe.moe_indices_to_multihot(torch.from_numpy(i_ref).to(DEV), torch.from_numpy(w_ref).to(DEV), E,
+                                multihot=mh, probs_in_multihot=pm, position_map=pos)
+    torch.cuda.synchronize()
+    for r, g_ in zip(ref, (mh, pm, pos)):
+        np.testing.assert_array_equal(g_.cpu().numpy(), r)
+    for b, lo in zip(bufs, (16, 4, 4)):   # nothing written outside the views
+        assert (b[:lo] == 7).all() and (b[lo + n:] == 7).all()
 
 
 def _align_case(moe, i_np, w_np, E):
