@@ -139,6 +139,38 @@ def test_grouped_ffn_every_last_tile_kind(H, I):
     assert_close_rel_max(to_np64(out), ref, 2e-2, "grouped ffn, every last-tile kind")
 
 
+# Remainders of every size (1, 31..33, 63..65, 129) after one to three full 256-row tiles,
+# with enough tiles that each SM pair runs several in a row, so the two accumulator
+# buffers alternate between full, swapped and ragged tiles.
+@pytest.mark.parametrize("H,I", [(1024, 1024), (1216, 320)])
+def test_grouped_ffn_remainders_after_full_tiles(H, I):
+    moe = need_gpu()
+    counts = [769, 800, 801, 832, 833, 768, 785, 816, 261, 316, 287, 385, 552, 0, 63, 256, 513, 577]
+    E, k = len(counts), 1
+    T = sum(counts)
+    rng = np.random.default_rng(H - I)
+    idx = rng.permutation(np.repeat(np.arange(E), counts)).astype(np.int32).reshape(T, 1)
+    w = rng.uniform(0.05, 1.0, size=(T, k)).astype(np.float32)
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, dtype="bf16", logits="distinct", seed=H + I)
+    al = align.align_by_expert(idx, w, E)
+    assert al["counts"].tolist() == counts
+    t = {k_: torch.from_numpy(np.ascontiguousarray(al[k_])).to(DEV)
+         for k_ in ("counts", "offsets", "sorted_token_ids", "sorted_weights", "reverse_indices")}
+    out = moe.moe_grouped_ffn(to_dev(d["hidden"], "bf16"), to_dev(d["w13"], "bf16"), to_dev(d["w2"], "bf16"),
+                              k, t["counts"], t["offsets"], t["sorted_token_ids"], t["sorted_weights"],
+                              t["reverse_indices"])
+    torch.cuda.synchronize()
+    ref = ffn.grouped_ffn(d["hidden"], d["w13"], d["w2"], "bf16", k, al["counts"], al["offsets"],
+                          al["sorted_token_ids"], al["sorted_weights"], al["reverse_indices"])
+    got = to_np64(out)
+    assert_close_rel_max(got, ref, 2e-2, "grouped ffn, remainders after full tiles")
+    # rows of the remainders alone, so a wrong remainder cannot hide under the global maximum
+    off = al["offsets"]
+    rem = np.concatenate([al["sorted_token_ids"][off[e] + (c // 256) * 256: off[e] + c]
+                          for e, c in enumerate(counts) if c >= 256 and 0 < c % 256 <= 64])
+    assert_close_rel_max(got[rem], ref[rem], 2e-2, "remainder rows")
+
+
 @pytest.mark.parametrize("T,H,I,E,k", [(300, 256, 256, 8, 2), (40, 128, 128, 16, 4), (90, 40, 24, 5, 2)])
 def test_grouped_ffn_dropped_slots_contribute_nothing(T, H, I, E, k):
     """Slots whose expert index is outside [0, E) are dropped by the align step; the FFN must
