@@ -13,6 +13,7 @@ namespace moe {
 namespace gate {
 
 constexpr int kNone = 0x7fffffff;   // "no candidate" index
+constexpr int kRegSel = 8;          // up to this k, one thread per token keeps the selected logits in registers
 
 // Logits are float32 or bf16; bf16 values are widened to float32 exactly, so
 // everything after the load is the float32 computation on the widened row.
@@ -143,9 +144,10 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
     if (base + i >= E) taken |= 1ull << i;
 
   float m = 0.0f, hi = 0.0f, lo = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = kNone;
+  // one round: the best remaining (value, expert) over the group's lanes
+  auto take = [&](float& bv, int& bi) {
+    bv = 0.0f;
+    bi = kNone;
 #pragma unroll
     for (int i = 0; i < V; ++i)
       if (!((taken >> i) & 1ull) && (bi == kNone || v[i] > bv)) { bv = v[i]; bi = base + i; }
@@ -156,6 +158,34 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
       if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
     if (bi / V == g) taken |= 1ull << (bi - base);
+  };
+  if (L == 1 && k <= kRegSel) {   // one thread per token: the selected logits stay in registers
+    float sel[kRegSel];
+#pragma unroll
+    for (int j = 0; j < kRegSel; ++j) {
+      if (j < k) {
+        int bi;
+        take(sel[j], bi);
+        if (j == 0) m = sel[0];
+        if (norm) two_sum_add(hi, lo, exp_diff(sel[j], m));
+        idx_out[t * k + j] = bi;
+      }
+    }
+    if (!norm) {
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (base + i < E) two_sum_add(hi, lo, exp_diff(v[i], m));
+    }
+    const float denom = hi + lo;
+#pragma unroll
+    for (int j = 0; j < kRegSel; ++j)
+      if (j < k) w_out[t * k + j] = __fdiv_rn(exp_diff(sel[j], m), denom);
+    return;
+  }
+  for (int j = 0; j < k; ++j) {
+    float bv;
+    int bi;
+    take(bv, bi);
     if (j == 0) m = bv;
     if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
     if ((j & (L - 1)) == g) {
@@ -196,20 +226,38 @@ constexpr int kStageLd = kStageRows + 1;
 
 // Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into col[EP][kStageLd],
 // experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows); the
-// caller synchronises before reading.
+// caller synchronises before reading. Each thread issues kStageBatch vector
+// loads before it stores any of them, so a block has that many loads per
+// thread in flight instead of one.
+constexpr int kStageBatch = 8;
+
 template <int EP, typename In = float>
 __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t0, int nt, int E,
                                            float* col, int tid, int nthr) {
   const In* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
+  constexpr int U = kStageBatch;
   if constexpr (!std::is_same<In, float>::value) {
     if ((E & 7) == 0) {
       const int n8 = nt * E / 8;
-      for (int f = tid; f < n8; f += nthr) {
-        float x[8];
-        load8_bf16(blk + 8 * f, x);
-        const int tl = (8 * f) / E, e0 = 8 * f - tl * E;
+      const uint4* src = reinterpret_cast<const uint4*>(blk);
+      for (int f0 = tid; f0 < n8; f0 += U * nthr) {
+        uint4 q[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) col[(e0 + i) * kStageLd + tl] = x[i];
+        for (int u = 0; u < U; ++u)
+          if (f0 + u * nthr < n8) q[u] = __ldg(src + f0 + u * nthr);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int f = f0 + u * nthr;
+          if (f < n8) {
+            const int tl = (int)((uint32_t)(8 * f) / (uint32_t)E), e0 = 8 * f - tl * E;
+            const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              col[(e0 + 2 * i) * kStageLd + tl] = lo_bf16(w[i]);
+              col[(e0 + 2 * i + 1) * kStageLd + tl] = hi_bf16(w[i]);
+            }
+          }
+        }
       }
     } else {
       for (int f = tid; f < nt * E; f += nthr) {
@@ -219,13 +267,23 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
     }
   } else if ((E & 3) == 0) {
     const int n4 = nt * E / 4;
-    for (int f = tid; f < n4; f += nthr) {
-      const float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);
-      const int tl = (4 * f) / E, e0 = 4 * f - tl * E;
-      col[e0 * kStageLd + tl] = q.x;
-      col[(e0 + 1) * kStageLd + tl] = q.y;
-      col[(e0 + 2) * kStageLd + tl] = q.z;
-      col[(e0 + 3) * kStageLd + tl] = q.w;
+    const float4* src = reinterpret_cast<const float4*>(blk);
+    for (int f0 = tid; f0 < n4; f0 += U * nthr) {
+      float4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (f0 + u * nthr < n4) q[u] = __ldg(src + f0 + u * nthr);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int f = f0 + u * nthr;
+        if (f < n4) {
+          const int tl = (int)((uint32_t)(4 * f) / (uint32_t)E), e0 = 4 * f - tl * E;
+          col[e0 * kStageLd + tl] = q[u].x;
+          col[(e0 + 1) * kStageLd + tl] = q[u].y;
+          col[(e0 + 2) * kStageLd + tl] = q[u].z;
+          col[(e0 + 3) * kStageLd + tl] = q[u].w;
+        }
+      }
     }
   } else {
     for (int f = tid; f < nt * E; f += nthr) {
@@ -278,9 +336,11 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
       lo += l[a];
     }
   }
-  for (int j = 0; j < k; ++j) {
-    float bv = gv[0];
-    int bi = gi[0], bg = 0;
+  // one round: the best remaining (value, expert); its group is rescanned
+  auto take = [&](float& bv, int& bi) {
+    bv = gv[0];
+    bi = gi[0];
+    int bg = 0;
 #pragma unroll
     for (int g = 1; g < G; ++g)
       if (gv[g] > bv) { bv = gv[g]; bi = gi[g]; bg = g; }
@@ -295,6 +355,28 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
 #pragma unroll
     for (int g = 0; g < G; ++g)
       if (g == bg) { gv[g] = nv; gi[g] = ni; }
+  };
+  if (!s_w && k <= kRegSel) {   // the selected logits stay in registers until the weights are formed
+    float sel[kRegSel];
+#pragma unroll
+    for (int j = 0; j < kRegSel; ++j) {
+      if (j < k) {
+        int bi;
+        take(sel[j], bi);
+        if (norm) two_sum_add(hi, lo, exp_diff(sel[j], m));
+        idx_out[t * k + j] = bi;
+      }
+    }
+    const float denom = hi + lo;
+#pragma unroll
+    for (int j = 0; j < kRegSel; ++j)
+      if (j < k) w_out[t * k + j] = __fdiv_rn(exp_diff(sel[j], m), denom);
+    return;
+  }
+  for (int j = 0; j < k; ++j) {
+    float bv;
+    int bi;
+    take(bv, bi);
     if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
     idx_out[t * k + j] = bi;
     if (s_w) {

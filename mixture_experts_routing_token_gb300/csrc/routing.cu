@@ -526,19 +526,30 @@ __global__ void __launch_bounds__(kSmemGroupThreads) group_topk_smem_kernel(
   const long t0 = (long)blockIdx.x * kSmemGroupThreads;
   const int nt = (int)min((long)kSmemGroupThreads, (long)T - t0);
   const float* blk = scores + t0 * (long)E;
-  if ((E & 3) == 0) {
+  if ((E & 3) == 0) {   // kStageBatch loads in flight per thread, then their stores
+    constexpr int U = gate::kStageBatch;
     const int n4 = nt * E / 4;
-    for (int f = tid; f < n4; f += kSmemGroupThreads) {
-      float4 q = __ldg(reinterpret_cast<const float4*>(blk) + f);
-      const int tl = (4 * f) / E, e0 = 4 * f - tl * E;
-      if (noaux) {
-        const float4 b = __ldg(reinterpret_cast<const float4*>(bias + e0));
-        q.x += b.x; q.y += b.y; q.z += b.z; q.w += b.w;
+    const float4* src = reinterpret_cast<const float4*>(blk);
+    for (int f0 = tid; f0 < n4; f0 += U * kSmemGroupThreads) {
+      float4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (f0 + u * kSmemGroupThreads < n4) q[u] = __ldg(src + f0 + u * kSmemGroupThreads);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int f = f0 + u * kSmemGroupThreads;
+        if (f < n4) {
+          const int tl = (int)((uint32_t)(4 * f) / (uint32_t)E), e0 = 4 * f - tl * E;
+          if (noaux) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(bias + e0));
+            q[u].x += b.x; q[u].y += b.y; q[u].z += b.z; q[u].w += b.w;
+          }
+          sm[e0 * LD + tl] = q[u].x;
+          sm[(e0 + 1) * LD + tl] = q[u].y;
+          sm[(e0 + 2) * LD + tl] = q[u].z;
+          sm[(e0 + 3) * LD + tl] = q[u].w;
+        }
       }
-      sm[e0 * LD + tl] = q.x;
-      sm[(e0 + 1) * LD + tl] = q.y;
-      sm[(e0 + 2) * LD + tl] = q.z;
-      sm[(e0 + 3) * LD + tl] = q.w;
     }
   } else {
     for (int f = tid; f < nt * E; f += kSmemGroupThreads) {
