@@ -17,9 +17,12 @@
 //      chunk_hist into an inclusive prefix over chunks, in place;
 //   3. align_scatter: each CTA derives offsets and its chunk's per-expert base
 //      from chunk_hist (summing the few chunks before it, or reading the
-//      prefix), then ranks its slots in order, 512 at a time: within a warp by
-//      __match_any_sync + popc of lower lanes, across warps by a per-expert
-//      prefix over the warps' counts.
+//      prefix), then ranks its slots in one round: warp w takes 256
+//      consecutive slots in 8 sub-rounds of 32 (__match_any_sync + popc of
+//      lower lanes on top of the warp's running per-expert count), a
+//      per-expert prefix over the warps' counts places the warps, the slots go
+//      to an expert-sorted copy of the chunk in shared memory, and each
+//      expert's run is copied out with consecutive threads (coalesced stores).
 // A single-chunk problem runs as one launch (the CTA makes its own histogram).
 #include <mutex>
 
@@ -31,15 +34,15 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSpt = 4;        // slots per thread per ranking round
-constexpr int kChunk = 4096;   // slots per CTA (a multiple of kThreads * kSpt)
+constexpr int kChunk = 4096;   // slots per CTA
+constexpr int kSub = kChunk / kThreads;   // sub-rounds of 32 slots per warp (its kChunk / kWarps slots)
 constexpr int kScanAbove = 16; // chunks above which the per-expert prefix gets its own launch
 
 __device__ __forceinline__ int valid_expert(int e, int E) { return (e >= 0 && e < E) ? e : -1; }
 
 // Dynamic shared memory of align_chunk for E experts.
 __host__ __device__ inline size_t align_smem_bytes(int E) {
-  return (size_t)(4 * E + 2 + kWarps * E + 3 * kChunk) * sizeof(int);
+  return (size_t)(3 * E + 2 + kWarps * E + 3 * kChunk) * sizeof(int);
 }
 
 __global__ void __launch_bounds__(kThreads) align_hist_kernel(const int32_t* __restrict__ idx,
@@ -133,21 +136,20 @@ __device__ __forceinline__ int warp0_exclusive_scan(int* v, int n) {
 }
 
 // Align chunk c of the slots (all kThreads threads of the CTA take part).
-// Shared layout (ints): base[E] | off[E+1] | cb[E] | cpre[E+1] | wcnt[kWarps][E]
+// Shared layout (ints): off[E+1] | cb[E] | cpre[E+1] | wcnt[kWarps][E]
 //                       | staged token ids, slots, weights [kChunk] each.
-// base[e] runs over the chunk's slots of expert e (global rank among all slots
-// of e), cb[e] is its value at the chunk start, cpre[e] the chunk-local start of
-// e's slots. Slots are ranked into the staging arrays in expert-sorted order,
-// then each expert's run is copied to its global positions by consecutive
-// threads (coalesced stores).
+// cb[e] is the number of expert e's slots in earlier chunks, cpre[e] the
+// chunk-local start of e's slots, wcnt[w][e] warp w's count of e, then the
+// number of e's slots in the chunk's warps before w. Slots are ranked into the
+// staging arrays in expert-sorted order, then each expert's run is copied to
+// its global positions by consecutive threads (coalesced stores).
 template <int SRC>
 __device__ __forceinline__ void align_chunk(
     int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
     const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ sorted_ids, float* __restrict__ sorted_w, int32_t* __restrict__ reverse,
     int32_t* status, int* sm) {
-  int* base = sm;
-  int* off = base + E;
+  int* off = sm;
   int* cb = off + E + 1;
   int* cpre = cb + E;
   int* wcnt = cpre + E + 1;
@@ -158,11 +160,24 @@ __device__ __forceinline__ void align_chunk(
   const long hi = min(S, lo + kChunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // 1. per-expert totals (off[]), base of this chunk (base[], cb[]) and this chunk's counts (cpre[])
+  // 0. this warp's slots (step 3), loaded first so that their latency overlaps steps 1-2;
+  //    the barriers of steps 1-2 also order the zeroing of wcnt before step 3
+  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+  const long wbase = lo + (long)warp * 32 * kSub;
+  int eu[kSub], ru[kSub];
+  float wu[kSub];
+#pragma unroll
+  for (int u = 0; u < kSub; ++u) {
+    const long s = wbase + u * 32 + lane;
+    eu[u] = s < hi ? load_i<SRC>(idx + s) : -1;
+    wu[u] = s < hi ? load_f<SRC>(wts + s) : 0.0f;
+  }
+
+  // 1. per-expert totals (off[]), slots of earlier chunks (cb[]) and this chunk's counts (cpre[])
   if (chunk_hist && hist_is_prefix) {
     for (int e = tid; e < E; e += kThreads) {
       const int before = c > 0 ? __ldg(chunk_hist + (long)(c - 1) * E + e) : 0;
-      base[e] = cb[e] = before;
+      cb[e] = before;
       cpre[e] = __ldg(chunk_hist + (long)c * E + e) - before;
       off[e] = __ldg(chunk_hist + (long)(nchunks - 1) * E + e);
     }
@@ -175,13 +190,13 @@ __device__ __forceinline__ void align_chunk(
         before += cc < c ? h : 0;
         total += h;
       }
-      base[e] = cb[e] = before;
+      cb[e] = before;
       cpre[e] = __ldg(chunk_hist + (long)c * E + e);
       off[e] = total;
     }
     __syncthreads();
   } else {   // single chunk: histogram here
-    for (int e = tid; e < E; e += kThreads) { base[e] = 0; cb[e] = 0; off[e] = 0; }
+    for (int e = tid; e < E; e += kThreads) { cb[e] = 0; off[e] = 0; }
     __syncthreads();
     bool bad = false;
     for (long s = lo + tid; s < hi; s += kThreads) {
@@ -197,7 +212,6 @@ __device__ __forceinline__ void align_chunk(
 
   // 2. exclusive scans over experts: totals -> offsets (warp 0), chunk counts -> cpre (warp 1)
   if (warp == 0) {
-    int cnt0 = 0;
     if (c == 0) {
       for (int e = lane; e < E; e += 32) counts[e] = off[e];
     }
@@ -207,7 +221,6 @@ __device__ __forceinline__ void align_chunk(
       off[E] = total;
       if (c == 0) offsets[E] = total;
     }
-    (void)cnt0;
   } else if (warp == 1) {
     const int total = warp0_exclusive_scan(cpre, E);
     if (lane == 31) cpre[E] = total;
@@ -216,59 +229,44 @@ __device__ __forceinline__ void align_chunk(
   if (c == 0)
     for (int e = tid; e < E; e += kThreads) offsets[e] = off[e];
 
-  // 3. ordered ranking into the staging arrays, kThreads * kSpt slots per round: warp w
-  //    takes the round's slots [w * 32 * kSpt, (w + 1) * 32 * kSpt) as kSpt consecutive
-  //    sub-rounds of 32, ranking each by __match_any_sync on top of the warp's running
-  //    per-expert count; a per-expert prefix over warps then places them.
-  for (long r0 = lo; r0 < hi; r0 += (long)kThreads * kSpt) {
-    for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
-    __syncthreads();
-    int eu[kSpt], ru[kSpt];
-    float wu[kSpt];
-    // issue all of this thread's loads for the round before ranking
+  // 3. ranking, one round: warp w takes the chunk's slots [w * 32 * kSub, (w + 1) * 32 * kSub)
+  //    as kSub sub-rounds of 32, ranking each by __match_any_sync on top of the warp's
+  //    running per-expert count; a per-expert prefix over the warps then places them.
 #pragma unroll
-    for (int u = 0; u < kSpt; ++u) {
-      const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
-      eu[u] = s < hi ? load_i<SRC>(idx + s) : -1;
-      wu[u] = s < hi ? load_f<SRC>(wts + s) : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < kSpt; ++u) {
-      const int e = valid_expert(eu[u], E);
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int below = __popc(peers & ((1u << lane) - 1u));
-      const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
-      __syncwarp();
-      if (e >= 0 && below == 0) wcnt[warp * E + e] = prior + __popc(peers);
-      __syncwarp();
-      eu[u] = e;
-      ru[u] = prior + below;
-    }
-    __syncthreads();
-    for (int x = tid; x < E; x += kThreads) {
-      int run = base[x];
-#pragma unroll 4
-      for (int w = 0; w < kWarps; ++w) {
-        const int cnt = wcnt[w * E + x];
-        wcnt[w * E + x] = run;
-        run += cnt;
-      }
-      base[x] = run;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kSpt; ++u) {
-      const int e = eu[u];
-      if (e >= 0) {
-        const long s = r0 + (long)warp * 32 * kSpt + u * 32 + lane;
-        const int q = cpre[e] + wcnt[warp * E + e] + ru[u] - cb[e];   // chunk-local, expert-sorted
-        s_tok[q] = s <= 0x7fffffffL ? (int)((uint32_t)s / (uint32_t)k) : (int)(s / k);
-        s_rev[q] = (int)s;
-        s_w[q] = wu[u];
-      }
-    }
-    __syncthreads();
+  for (int u = 0; u < kSub; ++u) {
+    const int e = valid_expert(eu[u], E);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int below = __popc(peers & ((1u << lane) - 1u));
+    const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
+    __syncwarp();
+    if (e >= 0 && below == 0) wcnt[warp * E + e] = prior + __popc(peers);
+    __syncwarp();
+    eu[u] = e;
+    ru[u] = prior + below;
   }
+  __syncthreads();
+  for (int x = tid; x < E; x += kThreads) {
+    int run = 0;
+#pragma unroll 4
+    for (int w = 0; w < kWarps; ++w) {
+      const int cnt = wcnt[w * E + x];
+      wcnt[w * E + x] = run;
+      run += cnt;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kSub; ++u) {
+    const int e = eu[u];
+    if (e >= 0) {
+      const long s = wbase + u * 32 + lane;
+      const int q = cpre[e] + wcnt[warp * E + e] + ru[u];   // chunk-local, expert-sorted
+      s_tok[q] = s <= 0x7fffffffL ? (int)((uint32_t)s / (uint32_t)k) : (int)(s / k);
+      s_rev[q] = (int)s;
+      s_w[q] = wu[u];
+    }
+  }
+  __syncthreads();
 
   // 4. copy each expert's run of the chunk to its global positions (coalesced)
   const int n = cpre[E];
