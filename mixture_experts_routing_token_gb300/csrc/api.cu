@@ -170,9 +170,9 @@ int check_ws(void* ws, size_t have, size_t need) {
 int run_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int T, int H, int I,
             int E, int k, const int32_t* counts, const int32_t* offsets, const int32_t* ids,
             const float* sw, const int32_t* rev, void* out, const FfnWs& w, int32_t* status,
-            cudaStream_t s, bool may_drop = true) {
+            cudaStream_t s, bool may_drop = true, const float* logits = nullptr, int norm = 0) {
   FfnArgs a{hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, ids, sw, rev,
-            out, w.act, w.staging, w.xs, status};
+            out, w.act, w.staging, w.xs, status, logits, norm};
   if (may_drop) {   // caller routing may hold indices outside [0, E)
     const int rc = launch_zero_dropped(offsets, E, (long)T * k, H, w.staging, s);
     if (rc) return rc;
@@ -492,9 +492,11 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
                            al.reverse, al.scratch, status, s)))
       return rc;
   }
-  // the layer's own gating only produces indices in [0, E): no slot is dropped
+  // the layer's own gating only produces indices in [0, E): no slot is dropped. The
+  // logits let the decode kernels start on the experts' weights before routing ends.
   return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, al.counts, al.offsets, al.sorted_ids,
-                 al.sorted_w, al.reverse, out, fw, status, s, /*may_drop=*/false);
+                 al.sorted_w, al.reverse, out, fw, status, s, /*may_drop=*/false, router_logits,
+                 norm_topk_prob != 0);
 }
 
 MOE_API int moe_profiler_enable(int on) {

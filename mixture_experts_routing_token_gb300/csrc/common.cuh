@@ -98,6 +98,11 @@ struct FfnArgs {
   float* staging;   // [S, H] float32
   void* xs;         // [S, H] dtype: expert-sorted copy of hidden (only without the TMA gather)
   int32_t* status;
+  // Router logits [T, E] (or null): with them the decode FC1 kernel derives the
+  // routing of its tokens itself (the same top-k and expert order as the routing
+  // kernel, whose outputs it then waits for only before FC2 may start).
+  const float* logits;
+  int norm;
 };
 
 // bf16 matrix [rows, cols] row-major as a TMA tensor map: box = box_rows x 64

@@ -23,7 +23,17 @@
 //   warps 2..5  epilogue: FC1 act = silu(g) * u -> bf16 act row of each token;
 //               FC2 y * routing weight -> float32 staging row of the slot.
 // All waits are bounded as in the prefill kernel.
+//
+// Inside the layer call (router logits given, E <= 64, T*k <= kLocalSlots) the
+// FC1 kernel does not wait for the routing kernel before it streams weights:
+// every CTA repeats the top-k selection of the batch's tokens (the same
+// comparisons, ties toward the lower expert, so the same experts) and the
+// stable expert order of the align step in shared memory, and takes its tiles,
+// token ids and activation rows from that. Its epilogue warps wait for the
+// routing kernel (griddepcontrol.wait) before they release FC2, which reads
+// the routing kernel's outputs, so FC1 also ends after it.
 #include "common.cuh"
+#include "gating_device.cuh"
 #include "sm100_ptx.cuh"
 
 namespace moe {
@@ -34,6 +44,8 @@ constexpr int DK = 64;           // K per stage (one 128-byte swizzle row)
 constexpr int DSTAGES_MAX = 12;
 constexpr int DTHREADS = 192;
 constexpr uint64_t DWAIT_NS = 2000000000ull;
+constexpr int kLocalExperts = 64;   // local routing: a warp per token, two experts per lane (E <= 64)
+constexpr int kLocalSlots = 512;    // and at most this many routed slots
 
 enum { DEC_FC1 = 0, DEC_FC2 = 1 };
 
@@ -50,6 +62,8 @@ struct DecParams {
   int w_rows;     // rows of one expert's weight matrix: 2I or H
   void* out;      // FC1: act bf16 [S, I]; FC2: staging f32 [S, H]
   int32_t* status;
+  const float* logits;   // FC1 only, or null: route the tokens locally (see above)
+  int norm, T, k;
 };
 
 template <int MODE, int NTOK>
@@ -97,9 +111,20 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ int tile_start[MOE_MAX_EXPERTS + 1];
+  // local routing (FC1 with logits): selected experts, counts, offsets and the
+  // expert-sorted token ids
+  __shared__ int32_t l_idx[MODE == DEC_FC1 ? kLocalSlots : 1];
+  __shared__ int32_t l_ids[MODE == DEC_FC1 ? kLocalSlots : 1];
+  __shared__ int32_t l_cnt[MODE == DEC_FC1 ? kLocalExperts : 1], l_off[MODE == DEC_FC1 ? kLocalExperts + 1 : 1];
+  __shared__ int32_t l_run[MODE == DEC_FC1 ? kLocalExperts : 1];
   extern __shared__ uint8_t dsmem_raw[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool local = MODE == DEC_FC1 && P.logits != nullptr;
+  const int32_t* counts = local ? l_cnt : P.counts;
+  const int32_t* offsets = local ? l_off : P.offsets;
+  const int32_t* sorted_ids = local ? l_ids : P.sorted_ids;
+  auto rd = [&](const int32_t* q) -> int { return local ? *q : __ldg(q); };   // shared or global
   const uint32_t dsmem = (ptx::smem_u32(dsmem_raw) + 1023u) & ~1023u;
   auto sA = [&](int s) { return dsmem + (uint32_t)(s * C::STAGE); };
   auto sB = [&](int s) { return dsmem + (uint32_t)(s * C::STAGE + C::A_BYTES); };
@@ -127,13 +152,66 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   // and ids it reads from here on. FC2 follows FC1 and reads only its activations
   // (after pdl_wait in the producer); the routing outputs it reads earlier come
   // from two launches back and are complete once FC1 has triggered.
-  if (MODE == DEC_FC1) pdl_wait();
-  pdl_trigger();
+  if (MODE == DEC_FC1 && !local) pdl_wait();
+  if (!local) pdl_trigger();
+  if (MODE == DEC_FC1 && local) {
+    // the routing of the batch, as the routing kernel computes it: top-k experts of
+    // each token, then each slot's rank among the earlier slots of its expert
+    const int S = P.T * P.k;
+    for (int t = warp; t < P.T; t += DTHREADS / 32) {   // a warp per token: lane l holds experts l, l + 32
+      const float* row = P.logits + (long)t * P.E;
+      unsigned key[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) key[i] = lane + 32 * i < P.E ? gate::okey(__ldg(row + lane + 32 * i)) : 0u;
+      unsigned taken = 0;
+      for (int j = 0; j < P.k; ++j) {   // largest value, then the lower expert among equal values
+        unsigned kv;
+        const int e = gate::warp_argmax_round<2>(key, taken, lane, &kv);
+        if ((e & 31) == lane) taken |= 1u << (e >> 5);
+        if (lane == 0) l_idx[t * P.k + j] = e;
+      }
+    }
+    for (int e = tid; e < P.E; e += DTHREADS) l_cnt[e] = 0;
+    __syncthreads();
+    for (int q = tid; q < S; q += DTHREADS) atomicAdd(&l_cnt[l_idx[q]], 1);
+    __syncthreads();
+    if (warp == 0) {   // exclusive offsets, two experts per lane (E <= 64)
+      const int a = 2 * lane < P.E ? l_cnt[2 * lane] : 0, b = 2 * lane + 1 < P.E ? l_cnt[2 * lane + 1] : 0;
+      int incl = a + b;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      if (2 * lane < P.E) l_off[2 * lane] = incl - a - b;
+      if (2 * lane + 1 < P.E) l_off[2 * lane + 1] = incl - b;
+      if (lane == 31) l_off[P.E] = incl;
+    }
+    __syncthreads();
+    if (warp == 0) {   // stable expert order: rounds of 32 slots, ranked by __match_any_sync
+      for (int e = lane; e < P.E; e += 32) l_run[e] = 0;
+      __syncwarp();
+      for (int q0 = 0; q0 < S; q0 += 32) {
+        const int q = q0 + lane;
+        const int e = q < S ? l_idx[q] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int below = __popc(peers & ((1u << lane) - 1u));
+        const int prior = e >= 0 ? l_run[e] : 0;
+        __syncwarp();
+        if (e >= 0) {
+          l_ids[l_off[e] + prior + below] = q / P.k;
+          if (below == 0) l_run[e] = prior + __popc(peers);
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 2) {   // tile_start[e] = sum over e' < e of ceil(count / NTOK) * NTW
     const int per = (P.E + 31) / 32;
     const int e0 = min(P.E, lane * per), e1 = min(P.E, e0 + per);
     int run = 0;
-    for (int e = e0; e < e1; ++e) run += (__ldg(P.counts + e) + NTOK - 1) / NTOK * P.NTW;
+    for (int e = e0; e < e1; ++e) run += (rd(counts + e) + NTOK - 1) / NTOK * P.NTW;
     int incl = run;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -143,7 +221,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     int acc = incl - run;
     for (int e = e0; e < e1; ++e) {
       tile_start[e] = acc;
-      acc += (__ldg(P.counts + e) + NTOK - 1) / NTOK * P.NTW;
+      acc += (rd(counts + e) + NTOK - 1) / NTOK * P.NTW;
     }
     if (lane == 31) tile_start[P.E] = incl;
   }
@@ -180,18 +258,18 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const DecTile d = dec_tile(t, tile_start, P.E, P.NTW);
-      const int cnt = __ldg(P.counts + d.e);
-      const int p0 = __ldg(P.offsets + d.e) + d.chunk * NTOK;
+      const int cnt = rd(counts + d.e);
+      const int p0 = rd(offsets + d.e) + d.chunk * NTOK;
       const int w0 = d.e * P.w_rows + d.wt * DM;           // FC1: gate rows; FC2: w2 rows
       const int w1 = w0 + P.N_out;                          // FC1: matching up rows (I further)
       int rid[4] = {0, 0, 0, 0};
       if (MODE == DEC_FC1 && lane < NTOK / 4) {
         const int valid = min(NTOK, cnt - d.chunk * NTOK);
-        const int first = __ldg(P.sorted_ids + p0);
+        const int first = rd(sorted_ids + p0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = lane * 4 + i;
-          rid[i] = r < valid ? __ldg(P.sorted_ids + p0 + r) : first;
+          rid[i] = r < valid ? rd(sorted_ids + p0 + r) : first;
         }
       }
       for (int kb = 0; kb < KB; ++kb) {
@@ -269,13 +347,17 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     const int row = q * 32 + lane;     // weight row within the tile = output column offset
     int acc = 0;
     uint32_t aph = 0;
+    if (local) {   // FC2 reads the routing kernel's outputs: release it only once they exist
+      pdl_wait();
+      pdl_trigger();
+    }
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const DecTile d = dec_tile(t, tile_start, P.E, P.NTW);
       if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, DWAIT_NS)) break;
       ptx::tc_fence_after();
-      const int cnt = __ldg(P.counts + d.e);
+      const int cnt = rd(counts + d.e);
       const int valid = min(NTOK, cnt - d.chunk * NTOK);
-      const long p0 = (long)__ldg(P.offsets + d.e) + d.chunk * NTOK;
+      const long p0 = (long)rd(offsets + d.e) + d.chunk * NTOK;
       const int col = d.wt * DM + row;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::ACC_COLS);
 #pragma unroll
@@ -347,11 +429,12 @@ int run_decode(const FfnArgs& a, cudaStream_t s) {
   if ((rc = make_tmap(&x1, a.hidden, (uint64_t)a.T, (uint64_t)a.H, 1))) return rc;
   if ((rc = make_tmap(&w2, a.w2, (uint64_t)a.E * a.H, (uint64_t)a.I, DM))) return rc;
   if ((rc = make_tmap(&x2, a.act, (uint64_t)S, (uint64_t)a.I, NTOK))) return rc;
+  const bool local = a.logits && a.E <= kLocalExperts && S <= kLocalSlots;
   DecParams p1{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.H, a.I,
-               (a.I + DM - 1) / DM, 2 * a.I, a.act, a.status};
+               (a.I + DM - 1) / DM, 2 * a.I, a.act, a.status, local ? a.logits : nullptr, a.norm, a.T, a.k};
   if ((rc = launch_dec<DEC_FC1, NTOK>(w1, x1, p1, S, s, "ffn_fc1_decode"))) return rc;
   DecParams p2{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H,
-               (a.H + DM - 1) / DM, a.H, a.staging, a.status};
+               (a.H + DM - 1) / DM, a.H, a.staging, a.status, nullptr, 0, a.T, a.k};
   if ((rc = launch_dec<DEC_FC2, NTOK>(w2, x2, p2, S, s, "ffn_fc2_decode"))) return rc;
   return launch_combine(a.staging, a.T, a.k, a.H, a.dtype, a.out, s);
 }
