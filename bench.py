@@ -579,8 +579,21 @@ def main():
     S = T * k
     launches = sum(v["launches"] for v in kern.values()) / args.steps
     fc1 = kern.get("ffn_fc1_tc") or kern.get("ffn_fc1_simt")
+    dec = kern.get("ffn_fc1_decode")
     roofline = None
-    if fc1 and fc1["launches"]:
+    if dec and dec["launches"]:
+        # decode: FC1 streams the weight rows of the experts the batch routes to (HBM-bound);
+        # algorithmic bytes = those rows + the token rows + the activations written
+        _, ti = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
+        active = int(torch.unique(ti).numel())
+        nbytes = float(active * 2 * I * H * 2 + T * H * 2 + S * I * 2)
+        dec_ms = dec["total_ms"] / dec["launches"]
+        gbs = nbytes / (dec_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "ffn_fc1_decode", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": kernel_traffic("ffn_fc1_decode", wl.name),
+                    "peak_source": peaks["source"] + " (copy bandwidth)", "active_experts": active,
+                    "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": dec_ms}
+    elif fc1 and fc1["launches"]:
         fc1_ms = fc1["total_ms"] / fc1["launches"]
         flops = 2.0 * S * H * (2 * I)          # FC1: S routed rows x H x 2I
         ach = flops / (fc1_ms / 1e3) / 1e12

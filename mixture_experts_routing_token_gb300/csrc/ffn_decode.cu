@@ -24,7 +24,7 @@
 //               FC2 y * routing weight -> float32 staging row of the slot.
 // All waits are bounded as in the prefill kernel.
 //
-// Inside the layer call (router logits given, E <= 64, T*k <= kLocalSlots) the
+// Inside the layer call (router logits given, E <= 64, T <= 16) the
 // FC1 kernel does not wait for the routing kernel before it streams weights:
 // every CTA repeats the top-k selection of the batch's tokens (the same
 // comparisons, ties toward the lower expert, so the same experts) and the
@@ -44,8 +44,9 @@ constexpr int DK = 64;           // K per stage (one 128-byte swizzle row)
 constexpr int DSTAGES_MAX = 12;
 constexpr int DTHREADS = 192;
 constexpr uint64_t DWAIT_NS = 2000000000ull;
-constexpr int kLocalExperts = 64;   // local routing: a warp per token, two experts per lane (E <= 64)
-constexpr int kLocalSlots = 512;    // and at most this many routed slots
+constexpr int kLocalExperts = 64;   // local routing: a warp per token, two experts per lane (E <= 64),
+constexpr int kLocalTokens = 16;    // for at most this many tokens (more cost FC1 what the overlap gains)
+constexpr int kLocalSlots = kLocalTokens * kLocalExperts;
 
 enum { DEC_FC1 = 0, DEC_FC2 = 1 };
 
@@ -113,14 +114,15 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   __shared__ int tile_start[MOE_MAX_EXPERTS + 1];
   // local routing (FC1 with logits): selected experts, counts, offsets and the
   // expert-sorted token ids
-  __shared__ int32_t l_idx[MODE == DEC_FC1 ? kLocalSlots : 1];
-  __shared__ int32_t l_ids[MODE == DEC_FC1 ? kLocalSlots : 1];
-  __shared__ int32_t l_cnt[MODE == DEC_FC1 ? kLocalExperts : 1], l_off[MODE == DEC_FC1 ? kLocalExperts + 1 : 1];
-  __shared__ int32_t l_run[MODE == DEC_FC1 ? kLocalExperts : 1];
+  constexpr bool kCanRoute = MODE == DEC_FC1 && NTOK == kLocalTokens;
+  __shared__ int32_t l_idx[kCanRoute ? kLocalSlots : 1];
+  __shared__ int32_t l_ids[kCanRoute ? kLocalSlots : 1];
+  __shared__ int32_t l_cnt[kCanRoute ? kLocalExperts : 1], l_off[kCanRoute ? kLocalExperts + 1 : 1];
+  __shared__ int32_t l_run[kCanRoute ? kLocalExperts : 1];
   extern __shared__ uint8_t dsmem_raw[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool local = MODE == DEC_FC1 && P.logits != nullptr;
+  const bool local = kCanRoute && P.logits != nullptr;
   const int32_t* counts = local ? l_cnt : P.counts;
   const int32_t* offsets = local ? l_off : P.offsets;
   const int32_t* sorted_ids = local ? l_ids : P.sorted_ids;
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   // from two launches back and are complete once FC1 has triggered.
   if (MODE == DEC_FC1 && !local) pdl_wait();
   if (!local) pdl_trigger();
-  if (MODE == DEC_FC1 && local) {
+  if (kCanRoute && local) {
     // the routing of the batch, as the routing kernel computes it: top-k experts of
     // each token, then each slot's rank among the earlier slots of its expert
     const int S = P.T * P.k;
@@ -429,7 +431,7 @@ int run_decode(const FfnArgs& a, cudaStream_t s) {
   if ((rc = make_tmap(&x1, a.hidden, (uint64_t)a.T, (uint64_t)a.H, 1))) return rc;
   if ((rc = make_tmap(&w2, a.w2, (uint64_t)a.E * a.H, (uint64_t)a.I, DM))) return rc;
   if ((rc = make_tmap(&x2, a.act, (uint64_t)S, (uint64_t)a.I, NTOK))) return rc;
-  const bool local = a.logits && a.E <= kLocalExperts && S <= kLocalSlots;
+  const bool local = a.logits && a.E <= kLocalExperts && a.T <= kLocalTokens;
   DecParams p1{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.H, a.I,
                (a.I + DM - 1) / DM, 2 * a.I, a.act, a.status, local ? a.logits : nullptr, a.norm, a.T, a.k};
   if ((rc = launch_dec<DEC_FC1, NTOK>(w1, x1, p1, S, s, "ffn_fc1_decode"))) return rc;

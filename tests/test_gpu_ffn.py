@@ -69,13 +69,13 @@ def test_layer_tensor_core_shapes(T, H, I, E, k, norm):
 
 
 # decode (weight-streaming, T <= 64) kernels at every token-chunk width and around the threshold;
-# in the layer call FC1 routes its tokens itself when E <= 64 and T*k <= 512 (else it waits
+# in the layer call FC1 routes its tokens itself when E <= 64 and T <= 16 (else it waits
 # for the routing kernel): E % 4 != 0, k > 8, norm=False and both fallbacks are covered
 @pytest.mark.parametrize("T,H,I,E,k,norm", [
     (1, 256, 128, 8, 2, True), (3, 128, 192, 16, 4, True), (16, 256, 256, 64, 8, True),
     (17, 128, 384, 32, 8, True), (33, 192, 320, 64, 8, True), (64, 256, 128, 8, 2, True),
     (64, 128, 256, 64, 8, True), (65, 128, 256, 64, 8, True),
-    (2, 128, 128, 5, 3, False), (40, 128, 128, 64, 10, True), (8, 128, 128, 100, 8, True),
+    (2, 128, 128, 5, 3, False), (12, 128, 128, 64, 10, True), (8, 128, 128, 100, 8, True),
     (60, 128, 128, 64, 9, False),
 ])
 def test_layer_decode_shapes(T, H, I, E, k, norm):
