@@ -173,7 +173,7 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
     """Each routing kernel on a token count large enough that its inputs and outputs
     (>= 768 MiB) stream through HBM rather than L2: algorithmic bytes / CUDA-event time.
 
-    Bytes per token (SURVEY-style accounting of what the method must move):
+    Bytes per token (what the method must move at the least):
       gating 4E + 8k (bf16 logits: 2E + 8k); indices->multihot 8k + 9E;
       multihot->indices 8E + 8k (probs and indices out); align 8k in + 12k out (+ E-sized
       tables); group-limited top-k (DeepSeek-V3 shape E=256, 8 groups, keep 4, k=8) 4E + 8k.

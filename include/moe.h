@@ -58,7 +58,7 @@ extern "C" {
 /* return codes */
 #define MOE_OK 0
 #define MOE_ERR_INVALID_ARG 1   /* null pointer, bad size, misalignment, k > E ... */
-#define MOE_ERR_UNSUPPORTED 2   /* a dtype/shape combination this build does not run */
+#define MOE_ERR_UNSUPPORTED 2   /* a dtype/shape combination the library does not run */
 #define MOE_ERR_CUDA 3          /* a CUDA runtime or launch error */
 #define MOE_ERR_WORKSPACE 4     /* workspace pointer null/misaligned or too small */
 
