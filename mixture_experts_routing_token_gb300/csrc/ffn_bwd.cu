@@ -146,21 +146,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 32 values of one row: workspace rows (32-byte aligned) move in whole 32-byte
+// sectors; store_bf16x32_16 is for caller buffers (16-byte aligned).
 __device__ __forceinline__ void load_f32x32(const float* p, float (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 q = *reinterpret_cast<const float4*>(p + 4 * i);
-    v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+  for (int i = 0; i < 4; ++i) {
+    uint32_t q[8];
+    ld_v8(p + 8 * i, q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[8 * i + j] = __uint_as_float(q[j]);
   }
 }
 
 __device__ __forceinline__ void store_f32x32(float* p, const float (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    *reinterpret_cast<float4*>(p + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  for (int i = 0; i < 4; ++i) {
+    float q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = v[8 * i + j];
+    st_v8(p + 8 * i, q);
+  }
 }
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = pack_bf16x2(v[16 * i + 2 * j], v[16 * i + 2 * j + 1]);
+    st_v8(p + 16 * i, q);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32_16(__nv_bfloat16* p, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -169,15 +187,14 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)
 }
 
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[32]) {
-  const uint4* s = reinterpret_cast<const uint4*>(p);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = s[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  for (int i = 0; i < 2; ++i) {
+    uint32_t w[8];
+    ld_v8(p + 16 * i, w);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    for (int j = 0; j < 8; ++j) {
+      v[16 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[16 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
     }
   }
 }
@@ -351,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAX_THREADS, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(y[i]);
-            store_bf16x32(dst + n0, v);
+            store_bf16x32_16(dst + n0, v);
           }
         }
       } else {

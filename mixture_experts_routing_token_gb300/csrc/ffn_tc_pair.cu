@@ -335,9 +335,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
               const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
               pk[i] = pack2(a0, a1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(act + p * I + col0);
+            uint32_t lo8[8], hi8[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) { lo8[i] = pk[i]; hi8[i] = pk[8 + i]; }
+            st_v8(act + p * I + col0, lo8);        // two whole 32-byte sectors
+            st_v8(act + p * I + col0 + 16, hi8);
           }
         }
       } else {
@@ -352,11 +354,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           ptx::tmem_ld_wait();
           const int col0 = ti.n_tile * PBN + c * 32;
           if (valid && col0 < H) {
-            float4* dst = reinterpret_cast<float4*>(staging + dst_row * H + col0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(y[4 * i]) * wt, __uint_as_float(y[4 * i + 1]) * wt,
-                                   __uint_as_float(y[4 * i + 2]) * wt, __uint_as_float(y[4 * i + 3]) * wt);
+            for (int i = 0; i < 4; ++i) {   // whole 32-byte sectors
+              float o[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o[j] = __uint_as_float(y[8 * i + j]) * wt;
+              st_v8(staging + dst_row * H + col0 + 8 * i, o);
+            }
           }
         }
       }
