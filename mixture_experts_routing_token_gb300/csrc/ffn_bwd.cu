@@ -98,6 +98,7 @@ struct BwdParams {
   float* dwp;
   float* staging;
   __nv_bfloat16* dw;
+  int dw_sector;    // WGRAD: dw is 32-byte aligned, so its rows take whole-sector stores
   int32_t* status;
 };
 
@@ -368,7 +369,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MAX_THREADS, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(y[i]);
-            store_bf16x32_16(dst + n0, v);
+            if (P.dw_sector) store_bf16x32(dst + n0, v);
+            else store_bf16x32_16(dst + n0, v);
           }
         }
       } else {
@@ -978,6 +980,7 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
   p.MT = (H + BN - 1) / BN;
   p.NT = (I + BN - 1) / BN;
   p.dw = static_cast<__nv_bfloat16*>(a.d_w2);
+  p.dw_sector = (reinterpret_cast<uintptr_t>(p.dw) & 31) == 0;
   if ((rc = launch_bwd_pair<WGRAD>(ta, tb, p, (long)E * p.MT * p.NT, s, "bwd_wgrad_w2"))) return rc;
   if ((rc = make_tmap(&ta, a.dgu, (uint64_t)Pmax, (uint64_t)2 * I, 64))) return rc;
   if ((rc = make_tmap(&tb, a.xs, (uint64_t)Pmax, (uint64_t)H, 64))) return rc;
@@ -986,6 +989,7 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
   p.MT = (2 * I + BN - 1) / BN;
   p.NT = (H + BN - 1) / BN;
   p.dw = static_cast<__nv_bfloat16*>(a.d_w13);
+  p.dw_sector = (reinterpret_cast<uintptr_t>(p.dw) & 31) == 0;
   if ((rc = launch_bwd_pair<WGRAD>(ta, tb, p, (long)E * p.MT * p.NT, s, "bwd_wgrad_w13"))) return rc;
   if ((rc = launch_small("bwd_zero_empty", bwd_zero_empty_kernel, dim3(64, (unsigned)std::min(E, 1024)), 256, 0,
                          s, a.counts, E, (long)2 * I * H / 8, (long)H * I / 8, static_cast<uint4*>(a.d_w13),

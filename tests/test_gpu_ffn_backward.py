@@ -115,6 +115,31 @@ def test_backward_dropped_slots_and_stale_workspace():
     assert (dwt.cpu().numpy()[idx < 0] == 0).all()
 
 
+def test_backward_weight_gradients_16_byte_aligned_only():
+    """d_w13 / d_w2 on a 16- but not 32-byte boundary take 16-byte stores; same results."""
+    moe = need_gpu()
+    T, H, I, E, k = 300, 256, 256, 6, 2
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, dtype="bf16", logits="distinct", seed=21)
+    w, idx = gating.softmax_topk(d["logits"], k, True)
+    al = align.align_by_expert(idx, w, E)
+    t = _routing_tensors(al)
+    dO = to_dev(gen_normal(np.random.SeedSequence(4), (T, H), 1.0, "bf16"), "bf16")
+    args = (to_dev(d["hidden"], "bf16"), to_dev(d["w13"], "bf16"), to_dev(d["w2"], "bf16"), k, t["counts"],
+            t["offsets"], t["sorted_token_ids"], t["sorted_weights"], t["reverse_indices"], dO)
+    n13, n2 = E * 2 * I * H, E * H * I
+    b13 = torch.full((n13 + 16,), 7.0, dtype=torch.bfloat16, device=DEV)
+    b2 = torch.full((n2 + 16,), 7.0, dtype=torch.bfloat16, device=DEV)
+    dw13 = b13[8:8 + n13].view(E, 2 * I, H)
+    dw2 = b2[8:8 + n2].view(E, H, I)
+    assert dw13.data_ptr() % 32 == 16 and dw2.data_ptr() % 32 == 16
+    moe.moe_grouped_ffn_backward(*args, d_w13=dw13, d_w2=dw2)
+    ref = moe.moe_grouped_ffn_backward(*args)
+    torch.cuda.synchronize()
+    assert torch.equal(dw13, ref[1]) and torch.equal(dw2, ref[2])
+    for b, n in ((b13, n13), (b2, n2)):   # nothing written outside the views
+        assert (b[:8] == 7).all() and (b[8 + n:] == 7).all()
+
+
 def test_backward_repeated_calls_are_identical():
     moe = need_gpu()
     T, H, I, E, k = 600, 256, 256, 8, 2
