@@ -774,28 +774,45 @@ __global__ void __launch_bounds__(256) bwd_gather_kernel(
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_poff[e] = __ldg(poff + e);
   __syncthreads();
   const long n = min(Pmax, (long)s_poff[E]) * H8;
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const int q = (int)div_idx(i, H8, sh);
-    const int c = (int)(i - (long)q * H8);
-    const int e = find_segment(s_poff, E, q);
-    const int r = q - s_poff[e];
-    uint4 x = make_uint4(0, 0, 0, 0), d = x, dy = x;
-    if (r < __ldg(counts + e)) {
-      const int p = __ldg(offsets + e) + r;
-      const long t = __ldg(ids + p);
-      const float w = __ldg(sw + p);
-      x = __ldg(hidden + t * H8 + c);
-      d = __ldg(dout + t * H8 + c);
-      const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
-      uint32_t o[4];
+  const long stride = (long)gridDim.x * blockDim.x;
+  constexpr int U = 4;   // rows chunks per thread loaded before any store (more reads in flight)
+  for (long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += U * stride) {
+    uint4 x[U], d[U];
+    float w[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        o[j] = pack_bf16x2(w * __uint_as_float(dw[j] << 16), w * __uint_as_float(dw[j] & 0xffff0000u));
-      dy = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int u = 0; u < U; ++u) {
+      x[u] = make_uint4(0, 0, 0, 0);
+      d[u] = x[u];
+      w[u] = 0.0f;
+      const long i = i0 + u * stride;
+      if (i < n) {
+        const int q = (int)div_idx(i, H8, sh);
+        const int c = (int)(i - (long)q * H8);
+        const int e = find_segment(s_poff, E, q);
+        const int r = q - s_poff[e];
+        if (r < __ldg(counts + e)) {
+          const int p = __ldg(offsets + e) + r;
+          const long t = __ldg(ids + p);
+          w[u] = __ldg(sw + p);
+          x[u] = __ldg(hidden + t * H8 + c);
+          d[u] = __ldg(dout + t * H8 + c);
+        }
+      }
     }
-    xs[i] = x;
-    dos[i] = d;
-    dys[i] = dy;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long i = i0 + u * stride;
+      if (i < n) {
+        const uint32_t dw[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = pack_bf16x2(w[u] * __uint_as_float(dw[j] << 16), w[u] * __uint_as_float(dw[j] & 0xffff0000u));
+        xs[i] = x[u];
+        dos[i] = d[u];
+        dys[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
   }
 }
 
