@@ -16,7 +16,10 @@
 // kernels of ffn_decode.cu instead.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -35,6 +38,74 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, const int32
     const int c = (int)(i - p * H16);
     xs[i] = __ldg(hidden + (long)__ldg(ids + p) * H16 + c);
   }
+}
+
+// The same copy with TMA bulk transfers (rows of at most kBulkRowMax bytes):
+// warp w takes batches of R consecutive sorted rows; its lane 0 loads the R
+// token rows of `hidden` into the warp's shared-memory slots (one mbarrier per
+// slot, bounded waits), then writes the batch to x_sorted as ONE contiguous
+// bulk store, and reuses the slots once that store has read them. The copy
+// engine moves the bytes, so R whole rows per warp are in flight with almost
+// no instructions.
+constexpr int kBulkWarps = 8;
+constexpr int kBulkMaxR = 4;
+constexpr int kBulkSmem = 128 * 1024;
+constexpr int kBulkRowMax = kBulkSmem / kBulkWarps;
+constexpr uint64_t kBulkWaitNs = 2000000000ull;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kBulkWarps * 32) gather_rows_bulk_kernel(
+    const uint8_t* __restrict__ hidden, const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
+    int E, int row_bytes, int R, uint8_t* __restrict__ xs, int32_t* status) {
+  extern __shared__ __align__(128) uint8_t slots[];   // [kBulkWarps][R][row_bytes]
+  __shared__ __align__(8) uint64_t bar[kBulkWarps][kBulkMaxR];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (lane == 0)
+    for (int r = 0; r < R; ++r) ptx::mbar_init(ptx::smem_u32(&bar[warp][r]), 1);
+  ptx::fence_mbar_init();
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  if (lane != 0) return;
+  volatile int* abort_p = &abort_flag;
+  const int n = __ldg(offsets + E);
+  const int nw = gridDim.x * kBulkWarps;
+  const uint32_t my = ptx::smem_u32(slots) + (uint32_t)(warp * R * row_bytes);
+  uint32_t ph = 0;
+  for (long p0 = (long)(blockIdx.x * kBulkWarps + warp) * R; p0 < n; p0 += (long)nw * R) {
+    const int nr = (int)min((long)R, n - p0);
+    for (int r = 0; r < nr; ++r) {
+      const uint32_t b = ptx::smem_u32(&bar[warp][r]);
+      ptx::mbar_arrive_expect_tx(b, (uint32_t)row_bytes);
+      bulk_load(my + (uint32_t)(r * row_bytes), hidden + (long)__ldg(ids + p0 + r) * row_bytes, (uint32_t)row_bytes, b);
+    }
+    bool ok = true;
+    for (int r = 0; r < nr && ok; ++r) ok = ptx::mbar_wait(ptx::smem_u32(&bar[warp][r]), ph, abort_p, kBulkWaitNs);
+    if (!ok) {   // let the loads still in flight land (bounded) before the slots go away
+      for (int r = 0; r < nr; ++r) {
+        int dummy = 0;
+        ptx::mbar_wait(ptx::smem_u32(&bar[warp][r]), ph, &dummy, kBulkWaitNs / 2);
+      }
+      if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
+      break;
+    }
+    bulk_store(xs + p0 * row_bytes, my, (uint32_t)(nr * row_bytes));
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the slots may be refilled
+    ph ^= 1u;
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---- host -------------------------------------------------------------------
@@ -88,9 +159,26 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   int rc;
   {
     ProfScope ps("gather_rows", s);
-    const cudaError_t e = launch_pdl(gather_rows_kernel, num_sms() * 4, 256, 0, s,
-                                     static_cast<const uint4*>(a.hidden), a.sorted_ids, a.offsets, a.E,
-                                     a.H / 8, pow2_shift(a.H / 8), static_cast<uint4*>(a.xs));
+    const int row_bytes = a.H * 2;
+    cudaError_t e;
+    if (row_bytes <= kBulkRowMax) {
+      static bool attr[64] = {};
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (dev < 64 && !attr[dev]) {
+        if (cudaFuncSetAttribute(gather_rows_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem) !=
+            cudaSuccess)
+          return check_launch("gather_rows");
+        attr[dev] = true;
+      }
+      const int R = std::min(kBulkMaxR, kBulkRowMax / row_bytes);
+      e = launch_pdl(gather_rows_bulk_kernel, num_sms(), kBulkWarps * 32, (size_t)kBulkWarps * R * row_bytes, s,
+                     static_cast<const uint8_t*>(a.hidden), a.sorted_ids, a.offsets, a.E, row_bytes, R,
+                     static_cast<uint8_t*>(a.xs), a.status);
+    } else {
+      e = launch_pdl(gather_rows_kernel, num_sms() * 4, 256, 0, s, static_cast<const uint4*>(a.hidden),
+                     a.sorted_ids, a.offsets, a.E, a.H / 8, pow2_shift(a.H / 8), static_cast<uint4*>(a.xs));
+    }
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gather_rows: %s", cudaGetErrorString(e));
     if ((rc = check_launch("gather_rows"))) return rc;
   }
