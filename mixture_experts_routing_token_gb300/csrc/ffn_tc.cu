@@ -6,10 +6,11 @@
 // token's row; mlc-llm moe_misc.py, scatter_output and moe_sum.
 //
 // Steps on the caller's stream, no host synchronisation:
-//   1. gather_rows_kernel copies the expert-sorted token rows of `hidden`
-//      into x_sorted (the FC1 A operand; one tiled TMA load per pipeline
-//      stage then feeds the MMA; a fused four-row TMA gather per stage was
-//      measured 3.4x slower on GB300);
+//   1. gather_rows_bulk_kernel (rows up to 16 KB; else gather_rows_kernel)
+//      copies the expert-sorted token rows of `hidden` into x_sorted (the
+//      FC1 A operand; one tiled TMA load per pipeline stage then feeds the
+//      MMA; a fused four-row TMA gather per stage was measured 3.4x slower
+//      on GB300);
 //   2. FC1 and FC2 run as persistent 2-SM grouped GEMMs (ffn_tc_pair.cu);
 //   3. the combine kernel sums each token's k weighted rows (combine.cu).
 // Batches of at most kDecodeMaxTokens tokens take the weight-streaming

@@ -74,9 +74,10 @@ int launch_gating_t(const In* logits, int T, int E, int k, int norm, float* w, i
 }
 
 // ---------------------------------------------------------------------------
-// indices -> multihot: one thread writes 4 consecutive experts of one row
-// (three 16/4-byte vector stores); it reads the row's k indices and probs as
-// vectors when k is 1, 2, 4 or 8 (the rows of a token's threads share them in L1).
+// indices -> multihot: one thread writes 8 consecutive experts of one row when
+// E % 8 == 0 (whole 32-byte sectors, indices_to_multihot8_kernel), else 4 (three
+// 16/4-byte vector stores); it reads the row's k indices and probs as vectors
+// when k is 1, 2, 4 or 8 (the row's threads share them in L1).
 
 template <int K>
 __device__ __forceinline__ void load_row(const int32_t* __restrict__ idx, const float* __restrict__ probs,
