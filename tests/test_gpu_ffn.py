@@ -61,6 +61,7 @@ def test_decode_workloads_full(name):
     (100, 128, 128, 256, 8, False),     # one-launch routing with a warp per token (E > 128)
     (129, 256, 128, 64, 8, True),       # first batch size past the one-launch routing
     (90, 192, 192, 12, 3, False),       # E % 4 != 0: scalar row staging
+    (150, 8256, 128, 4, 2, True),       # rows over 16 KB: the vector-copy gather instead of bulk copies
 ])
 def test_layer_tensor_core_shapes(T, H, I, E, k, norm):
     moe = need_gpu()
