@@ -19,7 +19,7 @@
 //      from chunk_hist (summing the few chunks before it, or reading the
 //      prefix), then ranks its slots in one round: warp w takes 256
 //      consecutive slots in 8 sub-rounds of 32 (lanes of the same expert by
-//      __match_any_sync, or per-bit ballots above 16 experts, + popc of
+//      __match_any_sync, or per-bit ballots above 16 experts here, + popc of
 //      lower lanes on top of the warp's running per-expert count), a
 //      per-expert prefix over the warps' counts places the warps, the slots go
 //      to an expert-sorted copy of the chunk in shared memory, and each
@@ -43,8 +43,9 @@ __device__ __forceinline__ int valid_expert(int e, int E) { return (e >= 0 && e 
 
 // Lanes of the warp holding the same expert as this lane (e >= 0), built from one
 // ballot per bit of the expert id plus one for validity; `bits` = bits of E - 1.
-// Measured against __match_any_sync in the align ranking: 12-14% faster for
-// E = 64 / 128, 5% slower for E = 8, so it is used above 16 experts.
+// Measured against __match_any_sync in the many-CTA align ranking: 12-14% faster
+// for E = 64 / 128, 5% slower for E = 8, so it is used there above 16 experts;
+// the single-CTA small-batch routing (latency-bound) measured slower with it.
 __device__ __forceinline__ unsigned same_expert_lanes(int e, int bits) {
   unsigned m = __ballot_sync(0xffffffffu, e >= 0);
   for (int b = 0; b < bits; ++b) {
@@ -250,7 +251,8 @@ __device__ __forceinline__ void align_chunk(
 #pragma unroll
   for (int u = 0; u < kSub; ++u) {
     const int e = valid_expert(eu[u], E);
-    const unsigned peers = ebits > 4 ? same_expert_lanes(e, ebits) : __match_any_sync(0xffffffffu, e);
+    const unsigned peers =
+        SRC == kSrcGlobal && ebits > 4 ? same_expert_lanes(e, ebits) : __match_any_sync(0xffffffffu, e);
     const int below = __popc(peers & ((1u << lane) - 1u));
     const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
     __syncwarp();
