@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) Mixture-of-Experts layer forward path.
+"""GB300 (sm_103a) Mixture-of-Experts layer forward path (and the backward of its
+grouped FFN).
 
 The compute lives in ``libmoe_gb300.so`` (hand-written CUDA for sm_103a behind
 the C ABI of ``include/moe.h``); this package is its thin Python binding with
