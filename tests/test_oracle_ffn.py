@@ -118,3 +118,41 @@ def test_empty_experts_and_zero_tokens():
     z = ffn.layer_forward(np.zeros((0, 4), np.float32), np.zeros((0, 8), np.float32),
                           np.zeros((4, 6, 8), np.float32), np.zeros((4, 8, 3), np.float32), 2, True, "f32")
     assert z["out"].shape == (0, 8)
+
+
+def _torch_token_major_forward(d, w, idx):
+    """An independent float64 forward, token-major: for every token and each of its k
+    slots, gather the slot's expert weights and evaluate silu(W1 x) * (W3 x), W2, the
+    routing weight and the running sum with torch einsums. No align step, no expert
+    loop, no scatter: it shares with the oracle only the input decoding (to_f64) and
+    the bf16 rounding (pinned on its own above)."""
+    dt = d["dtype"]
+    x = torch.tensor(ffn.to_f64(d["hidden"], dt))
+    W13 = torch.tensor(ffn.to_f64(d["w13"], dt))
+    W2 = torch.tensor(ffn.to_f64(d["w2"], dt))
+    I = d["I"]
+    ii = torch.tensor(idx, dtype=torch.int64)
+    wt = torch.tensor(np.asarray(w, np.float32).astype(np.float64))
+    out = torch.zeros((x.shape[0], x.shape[1]), dtype=torch.float64)
+    for j in range(idx.shape[1]):
+        e = ii[:, j]
+        g = torch.einsum("th,tih->ti", x, W13[e, :I])
+        u = torch.einsum("th,tih->ti", x, W13[e, I:])
+        a = (torch.nn.functional.silu(g) * u).numpy()
+        if dt == "bf16":
+            a = ffn.bf16_round(a)
+        out = out + wt[:, j:j + 1] * torch.einsum("ti,thi->th", torch.tensor(a), W2[e])
+    out = out.numpy()
+    return ffn.bf16_round(out) if dt == "bf16" else out.astype(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,H,I,E,k,norm", [(37, 24, 40, 6, 3, False), (64, 128, 96, 8, 2, True),
+                                            (19, 16, 8, 16, 4, True)])
+def test_layer_forward_matches_an_independent_token_major_forward(dtype, T, H, I, E, k, norm):
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, norm_topk_prob=norm, dtype=dtype, logits="distinct",
+                          seed=T + H + I)
+    res = ffn.layer_forward(d["logits"], d["hidden"], d["w13"], d["w2"], k, norm, dtype)
+    ref = _torch_token_major_forward(d, res["topk_weights"], res["topk_indices"])
+    assert np.abs(ref).max() > 0
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-12, atol=1e-300)
