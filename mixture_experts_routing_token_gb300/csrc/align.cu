@@ -25,6 +25,7 @@
 //      to an expert-sorted copy of the chunk in shared memory, and each
 //      expert's run is copied out with consecutive threads (coalesced stores).
 // A single-chunk problem runs as one launch (the CTA makes its own histogram).
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -355,13 +356,8 @@ template <typename Kernel>
 int launch_route_small_k(Kernel kernel, size_t smem, size_t smem_max, const float* logits, int T, int E,
                          int k, int norm, float* w, int32_t* idx, int32_t* counts, int32_t* offsets,
                          int32_t* sorted_ids, float* sorted_w, int32_t* reverse, int32_t* status,
-                         cudaStream_t s, bool* attr) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
-    attr[dev] = true;
-  }
+                         cudaStream_t s) {
+  if (int rc = ensure_smem_limit(kernel, smem_max, "route_small")) return rc;
   ProfScope ps("route_small", s);
   kernel<<<1, kThreads, smem, s>>>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w,
                                    reverse, status);
@@ -372,22 +368,20 @@ template <int EP>
 int launch_route_staged(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                         int32_t* reverse, int32_t* status, cudaStream_t s) {
-  static bool attr[64] = {};
   const size_t stage = (size_t)EP * gate::kStageLd * sizeof(float);
   const size_t copies = (size_t)T * k * (sizeof(int32_t) + sizeof(float));
   return launch_route_small_k(route_small_staged_kernel<EP>, stage + align_smem_bytes(E) + copies,
                               stage + align_smem_bytes(EP) + (size_t)kChunk * 8, logits, T, E, k, norm, w, idx,
-                              counts, offsets, sorted_ids, sorted_w, reverse, status, s, attr);
+                              counts, offsets, sorted_ids, sorted_w, reverse, status, s);
 }
 
 template <int V>
 int launch_route_warp(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                       int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                       int32_t* reverse, int32_t* status, cudaStream_t s) {
-  static bool attr[64] = {};
   return launch_route_small_k(route_small_kernel<32, V>, align_smem_bytes(E), align_smem_bytes(MOE_MAX_EXPERTS),
                               logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse,
-                              status, s, attr);
+                              status, s);
 }
 
 }  // namespace
@@ -413,8 +407,8 @@ int launch_route_small(const float* logits, int T, int E, int k, int norm, float
 #undef MOE_ROUTE_WARP
 }
 
-size_t align_scratch_bytes(int S, int E) {
-  const size_t nchunks = (size_t)(S + kChunk - 1) / kChunk;
+size_t align_scratch_bytes(long S, int E) {
+  const size_t nchunks = S > 0 ? (size_t)((S + kChunk - 1) / kChunk) : 0;
   return nchunks > 1 ? nchunks * (size_t)E * sizeof(int32_t) : 0;
 }
 
@@ -424,14 +418,8 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
   const long S = (long)T * k;
   const int nchunks = (int)((S + kChunk - 1) / kChunk);
   const size_t smem = align_smem_bytes(E);
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)align_smem_bytes(MOE_MAX_EXPERTS));
-    attr_set[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(align_scatter_kernel, align_smem_bytes(MOE_MAX_EXPERTS), "align_scatter"))
+    return rc;
   int32_t* hist = nullptr;
   if (nchunks > 1) {
     hist = static_cast<int32_t*>(scratch);
@@ -466,41 +454,54 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
 // are fully rewritten before they are read, so nothing needs clearing.
 static __device__ __align__(256) int32_t g_align_scratch[MOE_ALIGN_NOALLOC_SCRATCH_INTS];
 
-// Device address of g_align_scratch on the current device. In host code the
-// array's name is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress, once per device with that device current, on the first
-// call that needs it (that first call should come before any stream capture).
+// Device address of g_align_scratch in the CUDA context current on this thread.
+// In host code the array's name is only a host-side stand-in, so the address
+// is looked up with cudaGetSymbolAddress, with the device current, on the first
+// call that needs the array (ceil(T*k/4096) > 1) in that context: once per
+// device for callers of the runtime's primary context, once more for each
+// context of their own. That first call should come before any stream capture.
+// The address belongs to the context (a context of its own, or the primary
+// context after cudaDeviceReset, has its own copy of the array), so the cache
+// is keyed by the context's process-unique id, never by the device ordinal.
 static int align_scratch_address(int32_t** out) {
   static std::mutex mu;
-  static int32_t* addr[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d above 63", dev);
-  std::lock_guard<std::mutex> lk(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_align_scratch);
-    if (e != cudaSuccess || p == nullptr)
-      return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(align scratch): %s", cudaGetErrorString(e));
-    addr[dev] = static_cast<int32_t*>(p);
+  static std::map<unsigned long long, int32_t*> addr;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0) {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = addr.find(ctx);
+    if (it != addr.end()) {
+      *out = it->second;
+      return MOE_OK;
+    }
   }
-  *out = addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_align_scratch);
+  if (e != cudaSuccess || p == nullptr)
+    return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(align scratch): %s", cudaGetErrorString(e));
+  if (ctx != 0) {   // without a context id the address is looked up on every call
+    std::lock_guard<std::mutex> lk(mu);
+    addr[ctx] = static_cast<int32_t*>(p);
+  }
+  *out = static_cast<int32_t*>(p);
   return MOE_OK;
 }
 
 int launch_align_noalloc(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
                          int32_t* status, cudaStream_t s) {
-  const size_t need = align_scratch_bytes(T * k, E);
+  const long S = (long)T * k;
+  const size_t need = align_scratch_bytes(S, E);
   if (need > sizeof(g_align_scratch))
     return fail(MOE_ERR_UNSUPPORTED,
                 "align without workspace: T*k=%ld with E=%d needs %zu bytes of scratch, above the "
                 "fixed %zu (ceil(T*k/4096)*E must not exceed %d)",
-                (long)T * k, E, need, sizeof(g_align_scratch), MOE_ALIGN_NOALLOC_SCRATCH_INTS);
-  int32_t* scratch = nullptr;
-  int rc = align_scratch_address(&scratch);
-  if (rc) return rc;
+                S, E, need, sizeof(g_align_scratch), MOE_ALIGN_NOALLOC_SCRATCH_INTS);
+  int32_t* scratch = nullptr;   // a single chunk needs no scratch
+  if (need > 0) {
+    const int rc = align_scratch_address(&scratch);
+    if (rc) return rc;
+  }
   return launch_align(idx, w, T, k, E, counts, offsets, sorted_ids, sorted_w, reverse, scratch, status, s);
 }
 

@@ -40,6 +40,60 @@ int num_sms() {
   return n;
 }
 
+namespace {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<F>(p);
+  return nullptr;
+}
+}  // namespace
+
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) {
+    // nothing current on this thread yet: bind (and initialise) the primary context
+    // of the runtime's current device, which the next launch would use anyway
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  }
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;   // never 0 for a real context
+}
+
+int ensure_smem_limit(const void* kernel, size_t bytes, const char* name) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, unsigned long long>, size_t> done;
+  const unsigned long long ctx = current_context_id();
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find({kernel, ctx});
+    if (ctx != 0 && it != done.end() && it->second >= bytes) return MOE_OK;
+  }
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: shared-memory limit %zu: %s", name, bytes, cudaGetErrorString(e));
+  if (ctx != 0) {
+    std::lock_guard<std::mutex> lk(mu);
+    size_t& v = done[{kernel, ctx}];
+    if (v < bytes) v = bytes;
+  }
+  return MOE_OK;
+}
+
 // ---- kernel timing -------------------------------------------------------------
 
 namespace {
@@ -152,7 +206,7 @@ AlignWs carve_align(Carver& c, long S, int E) {
   w.sorted_ids = c.take<int32_t>(S);
   w.sorted_w = c.take<float>(S);
   w.reverse = c.take<int32_t>(S);
-  const size_t sb = align_scratch_bytes((int)S, E);
+  const size_t sb = align_scratch_bytes(S, E);
   w.scratch = c.take<char>(sb ? sb : 1);
   return w;
 }
@@ -264,7 +318,7 @@ MOE_API int moe_multihot_to_indices(const float* probs_in_multihot, const int32_
 
 MOE_API size_t moe_align_workspace_size(int T, int k, int E) {
   if (T < 0 || k < 1 || E < 1) return 0;
-  return align_up(align_scratch_bytes(T * k, E), 256);
+  return align_up(align_scratch_bytes((long)T * k, E), 256);
 }
 
 MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, int T, int k, int E,
@@ -283,7 +337,7 @@ MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, in
   if ((rc = check_tensor(sorted_weights, S, "sorted_weights"))) return rc;
   if ((rc = check_tensor(reverse_indices, S, "reverse_indices"))) return rc;
   if (status && (rc = check_tensor(status, 1, "status"))) return rc;
-  if ((rc = check_ws(ws, ws_bytes, align_scratch_bytes((int)S, E)))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, align_scratch_bytes(S, E)))) return rc;
   return launch_align(indices, weights, T, k, E, counts, offsets, sorted_token_ids, sorted_weights,
                       reverse_indices, ws, status, (cudaStream_t)stream);
 }

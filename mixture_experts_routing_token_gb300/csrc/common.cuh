@@ -19,6 +19,19 @@ int fail(int code, const char* fmt, ...);
 int check_launch(const char* what);
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
+// Process-unique id of the CUDA context current on this thread (the device's
+// primary context is made current first when none is). 0 if it cannot be read.
+unsigned long long current_context_id();
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` in the
+// context current on this thread. Function attributes belong to a context, not
+// to a device ordinal (a caller may run the library under its own driver
+// context beside the primary one), so the setting is remembered per
+// (kernel, context) and made again in a context that has not seen it.
+int ensure_smem_limit(const void* kernel, size_t bytes, const char* name);
+template <typename... KArgs>
+int ensure_smem_limit(void (*kernel)(KArgs...), size_t bytes, const char* name) {
+  return ensure_smem_limit(reinterpret_cast<const void*>(kernel), bytes, name);
+}
 
 // Row of a flat grid-stride index: i / d for d > 0. A shift when d is a power of
 // two (sh = log2(d), from pow2_shift on the host), else an unsigned 32-bit
@@ -69,7 +82,7 @@ int launch_indices_to_multihot(const int32_t* idx, const float* probs, int T, in
 int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E, int k,
                                float* probs, int32_t* idx, cudaStream_t s);
 
-size_t align_scratch_bytes(int S, int E);
+size_t align_scratch_bytes(long S, int E);
 // Gating + align in one single-CTA launch, for at most 128 tokens whose T*k
 // slots fit one align chunk.
 bool route_is_small(int T, int k);
@@ -96,7 +109,7 @@ struct FfnArgs {
   void* out;
   void* act;        // [S, I] dtype
   float* staging;   // [S, H] float32
-  void* xs;         // [S, H] dtype: expert-sorted copy of hidden (only without the TMA gather)
+  void* xs;         // [S, H] dtype: expert-sorted copy of hidden (the FC1 A operand)
   int32_t* status;
   // Router logits [T, E] (or null): with them the decode FC1 kernel derives the
   // routing of its tokens itself (the same top-k and expert order as the routing

@@ -858,15 +858,7 @@ __global__ void __launch_bounds__(256) bwd_zero_empty_kernel(const int32_t* __re
 template <int KIND>
 int launch_bwd_pair(const CUtensorMap& a, const CUtensorMap& b, const BwdParams& p, long max_tiles,
                     cudaStream_t s, const char* name) {
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(bwd_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, DSMEM) !=
-        cudaSuccess)
-      return check_launch(name);
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(bwd_pair_kernel<KIND>, DSMEM, name)) return rc;
   const long pairs = num_sms() / 2;
   const int grid = 2 * (int)std::min(max_tiles, pairs);
   if (grid <= 0) return MOE_OK;
@@ -878,15 +870,7 @@ int launch_bwd_pair(const CUtensorMap& a, const CUtensorMap& b, const BwdParams&
 
 int launch_fused_a(const CUtensorMap& x, const CUtensorMap& dO, const CUtensorMap& w13, const CUtensorMap& w2,
                    const BwdParams& p, long max_tiles, cudaStream_t s) {
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(bwd_fused_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DSMEM) !=
-        cudaSuccess)
-      return check_launch("bwd_fc1_dact");
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(bwd_fused_a_kernel, DSMEM, "bwd_fc1_dact")) return rc;
   const int grid = 2 * (int)std::min(max_tiles, (long)(num_sms() / 2));
   if (grid <= 0) return MOE_OK;
   ProfScope ps("bwd_fc1_dact", s);

@@ -404,15 +404,7 @@ template <int MODE, int NTOK>
 int launch_dec(const CUtensorMap& w, const CUtensorMap& x, const DecParams& p, long S, cudaStream_t s,
                const char* name) {
   using C = DecCfg<MODE, NTOK>;
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(ffn_decode_kernel<MODE, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::DSMEM) != cudaSuccess)
-      return check_launch(name);
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(ffn_decode_kernel<MODE, NTOK>, C::DSMEM, name)) return rc;
   const long max_tiles = ((S + NTOK - 1) / NTOK + p.E) * (long)p.NTW;
   const int grid = (int)(max_tiles < num_sms() ? max_tiles : num_sms());
   if (grid <= 0) return MOE_OK;

@@ -163,15 +163,7 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
     const int row_bytes = a.H * 2;
     cudaError_t e;
     if (row_bytes <= kBulkRowMax) {
-      static bool attr[64] = {};
-      int dev = 0;
-      cudaGetDevice(&dev);
-      if (dev < 64 && !attr[dev]) {
-        if (cudaFuncSetAttribute(gather_rows_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem) !=
-            cudaSuccess)
-          return check_launch("gather_rows");
-        attr[dev] = true;
-      }
+      if ((rc = ensure_smem_limit(gather_rows_bulk_kernel, kBulkSmem, "gather_rows"))) return rc;
       const int R = std::min(kBulkMaxR, kBulkRowMax / row_bytes);
       e = launch_pdl(gather_rows_bulk_kernel, num_sms(), kBulkWarps * 32, (size_t)kBulkWarps * R * row_bytes, s,
                      static_cast<const uint8_t*>(a.hidden), a.sorted_ids, a.offsets, a.E, row_bytes, R,

@@ -1,17 +1,17 @@
 // Grouped expert FFN on SM pairs: tcgen05.mma.cta_group::2, M = 256 (128 rows
 // per SM) x N = 256 x K = 16, accumulators in both SMs' TMEM.
 //
-// Same semantics and tile list as the single-SM kernel in ffn_tc.cu
-// (project_6 moe_expert_gemm.cpp moe_prefill_experts: FC1, silu_and_mul,
-// FC2, routing weight; mlc-llm moe_misc.py scatter_output), with tiles of
-// 256 sorted rows per expert. Each SM of a 2-CTA cluster loads its own 128
+// project_6 moe_expert_gemm.cpp moe_prefill_experts: FC1, silu_and_mul,
+// FC2, routing weight; mlc-llm moe_misc.py scatter_output. Tiles are 256
+// sorted rows of one expert (the tile list is built in every CTA from the
+// align step's counts). Each SM of a 2-CTA cluster loads its own 128
 // rows of A and ONE HALF of the 256 B rows:
 //   FC1: CTA 0 the 128 gate rows n0.., CTA 1 the 128 matching up rows I+n0..;
 //   FC2: CTA 0 rows n0..n0+127 of w2[e], CTA 1 rows n0+128..n0+255.
 // The pair's MMA then leaves, in each SM's TMEM, its 128 rows x all 256
-// columns (FC1: gate columns 0..127, up columns 128..255), so the epilogues
-// are the single-SM ones. Per SM and k-step this moves 32 KB instead of 48 KB
-// for the same tensor work, which is what lets a 6-stage ring hide the
+// columns (FC1: gate columns 0..127, up columns 128..255), so each SM's
+// epilogue sees whole rows. Per SM and k-step this moves 32 KB instead of the
+// 48 KB a one-SM 128 x 256 tile needs for the same tensor work, which is what lets a 6-stage ring hide the
 // L2 -> shared-memory latency.
 //
 // Swapped remainder tiles (FC2). An expert's last tile of at most kSwapMax
@@ -34,7 +34,8 @@
 // Launched with a programmatic dependency on the previous kernel: the prologue
 // (barriers, TMEM, tile list from the counts of the align step, which is
 // complete by then) overlaps that kernel's tail; everything after waits for it.
-// Waits are bounded as in the single-SM kernel; a cluster barrier brackets
+// Every mbarrier wait is bounded (2 s of global time, then the abort path
+// below); a cluster barrier brackets
 // the kernel so neither CTA leaves while the other may still touch its
 // shared memory.
 #include "common.cuh"
@@ -392,15 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
 template <int MODE>
 int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sw, const PairParams& p, long S,
                 cudaStream_t s, const char* name) {
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(ffn_tc_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, PDSMEM) !=
-        cudaSuccess)
-      return check_launch(name);
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(ffn_tc_pair_kernel<MODE>, PDSMEM, name)) return rc;
   const long max_tiles = ((S + 2 * PBM - 1) / (2 * PBM) + p.E) * (long)p.NT;
   const long pairs = num_sms() / 2;
   const int grid = 2 * (int)(max_tiles < pairs ? max_tiles : pairs);

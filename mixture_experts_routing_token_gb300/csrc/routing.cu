@@ -4,9 +4,10 @@
 // multihot: Megatron-LM fused_indices_converter.py, _indices_to_multihot_kernel
 //           and _multihot_to_indices_kernel.
 //
-// Layout: a token's row is handled by a group of L lanes (L = next power of two
-// of E, capped at 32), so small-E rows pack several tokens per warp and every
-// row is read with coalesced loads (lane g holds experts g, g+L, g+2L, ...).
+// Gating dispatch by E: up to 8 experts one thread per token (row in
+// registers); up to 128 one thread per token over a block's rows staged in
+// shared memory; wider rows a group of L lanes per token, lane g holding the
+// V = 64 contiguous experts g*V .. g*V + V - 1 (vector loads of its run).
 #include <float.h>
 #include <math.h>
 
@@ -52,13 +53,7 @@ template <int EP, typename In>
 int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
   const size_t smem = (size_t)EP * gate::kStageLd * sizeof(float);
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    cudaFuncSetAttribute(gating_smem_kernel<EP, In>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
   gating_smem_kernel<EP, In><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
       logits, T, E, k, norm, w, idx);
   return check_launch("gating_softmax_topk");
@@ -627,13 +622,7 @@ template <int EP>
 int launch_group_smem(const float* scores, const float* bias, int T, int E, int k, int n_group, int topk_group,
                       int noaux, float* w, int32_t* idx, cudaStream_t s) {
   const size_t smem = (size_t)(EP + 32) * (kSmemGroupThreads + 1) * sizeof(float);
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    cudaFuncSetAttribute(group_topk_smem_kernel<EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(group_topk_smem_kernel<EP>, smem, "group_limited_topk")) return rc;
   group_topk_smem_kernel<EP><<<(T + kSmemGroupThreads - 1) / kSmemGroupThreads, kSmemGroupThreads, smem, s>>>(
       scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
   return check_launch("group_limited_topk");
@@ -665,14 +654,9 @@ template <int V>
 int launch_group_t(const float* scores, const float* bias, int T, int E, int k, int n_group,
                    int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
   const size_t smem = (size_t)kGroupWarps * E * sizeof(float);
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    cudaFuncSetAttribute(group_topk_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kGroupWarps * MOE_MAX_EXPERTS * (int)sizeof(float));
-    attr[dev] = true;
-  }
+  if (int rc = ensure_smem_limit(group_topk_kernel<V>, (size_t)kGroupWarps * MOE_MAX_EXPERTS * sizeof(float),
+                                 "group_limited_topk"))
+    return rc;
   group_topk_kernel<V><<<(T + kGroupWarps - 1) / kGroupWarps, kGroupWarps * 32, smem, s>>>(
       scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
   return check_launch("group_limited_topk");

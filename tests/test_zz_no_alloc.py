@@ -89,3 +89,71 @@ def test_noalloc_rejects_sizes_beyond_its_fixed_scratch():
     torch.cuda.synchronize()
     for key in KEYS:
         assert torch.equal(got[key], ref[key]), key
+
+
+def test_noalloc_under_a_second_context_of_the_same_device():
+    """A caller with a driver context of its own (beside the runtime's primary
+    context, which torch uses) gets that context's copy of the fixed array: the
+    entry point must not reuse the address it looked up in the primary context."""
+    import ctypes
+    moe = need_gpu()
+    cu = ctypes.CDLL("libcuda.so.1")
+
+    def ok(rc, what):
+        assert rc == 0, f"{what} returned CUresult {rc}"
+
+    T, E, k = 16384, 64, 8            # 32 chunks: the scratch array (and the scan launch) is used
+    S = T * k
+    idx, w = _routing(T, E, k, seed=11, kind="zipf")
+    ref = moe.moe_align_by_expert(idx, w, E)
+    moe.moe_align_by_expert_noalloc(idx, w, E)   # caches the primary context's address first
+    torch.cuda.synchronize()
+    want = {key: ref[key].cpu().numpy() for key in KEYS}
+    host_in = {"indices": np.ascontiguousarray(idx.cpu().numpy()), "weights": np.ascontiguousarray(w.cpu().numpy())}
+    out_shapes = {"counts": (E, np.int32), "offsets": (E + 1, np.int32), "sorted_token_ids": (S, np.int32),
+                  "sorted_weights": (S, np.float32), "reverse_indices": (S, np.int32)}
+
+    dev = ctypes.c_int()
+    ok(cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()), "cuDeviceGet")
+    ctx = ctypes.c_void_p()
+    ok(cu.cuCtxCreate_v4(ctypes.byref(ctx), None, 0, dev), "cuCtxCreate")   # current on this thread now
+    ptrs = {}
+    try:
+        def alloc(name, nbytes):
+            p = ctypes.c_uint64()
+            ok(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(nbytes)), "cuMemAlloc")
+            ptrs[name] = p.value
+        for name, a in host_in.items():
+            alloc(name, a.nbytes)
+            ok(cu.cuMemcpyHtoD_v2(ctypes.c_uint64(ptrs[name]), a.ctypes.data_as(ctypes.c_void_p),
+                                  ctypes.c_size_t(a.nbytes)), "cuMemcpyHtoD")
+        for name, (n, dt) in out_shapes.items():
+            alloc(name, n * np.dtype(dt).itemsize)
+        alloc("status", 4)
+        zero = np.zeros(1, np.int32)
+        ok(cu.cuMemcpyHtoD_v2(ctypes.c_uint64(ptrs["status"]), zero.ctypes.data_as(ctypes.c_void_p),
+                              ctypes.c_size_t(4)), "cuMemcpyHtoD")
+        for call in range(2):
+            rc = moe.lib().moe_align_by_expert_noalloc(
+                ptrs["indices"], ptrs["weights"], T, k, E, ptrs["counts"], ptrs["offsets"],
+                ptrs["sorted_token_ids"], ptrs["sorted_weights"], ptrs["reverse_indices"], ptrs["status"], None)
+            assert rc == 0, moe.lib().moe_last_error().decode()
+            ok(cu.cuCtxSynchronize(), "cuCtxSynchronize")
+            for name, (n, dt) in out_shapes.items():
+                got = np.empty(n, dt)
+                ok(cu.cuMemcpyDtoH_v2(got.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(ptrs[name]),
+                                      ctypes.c_size_t(got.nbytes)), "cuMemcpyDtoH")
+                assert np.array_equal(got.view(np.int32), want[name].reshape(-1).view(np.int32)), (call, name)
+            st = np.empty(1, np.int32)
+            ok(cu.cuMemcpyDtoH_v2(st.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(ptrs["status"]),
+                                  ctypes.c_size_t(4)), "cuMemcpyDtoH")
+            assert st[0] == 0
+    finally:
+        for p in ptrs.values():
+            cu.cuMemFree_v2(ctypes.c_uint64(p))
+        cu.cuCtxDestroy_v2(ctx)
+    # back in the primary context, the cached address still serves
+    got = moe.moe_align_by_expert_noalloc(idx, w, E)
+    torch.cuda.synchronize()
+    for key in KEYS:
+        assert torch.equal(got[key], ref[key]), key
