@@ -1,7 +1,11 @@
 """Benchmark of the MoE layer forward path (one step = gating -> align -> grouped FFN -> combine).
 
-Default workload: Mixtral-shaped prefill, bf16 (T=4096, H=4096, I=14336, E=8,
-top_k=2, norm_topk_prob=True), synthetic seeded inputs resident in HBM.
+Default (headline) workload: the skewed-load large-E prefill, bf16 (T=32768,
+H=4096, I=1536, E=128, top_k=8, norm_topk_prob=True, Zipf(1.2) expert bias),
+the largest configuration; synthetic seeded inputs resident in HBM. After it,
+the JSON line's "workloads" object holds every other configuration (tiny f32,
+Mixtral-shaped prefill, decode T = 1 / 8 / 64, fine-grained prefill), each
+timed for at least 1 s and 200 steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -35,10 +39,12 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral", choices=list(WORKLOADS))
+    ap.add_argument("--workload", default="skew", choices=list(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations (each timed >= 1 s after the headline workload)")
     ap.add_argument("--no-routing", action="store_true", help="skip the large-T routing bandwidth section")
     ap.add_argument("--no-backward", action="store_true", help="skip the FFN backward section")
     ap.add_argument("--backward-only", action="store_true",
@@ -143,24 +149,32 @@ class ClockSampler:
 
 
 def make_device_inputs(wl, device, seed=0):
-    """Seeded synthetic inputs drawn on the device (same recipes as moe_inputs, torch RNG)."""
+    """Seeded synthetic inputs drawn on the device (same recipes as moe_inputs, torch RNG):
+    rows of the logits holding a repeated value are redrawn, as the recipes ask."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     T, H, I, E = wl.T, wl.H, wl.I, wl.E
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     hidden = torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(dt)
-    logits = torch.randn((T, E), generator=g, device=device, dtype=torch.float32)
+    bias = torch.zeros(E, device=device, dtype=torch.float32)
     if wl.logits == "jitter":
-        logits += 1e-3 * torch.arange(E, device=device, dtype=torch.float32)
+        bias = 1e-3 * torch.arange(E, device=device, dtype=torch.float32)
     elif wl.logits == "zipf":
         r = torch.arange(1, E + 1, dtype=torch.float64)
         p = r ** -1.2
-        bias = (2.0 * torch.log(p / p.sum())).float()
+        by_rank = (2.0 * torch.log(p / p.sum())).float()
         perm = torch.randperm(E, generator=torch.Generator().manual_seed(seed))
         b = torch.empty(E)
-        b[perm] = bias
-        logits += b.to(device)
+        b[perm] = by_rank
+        bias = b.to(device)
+    logits = torch.randn((T, E), generator=g, device=device, dtype=torch.float32) + bias
+    for _ in range(100):   # "distinct values": redraw rows with a repeated logit
+        srt = torch.sort(logits, dim=1).values
+        bad = torch.nonzero((srt[:, 1:] == srt[:, :-1]).any(dim=1)).flatten()
+        if bad.numel() == 0:
+            break
+        logits[bad] = torch.randn((bad.numel(), E), generator=g, device=device, dtype=torch.float32) + bias
     w13 = torch.empty((E, 2 * I, H), device=device, dtype=dt)
     w2 = torch.empty((E, H, I), device=device, dtype=dt)
     for e in range(E):   # one expert at a time keeps the fp32 temporaries small
@@ -360,7 +374,7 @@ def run_reference(args, wl, rank, world):
     from oracle import ffn, gating
     import moe_inputs as mi
     d = mi.make_layer_inputs(wl, with_weights=False)
-    n_tok = 8
+    n_tok = max(1, min(8, 16 // wl.k))     # at most 16 experts' weights touched per step
     tok = np.arange(n_tok)
     w, i = gating.softmax_topk(d["logits"], wl.k, wl.norm_topk_prob)
     used = sorted(set(np.unique(i[:n_tok]).tolist()))
@@ -399,8 +413,10 @@ def run_reference(args, wl, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                                            "k": wl.k, "norm_topk_prob": wl.norm_topk_prob},
+            "data": "synthetic", "config": workload_config(wl, world),
+            "inputs": "seeded numpy PCG64 on the host (moe_inputs recipes; weights only of the experts the "
+                      "sample touches, drawn per expert)",
+            "timing": "wall clock over the steps on the host cores",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"each step: oracle routing of all {wl.T} tokens + FFN of {n_tok} tokens; "
                                        "tokens/s extrapolated per token"},
@@ -408,44 +424,62 @@ def run_reference(args, wl, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse()
-    wl = WORKLOADS[args.workload]
-    if args.tokens or args.experts or args.topk:
-        import dataclasses
-        wl = dataclasses.replace(wl, name=wl.name + "_reduced", T=args.tokens or wl.T, E=args.experts or wl.E,
-                                 k=args.topk or wl.k)
-    rank, world, local = dist_env()
-    if args.impl == "reference":
-        run_reference(args, wl, rank, world)
-        return
-    import torch
-    import mixture_experts_routing_token_gb300 as moe
-    from mixture_experts_routing_token_gb300.build import build
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0 or not os.path.exists(moe.LIB_PATH):
-        build()
-    if world > 1:
-        dist.barrier()
-    moe.lib()
+def fp32_simt_peak_tflops():
+    """FP32 FMA rate of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
 
-    if args.routing_only:
-        if rank == 0:
-            print(json.dumps({"workload": wl.name, "routing": routing_bandwidth(moe, wl, dev, measured_peaks(),
-                                                                                 reps=max(1, args.steps))}), flush=True)
-        return
-    hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=rank)
+
+def dominant_roofline(moe, wl, kern, logits, peaks, step_ms):
+    """Roofline of the kernel that bounds the workload, from the per-kernel CUDA-event times.
+
+    decode (T <= 64): ffn_fc1_decode streams the weight rows of the experts the batch
+    routes to: algorithmic bytes = those rows + the token rows + the activations written;
+    the layer step's bandwidth over all active expert weights (w13 and w2) is added.
+    prefill bf16: ffn_fc1_tc, 2 S H 2I flops per launch against the measured bf16 burst peak.
+    float32 (CUDA cores): ffn_fc1_simt, the same flops against the FP32 FMA rate.
+    """
+    import torch
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
-    if args.backward_only:
-        if rank == 0:
-            print(json.dumps({"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
-                              "backward": backward_bench(moe, wl, dev, hidden, logits, w13, w2, measured_peaks(),
-                                                         max(3, min(args.steps, 10)))}), flush=True)
-        return
+    S = T * k
+    dec = kern.get("ffn_fc1_decode")
+    if dec and dec["launches"]:
+        _, ti = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
+        active = int(torch.unique(ti).numel())
+        nbytes = float(active * 2 * I * H * 2 + T * H * 2 + S * I * 2)
+        dec_ms = dec["total_ms"] / dec["launches"]
+        gbs = nbytes / (dec_ms / 1e3) / 1e9
+        step_bytes = float(active * 3 * I * H * 2)
+        return {"bound": "hbm", "kernel": "ffn_fc1_decode", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": kernel_traffic("ffn_fc1_decode", wl.name),
+                "peak_source": peaks["source"] + " (copy bandwidth)", "active_experts": active,
+                "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": dec_ms,
+                "layer_step_weight_GBps": step_bytes / (step_ms / 1e3) / 1e9,
+                "layer_step_weight_frac": step_bytes / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    for name, bound, peak, unit, src in (
+            ("ffn_fc1_tc", "tensor", peaks["bf16_tflops"], "TFLOP/s", peaks["source"] + " (burst bf16, cuBLAS)"),
+            ("ffn_fc1_simt", "alu", fp32_simt_peak_tflops(), "TFLOP/s",
+             "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz")):
+        r = kern.get(name)
+        if r and r["launches"]:
+            ms = r["total_ms"] / r["launches"]
+            flops = 2.0 * S * H * (2 * I)
+            ach = flops / (ms / 1e3) / 1e12
+            return {"bound": bound, "kernel": name, "achieved": ach, "peak": peak, "unit": unit,
+                    "frac": ach / peak, "traffic": kernel_traffic(name, wl.name), "peak_source": src,
+                    "algorithmic_flops_per_launch": flops, "avg_launch_ms": ms}
+    return None
+
+
+def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=0, world=1, clocks=False,
+            min_seconds=0.0, min_steps=0):
+    """One workload: device-timed layer steps, per-kernel times, end-to-end rate.
+
+    steps: timed steps; when min_seconds / min_steps are given the count grows until the
+    timed region lasts at least min_seconds (estimated from the warm-up) and min_steps.
+    """
+    import torch
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=seed)
     dcode = moe.MOE_BF16 if wl.dtype == "bf16" else moe.MOE_F32
     ws = torch.empty(moe.moe_layer_workspace_size(dcode, T, H, I, E, k), dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=hidden.dtype, device=dev)
@@ -455,11 +489,11 @@ def main():
         moe.moe_layer_forward(hidden, logits, w13, w2, k, wl.norm_topk_prob, out=out, workspace=ws,
                               stream=stream)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
 
-    use_graph = args.graph == "on" or (args.graph == "auto" and T <= 64)
+    use_graph = graph_mode == "on" or (graph_mode == "auto" and T <= 64)
     graph = None
     if use_graph:
         # one layer step captured once; the timed region replays it (what a decode loop does)
@@ -478,47 +512,62 @@ def main():
             graph.replay()
         torch.cuda.synchronize()
 
+    def run(n):
+        for _ in range(n):
+            if use_graph:
+                graph.replay()
+            else:
+                step()
+
+    if min_seconds > 0 or min_steps > 0:   # size the timed region from a short probe
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run(5)
+        b.record(stream)
+        torch.cuda.synchronize()
+        est = max(a.elapsed_time(b) / 5, 1e-3)
+        steps = max(steps, min_steps, int(min_seconds * 1e3 / est) + 1)
+
     # per-kernel CUDA-event times (each kernel bracketed on its own stream): a timed
-    # pass of K eager steps just before the timed region, under the clock sampler
-    clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
+    # pass of eager steps just before the timed region
+    clk = None
+    if clocks:
+        clk = ClockSampler(dev.index)
+        clk.start()
+        time.sleep(0.3)
+    n_prof = min(steps, 200)
     moe.profiler_enable(True)
-    for _ in range(args.steps):
+    for _ in range(n_prof):
         step()
     torch.cuda.synchronize()
     moe.profiler_enable(False)
     kern = moe.profiler_report()
 
-    # ---- timed region: K steps, device events on the launching stream. No events
+    # ---- timed region: the steps, device events on the launching stream. No events
     # between the layer's kernels here: an event recorded between two launches
     # serialises the programmatic dependent launch of the second one.
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    tstream = torch.cuda.current_stream(dev)
-    ev0.record(tstream)
-    for _ in range(args.steps):
-        if use_graph:
-            graph.replay()
-        else:
-            step()
-    ev1.record(tstream)
+    ev0.record(stream)
+    run(steps)
+    ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = clk.stop()
+    clk_rec = clk.stop() if clk else None
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
-    ms = ms_total / args.steps
-    value = whole_job_rate(T, world, args.steps, ms_total)
+    ms = ms_total / steps
+    value = whole_job_rate(T, world, steps, ms_total)
 
     # ---- end to end through the public call: pinned host inputs in, output back to host.
     # Every step copies its inputs in and its output back; with two buffer sets the
     # copies of the neighbouring steps run on two copy streams while a step computes
     # (H2D of step i+1 and D2H of step i-1 overlap step i, as a serving loop would).
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         h_hidden = hidden.cpu().pin_memory()
         h_logits = logits.cpu().pin_memory()
         nb = 2
@@ -556,19 +605,88 @@ def main():
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         s_in.wait_stream(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             e2e_step(i)
         stream.wait_stream(s_out)
         b.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(a.elapsed_time(b), dev)
-        h_out = h_out[0]
-        e2e = {"value": whole_job_rate(T, world, args.steps, e_ms), "unit": UNIT,
+        e2e = {"value": whole_job_rate(T, world, steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size() + h_logits.numel() * 4,
-               "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
+               "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(),
+               "ms_per_step": e_ms / steps,
                "copies": "pinned host buffers; the H2D of step i+1 and the D2H of step i-1 overlap step i "
                          "on two copy streams (two device buffer sets)"}
 
+    peaks = measured_peaks()
+    launches = sum(v["launches"] for v in kern.values()) / n_prof
+    per_kernel = {n: {"launches_per_step": v["launches"] / n_prof, "avg_ms": v["total_ms"] / max(v["launches"], 1),
+                      "share": v["total_ms"] / max(sum(x["total_ms"] for x in kern.values()), 1e-12)}
+                  for n, v in kern.items()}
+    res = {"value": value, "ms_per_step": ms, "steps": steps, "use_graph": use_graph,
+           "layer_tflops": 6.0 * T * k * H * I / (ms / 1e3) / 1e12,
+           "roofline": dominant_roofline(moe, wl, kern, logits, peaks, ms), "kernels": per_kernel,
+           "gpu_launches_per_step": launches, "clocks": clk_rec, "e2e": e2e,
+           "timing": ("CUDA graph replay of one layer step" if use_graph else "eager steps") +
+                     "; per-kernel CUDA events (roofline, kernels) from a timed pass of %d eager steps just "
+                     "before, since events between launches serialise the programmatic dependent launches" % n_prof,
+           }
+    return res, (hidden, logits, w13, w2)
+
+
+def workload_config(wl, world):
+    """The workload's configuration, identical for both arms (inputs and timing are reported beside it)."""
+    weights_gb = wl.E * 3 * wl.I * wl.H * (2 if wl.dtype == "bf16" else 4) / 1e9
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+            "norm_topk_prob": wl.norm_topk_prob, "dtype": wl.dtype,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (weights %.2f GB)" % weights_gb if weights_gb > 0.2 else
+                  "inputs smaller than L2: L2-warm steps (latency-bound workload)"}
+
+
+INPUTS_NOTE = "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)); distinct logits)"
+
+
+def main():
+    args = parse()
+    wl = WORKLOADS[args.workload]
+    if args.tokens or args.experts or args.topk:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=wl.name + "_reduced", T=args.tokens or wl.T, E=args.experts or wl.E,
+                                 k=args.topk or wl.k)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    import torch
+    import mixture_experts_routing_token_gb300 as moe
+    from mixture_experts_routing_token_gb300.build import build
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        build()
+    if world > 1:
+        dist.barrier()
+    moe.lib()
+
+    if args.routing_only:
+        if rank == 0:
+            print(json.dumps({"workload": wl.name, "routing": routing_bandwidth(moe, wl, dev, measured_peaks(),
+                                                                                 reps=max(1, args.steps))}), flush=True)
+        return
+    if args.backward_only:
+        hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=rank)
+        if rank == 0:
+            print(json.dumps({"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                              "backward": backward_bench(moe, wl, dev, hidden, logits, w13, w2, measured_peaks(),
+                                                         max(3, min(args.steps, 10)))}), flush=True)
+        return
+
+    res, (hidden, logits, w13, w2) = measure(moe, wl, dev, args.steps, args.warmup, args.graph,
+                                             with_e2e=not args.no_e2e, seed=rank, world=world, clocks=True)
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -576,59 +694,43 @@ def main():
         return
 
     peaks = measured_peaks()
-    S = T * k
-    launches = sum(v["launches"] for v in kern.values()) / args.steps
-    fc1 = kern.get("ffn_fc1_tc") or kern.get("ffn_fc1_simt")
-    dec = kern.get("ffn_fc1_decode")
-    roofline = None
-    if dec and dec["launches"]:
-        # decode: FC1 streams the weight rows of the experts the batch routes to (HBM-bound);
-        # algorithmic bytes = those rows + the token rows + the activations written
-        _, ti = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
-        active = int(torch.unique(ti).numel())
-        nbytes = float(active * 2 * I * H * 2 + T * H * 2 + S * I * 2)
-        dec_ms = dec["total_ms"] / dec["launches"]
-        gbs = nbytes / (dec_ms / 1e3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "ffn_fc1_decode", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": kernel_traffic("ffn_fc1_decode", wl.name),
-                    "peak_source": peaks["source"] + " (copy bandwidth)", "active_experts": active,
-                    "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": dec_ms}
-    elif fc1 and fc1["launches"]:
-        fc1_ms = fc1["total_ms"] / fc1["launches"]
-        flops = 2.0 * S * H * (2 * I)          # FC1: S routed rows x H x 2I
-        ach = flops / (fc1_ms / 1e3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "ffn_fc1_tc", "achieved": ach,
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                    "traffic": kernel_traffic("ffn_fc1_tc", wl.name), "peak_source": peaks["source"] + " (burst bf16, cuBLAS)",
-                    "algorithmic_flops_per_launch": flops, "avg_launch_ms": fc1_ms}
-    per_kernel = {n: {"launches_per_step": v["launches"] / args.steps, "avg_ms": v["total_ms"] / max(v["launches"], 1),
-                      "share": v["total_ms"] / max(sum(x["total_ms"] for x in kern.values()), 1e-12)}
-                  for n, v in kern.items()}
-    ffn_flops = 6.0 * S * H * I
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+    line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
-                       "norm_topk_prob": wl.norm_topk_prob, "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (weights %.2f GB read per step)" % (
-                           (w13.numel() + w2.numel()) * w13.element_size() / 1e9),
-                       "inputs": "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)))",
-                       "timing": ("CUDA graph replay of one layer step" if use_graph else "eager steps") +
-                                 "; per-kernel CUDA events (roofline, kernels) from a timed pass of K eager "
-                                 "steps just before, since events between launches serialise the "
-                                 "programmatic dependent launches"},
-            "layer_tflops": ffn_flops / (ms / 1e3) / 1e12,
-            "roofline": roofline, "kernels": per_kernel, "gpu_launches": launches * args.steps,
-            "gpu_launches_per_step": launches, "clocks": clocks, "e2e": e2e, "lib": moe.version()}
+            "config": workload_config(wl, world), "inputs": INPUTS_NOTE, "timing": res["timing"],
+            "layer_tflops": res["layer_tflops"], "roofline": res["roofline"], "kernels": res["kernels"],
+            "gpu_launches": res["gpu_launches_per_step"] * args.steps,
+            "gpu_launches_per_step": res["gpu_launches_per_step"], "clocks": res["clocks"], "e2e": res["e2e"],
+            "lib": moe.version()}
     if not args.no_routing:
         line["routing"] = routing_bandwidth(moe, wl, dev, peaks)
-    if not args.no_backward and wl.dtype == "bf16" and H % 64 == 0 and I % 64 == 0:
-        line["backward"] = backward_bench(moe, wl, dev, hidden, logits, w13, w2, peaks, max(3, min(args.steps, 10)))
+    if not args.no_backward and wl.dtype == "bf16" and wl.H % 64 == 0 and wl.I % 64 == 0:
+        line["backward"] = backward_bench(moe, wl, dev, hidden, logits, w13, w2, peaks,
+                                          max(3, min(args.steps, 10)))
     if not args.no_cpu_baseline:
         try:
             line["cpu_baseline"] = cpu_baseline(wl, hidden, logits, w13, w2)
         except Exception as ex:   # the baseline is reported, never required
             line["cpu_baseline"] = {"error": repr(ex)}
+    del hidden, logits, w13, w2
+    torch.cuda.empty_cache()
+    if not args.no_workloads and world == 1 and not (args.tokens or args.experts or args.topk):
+        # every other configuration of the benchmark, each timed for >= 1 s and >= 200 steps
+        others = {}
+        for name, w in WORKLOADS.items():
+            if name == wl.name:
+                continue
+            r, bufs = measure(moe, w, dev, 20, 5, "auto", with_e2e=True, seed=0, clocks=True,
+                              min_seconds=1.0, min_steps=200)
+            del bufs
+            torch.cuda.empty_cache()
+            others[name] = {"config": workload_config(w, 1), "timing": r["timing"],
+                            "tokens_per_s": r["value"], "ms_per_step": r["ms_per_step"], "steps": r["steps"],
+                            "layer_tflops": r["layer_tflops"], "e2e_tokens_per_s": (r["e2e"] or {}).get("value"),
+                            "e2e_ms_per_step": (r["e2e"] or {}).get("ms_per_step"),
+                            "roofline": r["roofline"], "kernels": r["kernels"],
+                            "gpu_launches_per_step": r["gpu_launches_per_step"], "clocks": r["clocks"]}
+        line["workloads"] = others
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

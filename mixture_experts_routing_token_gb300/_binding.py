@@ -316,7 +316,7 @@ def moe_grouped_ffn_backward(hidden, w13, w2, k, counts, offsets, sorted_token_i
         _ptr(hidden), _ptr(w13), _ptr(w2), dt, T, H, I, E, k, _ptr(counts), _ptr(offsets),
         _ptr(sorted_token_ids), _ptr(sorted_weights), _ptr(reverse_indices), _ptr(d_out), _ptr(d_hidden),
         _ptr(d_w13), _ptr(d_w2), _ptr(d_weights) if want_d_weights else None, _ptr(workspace),
-        workspace.numel(), _ptr(status), _stream(stream, d)))
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream, d)))
     return d_hidden, d_w13, d_w2, (d_weights if want_d_weights else None)
 
 
