@@ -178,16 +178,16 @@ int check_ffn_dims(int dtype, int H, int I) {
 
 struct FfnWs {
   void* act;
-  float* staging;
+  void* staging;
   void* xs;
 };
 
 size_t dsize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 
-FfnWs carve_ffn(Carver& c, int dtype, long S, int H, int I) {
+FfnWs carve_ffn(Carver& c, int dtype, int T, long S, int H, int I) {
   FfnWs w;
   w.act = c.take<char>((size_t)S * I * dsize(dtype));
-  w.staging = c.take<float>((size_t)S * H);
+  w.staging = c.take<char>((size_t)S * H * (staging_is_bf16(dtype, T, H, I) ? 2 : 4));
   const size_t xs = ffn_uses_tensor_cores(dtype, H, I) ? ffn_tc_extra_bytes(S, H) : 0;
   w.xs = xs ? c.take<char>(xs) : nullptr;
   return w;
@@ -228,7 +228,8 @@ int run_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int 
   FfnArgs a{hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, ids, sw, rev,
             out, w.act, w.staging, w.xs, status, logits, norm};
   if (may_drop) {   // caller routing may hold indices outside [0, E)
-    const int rc = launch_zero_dropped(offsets, E, (long)T * k, H, w.staging, s);
+    const int rc = launch_zero_dropped(offsets, E, (long)T * k, H, w.staging,
+                                       staging_is_bf16(dtype, T, H, I) ? 2 : 4, s);
     if (rc) return rc;
   }
   return ffn_uses_tensor_cores(dtype, H, I) ? launch_ffn_tc(a, s) : launch_ffn_simt(a, s);
@@ -365,7 +366,7 @@ MOE_API int moe_align_by_expert_noalloc(const int32_t* indices, const float* wei
 MOE_API size_t moe_grouped_ffn_workspace_size(int dtype, int T, int H, int I, int E, int k) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1) return 0;
   Carver c(nullptr);
-  carve_ffn(c, dtype, (long)T * k, H, I);
+  carve_ffn(c, dtype, T, (long)T * k, H, I);
   return align_up(c.used, 256);
 }
 
@@ -392,7 +393,7 @@ MOE_API int moe_grouped_ffn(const void* hidden, const void* w13, const void* w2,
   const size_t need = moe_grouped_ffn_workspace_size(dtype, T, H, I, E, k);
   if ((rc = check_ws(ws, ws_bytes, need))) return rc;
   Carver c(ws);
-  const FfnWs w = carve_ffn(c, dtype, S, H, I);
+  const FfnWs w = carve_ffn(c, dtype, T, S, H, I);
   return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, sorted_token_ids,
                  sorted_weights, reverse_indices, out, w, status, (cudaStream_t)stream);
 }
@@ -501,7 +502,7 @@ MOE_API size_t moe_layer_workspace_size(int dtype, int T, int H, int I, int E, i
   c.take<float>(S);
   c.take<int32_t>(S);
   carve_align(c, S, E);
-  carve_ffn(c, dtype, S, H, I);
+  carve_ffn(c, dtype, T, S, H, I);
   return align_up(c.used, 256);
 }
 
@@ -534,7 +535,7 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
   if (topk_weights_or_null) tw = topk_weights_or_null;
   if (topk_indices_or_null) ti = topk_indices_or_null;
   const AlignWs al = carve_align(c, S, E);
-  const FfnWs fw = carve_ffn(c, dtype, S, H, I);
+  const FfnWs fw = carve_ffn(c, dtype, T, S, H, I);
 
   if (route_is_small(T, k)) {
     if ((rc = launch_route_small(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, al.counts, al.offsets,

@@ -108,7 +108,7 @@ struct FfnArgs {
   const int32_t* reverse;
   void* out;
   void* act;        // [S, I] dtype
-  float* staging;   // [S, H] float32
+  void* staging;    // [S, H]: bf16 on the tensor-core prefill path (staging_is_bf16), else float32
   void* xs;         // [S, H] dtype: expert-sorted copy of hidden (the FC1 A operand)
   int32_t* status;
   // Router logits [T, E] (or null): with them the decode FC1 kernel derives the
@@ -168,9 +168,14 @@ bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
 int launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
-// Zeroes the staging rows when the align step dropped slots (offsets[E] < S).
-int launch_zero_dropped(const int32_t* offsets, int E, long S, int H, float* staging, cudaStream_t s);
-int launch_combine(const float* staging, int T, int k, int H, int dtype, void* out,
+// The FFN's weighted slot rows ([S, H] staging) are bf16 on the tensor-core
+// prefill path (bf16, T above the decode threshold) and float32 otherwise.
+bool staging_is_bf16(int dtype, int T, int H, int I);
+// Zeroes the staging rows (elem_bytes each) when the align step dropped slots (offsets[E] < S).
+int launch_zero_dropped(const int32_t* offsets, int E, long S, int H, void* staging, int elem_bytes,
+                        cudaStream_t s);
+// out[t] = sum_j staging[t*k + j] (j ascending, fp32), rounded once to `dtype`.
+int launch_combine(const void* staging, int staging_bf16, int T, int k, int H, int dtype, void* out,
                    cudaStream_t s);
 
 // Launch with programmatic stream serialization (PDL): the kernel may start while

@@ -134,9 +134,16 @@ __device__ __forceinline__ BTile btile(int t, const int* tile_start, const BwdPa
     }
     d.ksteps = (__ldg(P.poff + lo + 1) - __ldg(P.poff + lo)) / BK;
   } else {
+    // as in the forward tile list: the operand with fewer tiles of this expert
+    // stays in L2 (A and B tiles are both 256 rows x K)
     const int mt = (__ldg(P.counts + lo) + 2 * BM - 1) / (2 * BM);
-    d.n_tile = local / mt;
-    d.m_tile = local - d.n_tile * mt;
+    if (mt > P.NT) {
+      d.m_tile = local / P.NT;
+      d.n_tile = local - d.m_tile * P.NT;
+    } else {
+      d.n_tile = local / mt;
+      d.m_tile = local - d.n_tile * mt;
+    }
     d.ksteps = P.K / BK;
   }
   return d;
@@ -964,14 +971,14 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s) {
   }
 
   // dx = dgu W13 into the slot rows, then the sum over k
-  if ((rc = launch_zero_dropped(a.offsets, E, S, H, a.staging, s))) return rc;
+  if ((rc = launch_zero_dropped(a.offsets, E, S, H, a.staging, 4, s))) return rc;
   if ((rc = make_tmap(&ta, a.dgu, (uint64_t)Pmax, (uint64_t)2 * I, 128))) return rc;
   if ((rc = make_tmap(&tb, a.w13, (uint64_t)E * 2 * I, (uint64_t)H, 64))) return rc;
   p.K = 2 * I;
   p.NT = (H + BN - 1) / BN;
   p.b_rows = 2 * I;
   if ((rc = launch_bwd_pair<DGRAD_X>(ta, tb, p, row_tiles * p.NT, s, "bwd_dgrad_x"))) return rc;
-  if ((rc = launch_combine(a.staging, a.T, a.k, H, MOE_BF16, a.d_hidden, s))) return rc;
+  if ((rc = launch_combine(a.staging, 0, a.T, a.k, H, MOE_BF16, a.d_hidden, s))) return rc;
 
   // dW2[e] = dys^T act, dW13[e] = dgu^T xs over the expert's padded rows
   if ((rc = make_tmap(&ta, a.dys, (uint64_t)Pmax, (uint64_t)H, 64))) return rc;

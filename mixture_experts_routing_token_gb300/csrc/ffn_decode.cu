@@ -430,7 +430,7 @@ int run_decode(const FfnArgs& a, cudaStream_t s) {
   DecParams p2{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H,
                (a.H + DM - 1) / DM, a.H, a.staging, a.status, nullptr, 0, a.T, a.k};
   if ((rc = launch_dec<DEC_FC2, NTOK>(w2, x2, p2, S, s, "ffn_fc2_decode"))) return rc;
-  return launch_combine(a.staging, a.T, a.k, a.H, a.dtype, a.out, s);
+  return launch_combine(a.staging, 0, a.T, a.k, a.H, a.dtype, a.out, s);
 }
 
 }  // namespace

@@ -138,11 +138,11 @@ int launch_simt_t(const FfnArgs& a, cudaStream_t s) {
     dim3 grid(gx, (a.H + TN - 1) / TN);
     ffn_simt_kernel<1, T><<<grid, 256, 0, s>>>(
         static_cast<const T*>(a.act), static_cast<const T*>(a.w2), a.counts, a.offsets,
-        a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H, nullptr, a.staging);
+        a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H, nullptr, static_cast<float*>(a.staging));
     int rc = check_launch("ffn_fc2_simt");
     if (rc) return rc;
   }
-  return launch_combine(a.staging, a.T, a.k, a.H, a.dtype, a.out, s);
+  return launch_combine(a.staging, 0, a.T, a.k, a.H, a.dtype, a.out, s);
 }
 
 }  // namespace

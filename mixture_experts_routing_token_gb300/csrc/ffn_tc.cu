@@ -150,6 +150,10 @@ bool ffn_uses_tensor_cores(int dtype, int H, int I) {
   return dtype == MOE_BF16 && H % 64 == 0 && I % 64 == 0 && H > 0 && I > 0;
 }
 
+bool staging_is_bf16(int dtype, int T, int H, int I) {
+  return ffn_uses_tensor_cores(dtype, H, I) && T > kDecodeMaxTokens;
+}
+
 size_t ffn_tc_extra_bytes(long S, int H) { return (size_t)S * H * 2; }
 
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
@@ -182,7 +186,7 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   if ((rc = make_tmap(&tS2, a.act, (uint64_t)S, (uint64_t)a.I, 32))) return rc;
 
   if ((rc = launch_ffn_pair_gemms(a, tA1, tB1, tA2, tB2, tS2, s))) return rc;
-  return launch_combine(a.staging, a.T, a.k, a.H, a.dtype, a.out, s);
+  return launch_combine(a.staging, 1, a.T, a.k, a.H, a.dtype, a.out, s);
 }
 
 }  // namespace moe

@@ -97,7 +97,15 @@ __host__ __device__ __forceinline__ int expert_tiles(int cnt, int NT, int NTs) {
   return full_mtiles(cnt, NTs) * NT + (swap_cols(cnt, NTs) ? NTs : 0);
 }
 
-// Tile t of the list: the expert's 256-row tiles N-tile-major, then its swapped tiles.
+// Tile t of the list: the expert's 256-row tiles, then its swapped tiles. Pairs
+// take consecutive tiles in the same round, so the order within an expert
+// decides which operand they share in L2: with fewer M tiles than N tiles the
+// expert's A rows (mt tiles) stay in L2 while N walks the weights once
+// (N-tile-major); with more M tiles than N tiles its weight tiles (NT of them,
+// at most a few tens of MB) stay in L2 while M walks the rows once
+// (M-tile-major). A and B tiles have the same size (256 rows x K), so the
+// smaller count is the smaller operand. (N-tile-major for an expert with 128
+// M tiles and 12 N tiles streamed its 268 MB of rows past L2 once per N tile.)
 __device__ __forceinline__ PTile ptile(int t, const int* tile_start, const int32_t* counts, int E, int NT,
                                        int NTs) {
   int lo = 0, hi = E;
@@ -111,8 +119,13 @@ __device__ __forceinline__ PTile ptile(int t, const int* tile_start, const int32
   PTile d;
   d.e = lo;
   if (local < mt * NT) {
-    d.n_tile = local / mt;
-    d.m_tile = local - d.n_tile * mt;
+    if (mt > NT) {
+      d.m_tile = local / NT;
+      d.n_tile = local - d.m_tile * NT;
+    } else {
+      d.n_tile = local / mt;
+      d.m_tile = local - d.n_tile * mt;
+    }
     d.swap_n = 0;
   } else {
     d.n_tile = local - mt * NT;
@@ -292,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         const int f = ti.n_tile * (2 * PBM) + (int)rank * PBM + row;
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PBN);
         const int H = P.N_out;
-        float* staging = static_cast<float*>(P.out);
+        __nv_bfloat16* staging = static_cast<__nv_bfloat16*>(P.out);
 #pragma unroll 1
         for (int c = 0; c < ti.swap_n / 32; ++c) {
           uint32_t y[32];
@@ -305,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           for (int j = 0; j < 32; ++j) {
             const float wj = __shfl_sync(0xffffffffu, wl, j);
             const int sj = __shfl_sync(0xffffffffu, sl, j);
-            if (r0 + c * 32 + j < cnt && f < H) staging[(long)sj * H + f] = __uint_as_float(y[j]) * wj;
+            if (r0 + c * 32 + j < cnt && f < H) staging[(long)sj * H + f] = __float2bfloat16_rn(__uint_as_float(y[j]) * wj);
           }
         }
         ptx::tc_fence_before();
@@ -345,7 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         }
       } else {
         const int H = P.N_out;
-        float* staging = static_cast<float*>(P.out);
+        __nv_bfloat16* staging = static_cast<__nv_bfloat16*>(P.out);
         const float wt = valid ? __ldg(P.sorted_w + p) : 0.0f;
         const long dst_row = valid ? (long)__ldg(P.reverse + p) : 0;
 #pragma unroll 1
@@ -354,14 +367,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           ptx::tmem_ld32(taddr + c * 32, y);
           ptx::tmem_ld_wait();
           const int col0 = ti.n_tile * PBN + c * 32;
-          if (valid && col0 < H) {
+          if (valid && col0 < H) {   // 32 bf16 = two whole 32-byte sectors
+            uint32_t lo8[8], hi8[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {   // whole 32-byte sectors
-              float o[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) o[j] = __uint_as_float(y[8 * i + j]) * wt;
-              st_v8(staging + dst_row * H + col0 + 8 * i, o);
+            for (int i = 0; i < 8; ++i) {
+              lo8[i] = pack2(__uint_as_float(y[2 * i]) * wt, __uint_as_float(y[2 * i + 1]) * wt);
+              hi8[i] = pack2(__uint_as_float(y[16 + 2 * i]) * wt, __uint_as_float(y[17 + 2 * i]) * wt);
             }
+            st_v8(staging + dst_row * H + col0, lo8);
+            st_v8(staging + dst_row * H + col0 + 16, hi8);
           }
         }
       }

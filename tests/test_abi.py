@@ -47,7 +47,9 @@ def test_workspace_sizes_without_gpu(built_lib):
     # pure host arithmetic
     S = 4096 * 2
     n = moe.moe_layer_workspace_size(moe.MOE_BF16, 4096, 4096, 14336, 8, 2)
-    assert n >= S * 14336 * 2 + S * 4096 * 4
+    assert n >= S * 14336 * 2 + S * 4096 * 2 + S * 4096 * 2   # act, bf16 staging, sorted token rows
+    # decode batches (T <= 64) keep float32 staging rows
+    assert moe.moe_layer_workspace_size(moe.MOE_BF16, 64, 2048, 1408, 64, 8) >= 512 * 1408 * 2 + 512 * 2048 * 4
     assert moe.moe_align_workspace_size(1, 8, 64) == 0          # single chunk: no scratch
     assert moe.moe_align_workspace_size(32768, 8, 128) >= 64 * 128 * 4
     assert moe.moe_grouped_ffn_workspace_size(moe.MOE_F32, 0, 8, 8, 4, 2) >= 0
