@@ -184,9 +184,10 @@ MOE_API int moe_align_by_expert(const int32_t* indices, const float* weights, in
  *     ceil(T*k / 4096) * E > MOE_ALIGN_NOALLOC_SCRATCH_INTS, are rejected with
  *     MOE_ERR_UNSUPPORTED and a message from moe_last_error(); nothing is
  *     launched. (E = 128 allows T*k up to 2,097,152; E = 1024 up to 262,144.)
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *   - The first call that needs the array (T*k > 4096) in a CUDA context looks
+ *     up its device address in that context (once per device for callers of
+ *     the runtime's primary context; again for each context of their own, or
+ *     after cudaDeviceReset); make that first call before any stream capture.
  *   - All calls share the array: calls whose work overlaps on the GPU (other
  *     streams, other host threads) race and must be serialised by the caller.
  */
@@ -268,6 +269,61 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
                               int norm_topk_prob, void* out, float* topk_weights_or_null,
                               int32_t* topk_indices_or_null, void* ws, size_t ws_bytes,
                               int32_t* status, void* stream);
+
+/*
+ * Expert-parallel exchange: G ranks, rank r owning the E_local = E / G
+ * consecutive experts [r*E_local, (r+1)*E_local). [mgt]
+ * _indices_to_multihot_kernel restricts a rank's routing map to its local
+ * experts; the owner runs [p6] moe_prefill_experts on the rows routed to them;
+ * the sender forms [mlc] scatter_output + moe_sum. These calls are the index
+ * and row work on either side of the two all-to-all exchanges (which the
+ * caller runs, e.g. with NCCL):
+ *   sender:   gating, moe_align_by_expert (global E), moe_gather_rows; the rows
+ *             for owner r are x_sorted[offsets[r*E_local] .. offsets[(r+1)*E_local])
+ *             and go out in rank order, with the [G, E_local] slices of counts;
+ *   owner:    moe_ep_receive_index on the received counts table, then
+ *             moe_grouped_ffn on the received rows with k = 1, sorted_token_ids =
+ *             reverse_indices = perm and weights 1: its output rows stay in the
+ *             received order;
+ *   sender:   the rows come back in x_sorted order; moe_ep_combine.
+ */
+
+/*
+ * x_sorted[p] = hidden[sorted_token_ids[p]] for p < offsets[E] (rows beyond are
+ * left as they are). hidden [T, H] dtype; sorted_token_ids [T*k] and offsets
+ * [E+1] from moe_align_by_expert; x_sorted [T*k, H] dtype. Rows must be a
+ * multiple of 16 bytes (H % 8 == 0 for bf16, H % 4 for float32), else
+ * MOE_ERR_UNSUPPORTED.
+ */
+MOE_API int moe_gather_rows(const void* hidden, const int32_t* sorted_token_ids, const int32_t* offsets,
+                            int dtype, int T, int H, int E, int k, void* x_sorted, void* stream);
+
+/*
+ * Owner side. recv_counts [G, E_local] int32: row g = the counts of this
+ * rank's experts that source g sent (its rows arrive source-major, each
+ * source's rows expert-major); R = their sum (rows received).
+ *   local_counts  [E_local]      rows per local expert;
+ *   local_offsets [E_local + 1]  exclusive prefix;
+ *   perm          [R]            perm[p] = received row at expert-major position
+ *                                p (sources in rank order within an expert).
+ * G * E_local <= 65536. ws / ws_bytes: moe_ep_receive_workspace_size(G, E_local).
+ */
+MOE_API size_t moe_ep_receive_workspace_size(int G, int E_local);
+MOE_API int moe_ep_receive_index(const int32_t* recv_counts, int G, int E_local, int R, int32_t* local_counts,
+                                 int32_t* local_offsets, int32_t* perm, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Sender side, after the return exchange: y_sorted [T*k, H] dtype holds the
+ * expert output of sorted row p (its first offsets[E] rows are used);
+ *   out[t] = sum_{j<k} topk_weights[t, j] * y_sorted[pos(t*k + j)]
+ * where pos inverts reverse_indices (slots the align step dropped add
+ * nothing); float32 accumulation in j order, one rounding to dtype. Rows must
+ * be a multiple of 16 bytes. ws / ws_bytes: moe_ep_combine_workspace_size(T, k).
+ */
+MOE_API size_t moe_ep_combine_workspace_size(int T, int k);
+MOE_API int moe_ep_combine(const void* y_sorted, const float* topk_weights, const int32_t* reverse_indices,
+                           const int32_t* offsets, int dtype, int T, int k, int H, int E, void* out, void* ws,
+                           size_t ws_bytes, void* stream);
 
 /*
  * Kernel timing.  moe_profiler_enable(1) makes every launch of this library

@@ -43,6 +43,11 @@ SIGNATURES = {
                                       _p, _p, _sz, _p, _p]),
     "moe_layer_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_layer_forward": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p, _p]),
+    "moe_gather_rows": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
+    "moe_ep_receive_workspace_size": (_sz, [_i, _i]),
+    "moe_ep_receive_index": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _sz, _p]),
+    "moe_ep_combine_workspace_size": (_sz, [_i, _i]),
+    "moe_ep_combine": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _sz, _p]),
     "moe_profiler_enable": (_i, [_i]),
     "moe_profiler_report": (_i, [ctypes.c_char_p, _sz]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -352,6 +357,56 @@ def moe_layer_forward(hidden, router_logits, w13, w2, k, norm_topk_prob=True, ou
         int(bool(norm_topk_prob)), _ptr(out), _ptr(topk_weights), _ptr(topk_indices),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream, d)))
+    return out
+
+
+def moe_gather_rows(hidden, sorted_token_ids, offsets, k, out=None, stream=None):
+    """Expert-sorted copy of the routed token rows -> x_sorted [T*k, H] (rows p < offsets[E])."""
+    _dev(hidden, "hidden")
+    dt = _dtype_code(hidden)
+    T, H = hidden.shape
+    E = offsets.numel() - 1
+    d = hidden.device
+    out = _out(out, (T * k, H), hidden.dtype, d, "out")
+    _check("moe_gather_rows", lib().moe_gather_rows(
+        _ptr(hidden), _ptr(sorted_token_ids), _ptr(offsets), dt, T, H, E, k, _ptr(out), _stream(stream, d)))
+    return out
+
+
+def moe_ep_receive_index(recv_counts, R, local_counts=None, local_offsets=None, perm=None, workspace=None,
+                         stream=None):
+    """Owner side of the expert-parallel exchange: recv_counts [G, E_local] int32 (device) ->
+    (local_counts [E_local], local_offsets [E_local+1], perm [R]) int32."""
+    _dev(recv_counts, "recv_counts", torch.int32)
+    G, El = recv_counts.shape
+    d = recv_counts.device
+    local_counts = _out(local_counts, (El,), torch.int32, d, "local_counts")
+    local_offsets = _out(local_offsets, (El + 1,), torch.int32, d, "local_offsets")
+    perm = _out(perm, (R,), torch.int32, d, "perm")
+    need = int(lib().moe_ep_receive_workspace_size(G, El))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d)
+    _check("moe_ep_receive_index", lib().moe_ep_receive_index(
+        _ptr(recv_counts), G, El, int(R), _ptr(local_counts), _ptr(local_offsets), _ptr(perm), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream, d)))
+    return local_counts, local_offsets, perm
+
+
+def moe_ep_combine(y_sorted, topk_weights, reverse_indices, offsets, out=None, workspace=None, stream=None):
+    """Sender side after the return exchange: out[t] = sum_j w[t,j] * y_sorted[pos(t, j)] -> [T, H]."""
+    _dev(y_sorted, "y_sorted")
+    dt = _dtype_code(y_sorted)
+    T, k = topk_weights.shape
+    H = y_sorted.shape[1]
+    E = offsets.numel() - 1
+    d = y_sorted.device
+    out = _out(out, (T, H), y_sorted.dtype, d, "out")
+    need = int(lib().moe_ep_combine_workspace_size(T, k))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d)
+    _check("moe_ep_combine", lib().moe_ep_combine(
+        _ptr(y_sorted), _ptr(topk_weights), _ptr(reverse_indices), _ptr(offsets), dt, T, k, H, E, _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, d)))
     return out
 
 

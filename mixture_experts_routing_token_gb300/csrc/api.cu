@@ -554,6 +554,70 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
                  norm_topk_prob != 0);
 }
 
+MOE_API int moe_gather_rows(const void* hidden, const int32_t* sorted_token_ids, const int32_t* offsets,
+                            int dtype, int T, int H, int E, int k, void* x_sorted, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, "dtype must be MOE_F32 or MOE_BF16 (got %d)", dtype);
+  REQUIRE(H >= 1, "H must be >= 1 (got %d)", H);
+  const long S = (long)T * k;
+  if ((rc = check_tensor(hidden, (long)T * H, "hidden"))) return rc;
+  if ((rc = check_tensor(sorted_token_ids, S, "sorted_token_ids"))) return rc;
+  if ((rc = check_tensor(offsets, E + 1, "offsets"))) return rc;
+  if ((rc = check_tensor(x_sorted, S * H, "x_sorted"))) return rc;
+  if (S == 0) return MOE_OK;
+  return launch_gather_rows(hidden, sorted_token_ids, offsets, E, H * (int)dsize(dtype), x_sorted, nullptr,
+                            (cudaStream_t)stream);
+}
+
+MOE_API size_t moe_ep_receive_workspace_size(int G, int E_local) {
+  if (G < 1 || E_local < 1) return 0;
+  return align_up(ep_receive_workspace_bytes(G, E_local), 256);
+}
+
+MOE_API int moe_ep_receive_index(const int32_t* recv_counts, int G, int E_local, int R, int32_t* local_counts,
+                                 int32_t* local_offsets, int32_t* perm, void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  REQUIRE(G >= 1 && E_local >= 1 && E_local <= MOE_MAX_EXPERTS, "need G >= 1 and 1 <= E_local <= %d",
+          MOE_MAX_EXPERTS);
+  REQUIRE((long)G * E_local <= 65536, "G * E_local must not exceed 65536");
+  REQUIRE(R >= 0, "R must be >= 0");
+  if ((rc = check_tensor(recv_counts, (long)G * E_local, "recv_counts"))) return rc;
+  if ((rc = check_tensor(local_counts, E_local, "local_counts"))) return rc;
+  if ((rc = check_tensor(local_offsets, E_local + 1, "local_offsets"))) return rc;
+  if ((rc = check_tensor(perm, R, "perm"))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, ep_receive_workspace_bytes(G, E_local)))) return rc;
+  return launch_ep_receive_index(recv_counts, G, E_local, local_counts, local_offsets, perm, ws,
+                                 (cudaStream_t)stream);
+}
+
+MOE_API size_t moe_ep_combine_workspace_size(int T, int k) {
+  if (T < 0 || k < 1) return 0;
+  return align_up((size_t)T * k * sizeof(int32_t), 256);
+}
+
+MOE_API int moe_ep_combine(const void* y_sorted, const float* topk_weights, const int32_t* reverse_indices,
+                           const int32_t* offsets, int dtype, int T, int k, int H, int E, void* out, void* ws,
+                           size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc;
+  if ((rc = check_routing_dims(T, E, k))) return rc;
+  REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, "dtype must be MOE_F32 or MOE_BF16 (got %d)", dtype);
+  REQUIRE(H >= 1, "H must be >= 1 (got %d)", H);
+  const long S = (long)T * k;
+  if ((rc = check_tensor(y_sorted, S * H, "y_sorted"))) return rc;
+  if ((rc = check_tensor(topk_weights, S, "topk_weights"))) return rc;
+  if ((rc = check_tensor(reverse_indices, S, "reverse_indices"))) return rc;
+  if ((rc = check_tensor(offsets, E + 1, "offsets"))) return rc;
+  if ((rc = check_tensor(out, (long)T * H, "out"))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, (size_t)S * sizeof(int32_t)))) return rc;
+  if (S == 0) return MOE_OK;
+  return launch_ep_combine(y_sorted, topk_weights, reverse_indices, offsets, dtype, T, k, H, E, out,
+                           static_cast<int32_t*>(ws), (cudaStream_t)stream);
+}
+
 MOE_API int moe_profiler_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   g_prof_on = on != 0;

@@ -121,6 +121,15 @@ struct FfnArgs {
 // bf16 matrix [rows, cols] row-major as a TMA tensor map: box = box_rows x 64
 // columns, 128-byte swizzle, zero fill out of bounds.
 int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// x_sorted[p] = hidden[sorted_ids[p]] for p < offsets[E] (rows of row_bytes, a multiple of 16).
+int launch_gather_rows(const void* hidden, const int32_t* sorted_ids, const int32_t* offsets, int E, int row_bytes,
+                       void* xs, int32_t* status, cudaStream_t s);
+// Expert-parallel index work (expert_parallel.cu).
+size_t ep_receive_workspace_bytes(int G, int El);
+int launch_ep_receive_index(const int32_t* recv_counts, int G, int El, int32_t* counts, int32_t* offsets,
+                            int32_t* perm, void* ws, cudaStream_t s);
+int launch_ep_combine(const void* y, const float* w, const int32_t* reverse, const int32_t* offsets, int dtype,
+                      int T, int k, int H, int E, void* out, int32_t* pos, cudaStream_t s);
 // Token-count threshold at or below which the weight-streaming decode kernels run.
 constexpr int kDecodeMaxTokens = 64;
 int launch_ffn_decode(const FfnArgs& a, cudaStream_t s);

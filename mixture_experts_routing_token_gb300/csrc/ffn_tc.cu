@@ -131,6 +131,26 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+int launch_gather_rows(const void* hidden, const int32_t* sorted_ids, const int32_t* offsets, int E, int row_bytes,
+                       void* xs, int32_t* status, cudaStream_t s) {
+  if (row_bytes % 16 != 0) return fail(MOE_ERR_UNSUPPORTED, "gather_rows: rows of %d bytes (need a multiple of 16)", row_bytes);
+  ProfScope ps("gather_rows", s);
+  cudaError_t e;
+  if (row_bytes <= kBulkRowMax) {
+    if (int rc = ensure_smem_limit(gather_rows_bulk_kernel, kBulkSmem, "gather_rows")) return rc;
+    const int R = std::min(kBulkMaxR, kBulkRowMax / row_bytes);
+    e = launch_pdl(gather_rows_bulk_kernel, num_sms(), kBulkWarps * 32, (size_t)kBulkWarps * R * row_bytes, s,
+                   static_cast<const uint8_t*>(hidden), sorted_ids, offsets, E, row_bytes, R,
+                   static_cast<uint8_t*>(xs), status);
+  } else {
+    const int r16 = row_bytes / 16;
+    e = launch_pdl(gather_rows_kernel, num_sms() * 4, 256, 0, s, static_cast<const uint4*>(hidden), sorted_ids,
+                   offsets, E, r16, pow2_shift(r16), static_cast<uint4*>(xs));
+  }
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gather_rows: %s", cudaGetErrorString(e));
+  return check_launch("gather_rows");
+}
+
 // bf16 matrix [rows, cols] row-major; box = box_rows x 64 columns, 128-byte swizzle.
 int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -162,23 +182,7 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   if (a.T <= kDecodeMaxTokens) return launch_ffn_decode(a, s);
   CUtensorMap tA1, tB1, tA2, tB2, tS2;
   int rc;
-  {
-    ProfScope ps("gather_rows", s);
-    const int row_bytes = a.H * 2;
-    cudaError_t e;
-    if (row_bytes <= kBulkRowMax) {
-      if ((rc = ensure_smem_limit(gather_rows_bulk_kernel, kBulkSmem, "gather_rows"))) return rc;
-      const int R = std::min(kBulkMaxR, kBulkRowMax / row_bytes);
-      e = launch_pdl(gather_rows_bulk_kernel, num_sms(), kBulkWarps * 32, (size_t)kBulkWarps * R * row_bytes, s,
-                     static_cast<const uint8_t*>(a.hidden), a.sorted_ids, a.offsets, a.E, row_bytes, R,
-                     static_cast<uint8_t*>(a.xs), a.status);
-    } else {
-      e = launch_pdl(gather_rows_kernel, num_sms() * 4, 256, 0, s, static_cast<const uint4*>(a.hidden),
-                     a.sorted_ids, a.offsets, a.E, a.H / 8, pow2_shift(a.H / 8), static_cast<uint4*>(a.xs));
-    }
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gather_rows: %s", cudaGetErrorString(e));
-    if ((rc = check_launch("gather_rows"))) return rc;
-  }
+  if ((rc = launch_gather_rows(a.hidden, a.sorted_ids, a.offsets, a.E, a.H * 2, a.xs, a.status, s))) return rc;
   if ((rc = make_tmap(&tA1, a.xs, (uint64_t)S, (uint64_t)a.H, 128))) return rc;
   if ((rc = make_tmap(&tB1, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, 128))) return rc;
   if ((rc = make_tmap(&tA2, a.act, (uint64_t)S, (uint64_t)a.I, 128))) return rc;
