@@ -326,6 +326,20 @@ MOE_API int moe_ep_combine(const void* y_sorted, const float* topk_weights, cons
                            size_t ws_bytes, void* stream);
 
 /*
+ * Bounded waits. Every wait of the tensor-core FFN kernels (forward
+ * prefill and decode) on another role of the same kernel (a pipeline slot,
+ * an accumulator buffer) gives up after `ns` nanoseconds of GPU global time:
+ * the kernel then stops issuing work, lets the copies and MMAs it already
+ * issued finish, frees its tensor memory, ORs MOE_STATUS_TIMEOUT into the
+ * call's `status` word and returns, leaving the CUDA context usable (the
+ * call's output is then undefined). The default is 2 s; ns = 0 restores it.
+ * The value is read when a kernel is launched (a captured CUDA graph keeps
+ * the value of its capture). Returns the previous limit. The pages have no
+ * counterpart: this is the watchdog of the library's own pipelines.
+ */
+MOE_API uint64_t moe_set_wait_limit_ns(uint64_t ns);
+
+/*
  * Kernel timing.  moe_profiler_enable(1) makes every launch of this library
  * record a CUDA event pair on its stream; moe_profiler_report() synchronises
  * on those events, writes a JSON object {"kernel": {"launches": n,

@@ -15,7 +15,7 @@ from ._binding import (  # noqa: F401
     moe_grouped_ffn_backward, moe_grouped_ffn_backward_workspace_size, moe_grouped_ffn, moe_grouped_ffn_workspace_size,
     moe_indices_to_multihot, moe_layer_forward, moe_layer_workspace_size, moe_multihot_to_indices,
     moe_gather_rows, moe_ep_receive_index, moe_ep_combine,
-    profiler_enable, profiler_report, version,
+    profiler_enable, profiler_report, set_wait_limit_ns, version,
 )
 
 

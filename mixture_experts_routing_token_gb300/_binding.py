@@ -48,6 +48,7 @@ SIGNATURES = {
     "moe_ep_receive_index": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _sz, _p]),
     "moe_ep_combine_workspace_size": (_sz, [_i, _i]),
     "moe_ep_combine": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _sz, _p]),
+    "moe_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "moe_profiler_enable": (_i, [_i]),
     "moe_profiler_report": (_i, [ctypes.c_char_p, _sz]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -408,6 +409,12 @@ def moe_ep_combine(y_sorted, topk_weights, reverse_indices, offsets, out=None, w
         _ptr(y_sorted), _ptr(topk_weights), _ptr(reverse_indices), _ptr(offsets), dt, T, k, H, E, _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, d)))
     return out
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of the tensor-core FFN kernels' waits on their other roles (0: the default, 2 s);
+    returns the previous limit."""
+    return int(lib().moe_set_wait_limit_ns(int(ns)))
 
 
 def profiler_enable(on: bool = True) -> None:

@@ -3,6 +3,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -27,6 +28,13 @@ int check_launch(const char* what) {
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return MOE_OK;
 }
+
+namespace {
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 int num_sms() {
   static int cache[64] = {};
@@ -616,6 +624,10 @@ MOE_API int moe_ep_combine(const void* y_sorted, const float* topk_weights, cons
   if (S == 0) return MOE_OK;
   return launch_ep_combine(y_sorted, topk_weights, reverse_indices, offsets, dtype, T, k, H, E, out,
                            static_cast<int32_t*>(ws), (cudaStream_t)stream);
+}
+
+MOE_API uint64_t moe_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_ns.exchange(ns ? ns : kDefaultWaitNs);
 }
 
 MOE_API int moe_profiler_enable(int on) {

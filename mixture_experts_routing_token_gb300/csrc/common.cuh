@@ -17,6 +17,9 @@ namespace moe {
 int fail(int code, const char* fmt, ...);
 // Turns the last CUDA launch error into MOE_ERR_CUDA (or MOE_OK).
 int check_launch(const char* what);
+// Limit (ns of global time) of the tensor-core FFN kernels' waits on their other
+// roles; set by moe_set_wait_limit_ns, read when a kernel is launched.
+uint64_t wait_limit_ns();
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
 // Process-unique id of the CUDA context current on this thread (the device's

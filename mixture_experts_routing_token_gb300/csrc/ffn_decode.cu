@@ -43,7 +43,7 @@ constexpr int DM = 128;          // weight rows per tile (MMA M)
 constexpr int DK = 64;           // K per stage (one 128-byte swizzle row)
 constexpr int DSTAGES_MAX = 12;
 constexpr int DTHREADS = 192;
-constexpr uint64_t DWAIT_NS = 2000000000ull;
+constexpr uint64_t DWAIT_NS = 2000000000ull;   // drains (copies and MMAs already issued)
 constexpr int kLocalExperts = 64;   // local routing: a warp per token, two experts per lane (E <= 64),
 constexpr int kLocalTokens = 16;    // for at most this many tokens (more cost FC1 what the overlap gains)
 constexpr int kLocalSlots = kLocalTokens * kLocalExperts;
@@ -65,6 +65,7 @@ struct DecParams {
   int32_t* status;
   const float* logits;   // FC1 only, or null: route the tokens locally (see above)
   int norm, T, k;
+  uint64_t wait_ns;       // limit of the waits on the other roles (moe_set_wait_limit_ns)
 };
 
 template <int MODE, int NTOK>
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         const bool preloaded = t == (int)blockIdx.x && kb < pre;   // weights already requested
         int ok = 1;
         if (lane == 0 && !preloaded)
-          ok = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, DWAIT_NS);
+          ok = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, P.wait_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto producer_done;
         {
@@ -314,12 +315,12 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       int stage = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aph ^ 1u, abort_p, DWAIT_NS)) break;
+        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aph ^ 1u, abort_p, P.wait_ns)) break;
         ptx::tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(acc * C::ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, DWAIT_NS)) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, P.wait_ns)) {
             ok = false;
             break;
           }
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const DecTile d = dec_tile(t, tile_start, P.E, P.NTW);
-      if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, DWAIT_NS)) break;
+      if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, P.wait_ns)) break;
       ptx::tc_fence_after();
       const int cnt = rd(counts + d.e);
       const int valid = min(NTOK, cnt - d.chunk * NTOK);
@@ -425,10 +426,11 @@ int run_decode(const FfnArgs& a, cudaStream_t s) {
   if ((rc = make_tmap(&x2, a.act, (uint64_t)S, (uint64_t)a.I, NTOK))) return rc;
   const bool local = a.logits && a.E <= kLocalExperts && a.T <= kLocalTokens;
   DecParams p1{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.H, a.I,
-               (a.I + DM - 1) / DM, 2 * a.I, a.act, a.status, local ? a.logits : nullptr, a.norm, a.T, a.k};
+               (a.I + DM - 1) / DM, 2 * a.I, a.act, a.status, local ? a.logits : nullptr, a.norm, a.T, a.k,
+               wait_limit_ns()};
   if ((rc = launch_dec<DEC_FC1, NTOK>(w1, x1, p1, S, s, "ffn_fc1_decode"))) return rc;
   DecParams p2{a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse, a.E, a.I, a.H,
-               (a.H + DM - 1) / DM, a.H, a.staging, a.status, nullptr, 0, a.T, a.k};
+               (a.H + DM - 1) / DM, a.H, a.staging, a.status, nullptr, 0, a.T, a.k, wait_limit_ns()};
   if ((rc = launch_dec<DEC_FC2, NTOK>(w2, x2, p2, S, s, "ffn_fc2_decode"))) return rc;
   return launch_combine(a.staging, 0, a.T, a.k, a.H, a.dtype, a.out, s);
 }

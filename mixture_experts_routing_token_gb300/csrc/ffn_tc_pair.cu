@@ -56,7 +56,7 @@ constexpr int PSTAGE = PA_BYTES + PB_BYTES;
 constexpr int PDSMEM = PSTAGES * PSTAGE + 1024;
 constexpr int PTHREADS = 192;
 constexpr uint32_t PTMEM_COLS = 2 * PBN;
-constexpr uint64_t PWAIT_NS = 2000000000ull;
+constexpr uint64_t PWAIT_NS = 2000000000ull;   // the drain of issued MMAs
 constexpr uint32_t PIDESC = ptx::idesc_bf16_f32(2 * PBM, PBN);
 constexpr int kSwapMax = 128;           // FC2 remainders up to this many rows take a swapped tile
 constexpr int kSwapBox = 32;            // token rows per TMA box of a swapped tile's B operand
@@ -76,6 +76,7 @@ struct PairParams {
   int b_rows;     // 2I (FC1) or H (FC2)
   void* out;
   int32_t* status;
+  uint64_t wait_ns;   // limit of the waits on the other roles (moe_set_wait_limit_ns)
 };
 
 struct PTile {
@@ -226,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           const int tok_row = __ldg(P.offsets + ti.e) + ti.m_tile * (2 * PBM) + (int)rank * half;
           const int w_row = ti.e * P.b_rows + ti.n_tile * (2 * PBM) + (int)rank * PBM;
           for (int kb = 0; kb < KB; ++kb) {
-            if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, PWAIT_NS)) goto producer_done;
+            if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, P.wait_ns)) goto producer_done;
             const uint32_t fb_local = ptx::smem_u32(&full_bar[stage]);
             if (leader) ptx::mbar_arrive_expect_tx(fb_local, 2 * (PA_BYTES + half * PBK * 2));
             const uint32_t fb = map_to_rank(fb_local, 0);
@@ -242,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         if (MODE == PAIR_FC1) b_row = ti.e * P.b_rows + ti.n_tile * 128 + (leader ? 0 : P.N_out);
         else b_row = ti.e * P.b_rows + ti.n_tile * PBN + (int)rank * 128;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, PWAIT_NS)) goto producer_done;
+          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), ph ^ 1u, abort_p, P.wait_ns)) goto producer_done;
           const uint32_t fb_local = ptx::smem_u32(&full_bar[stage]);
           if (leader) ptx::mbar_arrive_expect_tx(fb_local, 2 * PSTAGE);
           const uint32_t fb = map_to_rank(fb_local, 0);
@@ -261,12 +262,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       for (int t = cluster_id; t < total; t += nclusters) {
         const PTile ti = ptile(t, tile_start, P.counts, P.E, P.NT, P.NTs);
         const uint32_t idesc = ti.swap_n ? ptx::idesc_bf16_f32(2 * PBM, ti.swap_n) : PIDESC;
-        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aph ^ 1u, abort_p, PWAIT_NS)) break;
+        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aph ^ 1u, abort_p, P.wait_ns)) break;
         ptx::tc_fence_after();
         bool ok = true;
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, PWAIT_NS)) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), ph, abort_p, P.wait_ns)) {
             ok = false;
             break;
           }
@@ -295,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     uint32_t aph = 0;
     for (int t = cluster_id; t < total; t += nclusters) {
       const PTile ti = ptile(t, tile_start, P.counts, P.E, P.NT, P.NTs);
-      if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, PWAIT_NS)) break;
+      if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, P.wait_ns)) break;
       ptx::tc_fence_after();
       const int cnt = __ldg(P.counts + ti.e);
       if (MODE == PAIR_FC2 && ti.swap_n) {
@@ -425,11 +426,11 @@ int launch_ffn_pair_gemms(const FfnArgs& a, const CUtensorMap& tA1, const CUtens
                           cudaStream_t s) {
   const long S = (long)a.T * a.k;
   PairParams p1{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.H, a.I, (a.I + 127) / 128, 0,
-                2 * a.I, a.act, a.status};
+                2 * a.I, a.act, a.status, wait_limit_ns()};
   int rc = launch_pair<PAIR_FC1>(tA1, tB1, tA1, p1, S, s, "ffn_fc1_tc");   // (no swapped tiles: tmS unused)
   if (rc) return rc;
   PairParams p2{a.counts, a.offsets, a.sorted_w, a.reverse, a.E, a.I, a.H, (a.H + PBN - 1) / PBN,
-                (a.H + 2 * PBM - 1) / (2 * PBM), a.H, a.staging, a.status};
+                (a.H + 2 * PBM - 1) / (2 * PBM), a.H, a.staging, a.status, wait_limit_ns()};
   return launch_pair<PAIR_FC2>(tA2, tB2, tS2, p2, S, s, "ffn_fc2_tc");
 }
 

@@ -51,11 +51,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are polled without suspending and checked at every poll
+// (a try_wait may suspend the thread until the phase completes).
+constexpr uint64_t kShortWaitNs = 1000;
+
 // Bounded wait for the phase of parity `parity` to complete. Gives up after
 // `limit_ns` of global time or as soon as *abort is set by another thread;
 // on giving up it sets *abort and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
+  if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (globaltimer() - t0 >= limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
