@@ -58,7 +58,7 @@ __device__ __forceinline__ unsigned same_expert_lanes(int e, int bits) {
 
 // Dynamic shared memory of align_chunk for E experts.
 __host__ __device__ inline size_t align_smem_bytes(int E) {
-  return (size_t)(3 * E + 2 + kWarps * E + 3 * kChunk) * sizeof(int);
+  return (size_t)(3 * E + 2 + kWarps * E + 4 * kChunk) * sizeof(int);
 }
 
 __global__ void __launch_bounds__(kThreads) align_hist_kernel(const int32_t* __restrict__ idx,
@@ -153,12 +153,13 @@ __device__ __forceinline__ int warp0_exclusive_scan(int* v, int n) {
 
 // Align chunk c of the slots (all kThreads threads of the CTA take part).
 // Shared layout (ints): off[E+1] | cb[E] | cpre[E+1] | wcnt[kWarps][E]
-//                       | staged token ids, slots, weights [kChunk] each.
+//                       | staged token ids, slots, weights, destinations [kChunk] each.
 // cb[e] is the number of expert e's slots in earlier chunks, cpre[e] the
 // chunk-local start of e's slots, wcnt[w][e] warp w's count of e, then the
 // number of e's slots in the chunk's warps before w. Slots are ranked into the
-// staging arrays in expert-sorted order, then each expert's run is copied to
-// its global positions by consecutive threads (coalesced stores).
+// staging arrays in expert-sorted order together with their global position,
+// then copied out by consecutive threads (each expert's run is contiguous in
+// both orders: coalesced stores). Slot indices are 32-bit (T*k < 2^31).
 template <int SRC>
 __device__ __forceinline__ void align_chunk(
     int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
@@ -172,19 +173,21 @@ __device__ __forceinline__ void align_chunk(
   int* s_tok = wcnt + kWarps * E;
   int* s_rev = s_tok + kChunk;
   float* s_w = reinterpret_cast<float*>(s_rev + kChunk);
-  const long lo = (long)c * kChunk;
-  const long hi = min(S, lo + kChunk);
+  int* s_dst = s_rev + 2 * kChunk;
+  const int lo = c * kChunk;
+  const int hi = (int)min(S, (long)lo + kChunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // token of slot s: s >> kshift or s / k
 
   // 0. this warp's slots (step 3), loaded first so that their latency overlaps steps 1-2;
   //    the barriers of steps 1-2 also order the zeroing of wcnt before step 3
   for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
-  const long wbase = lo + (long)warp * 32 * kSub;
+  const int wbase = lo + warp * 32 * kSub;
   int eu[kSub], ru[kSub];
   float wu[kSub];
 #pragma unroll
   for (int u = 0; u < kSub; ++u) {
-    const long s = wbase + u * 32 + lane;
+    const int s = wbase + u * 32 + lane;
     eu[u] = s < hi ? load_i<SRC>(idx + s) : -1;
     wu[u] = s < hi ? load_f<SRC>(wts + s) : 0.0f;
   }
@@ -215,7 +218,7 @@ __device__ __forceinline__ void align_chunk(
     for (int e = tid; e < E; e += kThreads) { cb[e] = 0; off[e] = 0; }
     __syncthreads();
     bool bad = false;
-    for (long s = lo + tid; s < hi; s += kThreads) {
+    for (int s = lo + tid; s < hi; s += kThreads) {
       const int e = load_i<SRC>(idx + s);
       if (e >= 0 && e < E) atomicAdd(&off[e], 1);
       else bad = true;
@@ -277,24 +280,21 @@ __device__ __forceinline__ void align_chunk(
   for (int u = 0; u < kSub; ++u) {
     const int e = eu[u];
     if (e >= 0) {
-      const long s = wbase + u * 32 + lane;
-      const int q = cpre[e] + wcnt[warp * E + e] + ru[u];   // chunk-local, expert-sorted
-      s_tok[q] = s <= 0x7fffffffL ? (int)((uint32_t)s / (uint32_t)k) : (int)(s / k);
-      s_rev[q] = (int)s;
+      const int s = wbase + u * 32 + lane;
+      const int base = cpre[e];
+      const int q = base + wcnt[warp * E + e] + ru[u];   // chunk-local, expert-sorted
+      s_tok[q] = kshift >= 0 ? s >> kshift : (int)((uint32_t)s / (uint32_t)k);
+      s_rev[q] = s;
       s_w[q] = wu[u];
+      s_dst[q] = off[e] + cb[e] + (q - base);
     }
   }
   __syncthreads();
 
-  // 4. copy each expert's run of the chunk to its global positions (coalesced)
+  // 4. copy the staged slots to their global positions (coalesced within each expert's run)
   const int n = cpre[E];
   for (int q = tid; q < n; q += kThreads) {
-    int lo_e = 0, hi_e = E - 1;               // expert e with cpre[e] <= q < cpre[e + 1]
-    while (lo_e < hi_e) {
-      const int mid = (lo_e + hi_e + 1) >> 1;
-      if (cpre[mid] <= q) lo_e = mid; else hi_e = mid - 1;
-    }
-    const int p = off[lo_e] + cb[lo_e] + (q - cpre[lo_e]);
+    const int p = s_dst[q];
     sorted_ids[p] = s_tok[q];
     reverse[p] = s_rev[q];
     sorted_w[p] = s_w[q];
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
   extern __shared__ int sm[];
   pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
   float* col = reinterpret_cast<float*>(sm);
-  int* asm_ = sm + EP * gate::kStageLd;                       // align_chunk's shared memory
+  int* asm_ = sm + gate::stage_floats<EP>();                  // align_chunk's shared memory
   int32_t* s_idx = asm_ + align_smem_bytes(E) / sizeof(int);  // shared copies of the routing
   float* s_w = reinterpret_cast<float*>(s_idx + T * k);
   gate::stage_rows<EP>(logits, 0, T, E, col, threadIdx.x, kThreads);
@@ -368,7 +368,7 @@ template <int EP>
 int launch_route_staged(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
                         int32_t* reverse, int32_t* status, cudaStream_t s) {
-  const size_t stage = (size_t)EP * gate::kStageLd * sizeof(float);
+  const size_t stage = (size_t)gate::stage_floats<EP>() * sizeof(float);
   const size_t copies = (size_t)T * k * (sizeof(int32_t) + sizeof(float));
   return launch_route_small_k(route_small_staged_kernel<EP>, stage + align_smem_bytes(E) + copies,
                               stage + align_smem_bytes(EP) + (size_t)kChunk * 8, logits, T, E, k, norm, w, idx,

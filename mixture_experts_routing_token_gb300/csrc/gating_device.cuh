@@ -216,111 +216,129 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
 //
 // A block of up to kStageRows rows is stored column-major, element e of row r at
 // col[e * kStageLd + r] (padded stride: every access below is bank-conflict
-// free). The thread of row r keeps the maxima of its groups of 8 experts in
-// registers; each of the k rounds scans the group maxima, takes the winner
-// (value desc, then index asc: scans run in ascending index with strict >),
-// marks it taken (-inf; logits are finite) and rescans only the winner's group.
+// free); the thread of row r selects with the tournament of topk_staged_row.
 // Weights as in gate_one_token.
 constexpr int kStageRows = 128;
 constexpr int kStageLd = kStageRows + 1;
 
 // Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into col[EP][kStageLd],
 // experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows); the
-// caller synchronises before reading. Each thread issues kStageBatch vector
-// loads before it stores any of them, so a block has that many loads per
-// thread in flight instead of one.
-constexpr int kStageBatch = 8;
+// caller synchronises before reading. Each thread issues U 16-byte loads before
+// it stores any of them; with U = the vectors per thread of a full stage
+// (kStageBatch<EP, In>(nthr)), a whole stage is one round trip to memory.
+template <int EP, typename In>
+__host__ __device__ constexpr int kStageBatch(int nthr) {
+  const int per = EP * kStageRows / (16 / (int)sizeof(In)) / nthr;
+  return per < 1 ? 1 : (per > 32 ? 32 : per);
+}
 
-template <int EP, typename In = float>
+// Widen one 16-byte vector of logits (4 float32 or 8 bf16) into row r, experts e0.., of the stage.
+__device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, float) {
+  col[e0 * kStageLd + r] = __uint_as_float(q.x);
+  col[(e0 + 1) * kStageLd + r] = __uint_as_float(q.y);
+  col[(e0 + 2) * kStageLd + r] = __uint_as_float(q.z);
+  col[(e0 + 3) * kStageLd + r] = __uint_as_float(q.w);
+}
+__device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, __nv_bfloat16) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    col[(e0 + 2 * i) * kStageLd + r] = lo_bf16(w[i]);
+    col[(e0 + 2 * i + 1) * kStageLd + r] = hi_bf16(w[i]);
+  }
+}
+
+template <int EP, typename In = float, int U = 8>
 __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t0, int nt, int E,
                                            float* col, int tid, int nthr) {
+  constexpr int VEC = 16 / (int)sizeof(In);   // logits per 16-byte vector
   const In* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
-  constexpr int U = kStageBatch;
-  if constexpr (!std::is_same<In, float>::value) {
-    if ((E & 7) == 0) {
-      const int n8 = nt * E / 8;
-      const uint4* src = reinterpret_cast<const uint4*>(blk);
-      for (int f0 = tid; f0 < n8; f0 += U * nthr) {
+  if (E % VEC == 0) {
+    const int R = E / VEC;                   // vectors per row
+    const uint4* src = reinterpret_cast<const uint4*>(blk);
+    if (nthr % R == 0) {
+      // every vector of this thread is column c of a row: no division per vector
+      const int c = tid % R, e0 = c * VEC, dr = nthr / R;
+      for (int r0 = tid / R; r0 < nt; r0 += U * dr) {
         uint4 q[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (f0 + u * nthr < n8) q[u] = __ldg(src + f0 + u * nthr);
+          if (r0 + u * dr < nt) q[u] = __ldg(src + (r0 + u * dr) * R + c);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (r0 + u * dr < nt) put_vec(col, e0, r0 + u * dr, q[u], In());
+      }
+    } else {
+      const int n = nt * R;
+      for (int f0 = tid; f0 < n; f0 += U * nthr) {
+        uint4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (f0 + u * nthr < n) q[u] = __ldg(src + f0 + u * nthr);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int f = f0 + u * nthr;
-          if (f < n8) {
-            const int tl = (int)((uint32_t)(8 * f) / (uint32_t)E), e0 = 8 * f - tl * E;
-            const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              col[(e0 + 2 * i) * kStageLd + tl] = lo_bf16(w[i]);
-              col[(e0 + 2 * i + 1) * kStageLd + tl] = hi_bf16(w[i]);
-            }
+          if (f < n) {
+            const int r = (int)((uint32_t)f / (uint32_t)R);
+            put_vec(col, (f - r * R) * VEC, r, q[u], In());
           }
-        }
-      }
-    } else {
-      for (int f = tid; f < nt * E; f += nthr) {
-        const int tl = f / E;
-        col[(f - tl * E) * kStageLd + tl] = load_logit(blk + f);
-      }
-    }
-  } else if ((E & 3) == 0) {
-    const int n4 = nt * E / 4;
-    const float4* src = reinterpret_cast<const float4*>(blk);
-    for (int f0 = tid; f0 < n4; f0 += U * nthr) {
-      float4 q[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (f0 + u * nthr < n4) q[u] = __ldg(src + f0 + u * nthr);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int f = f0 + u * nthr;
-        if (f < n4) {
-          const int tl = (int)((uint32_t)(4 * f) / (uint32_t)E), e0 = 4 * f - tl * E;
-          col[e0 * kStageLd + tl] = q[u].x;
-          col[(e0 + 1) * kStageLd + tl] = q[u].y;
-          col[(e0 + 2) * kStageLd + tl] = q[u].z;
-          col[(e0 + 3) * kStageLd + tl] = q[u].w;
         }
       }
     }
   } else {
     for (int f = tid; f < nt * E; f += nthr) {
-      const int tl = f / E;
-      col[(f - tl * E) * kStageLd + tl] = __ldg(blk + f);
+      const int r = f / E;
+      col[(f - r * E) * kStageLd + r] = load_logit(blk + f);
     }
   }
   if (tid < kStageRows)
     for (int e = E; e < EP; ++e) col[e * kStageLd + tid] = -INFINITY;
 }
 
+// Shared memory (floats) of a stage of kStageRows rows padded to EP experts:
+// the rows [EP][kStageLd], then the maxima of their groups of 8 [EP / 8][kStageLd].
+template <int EP>
+__host__ __device__ constexpr int stage_floats() { return (EP + EP / 8) * kStageLd; }
+
 // Top-k and softmax of staged row r (called by one thread), written as token t. With
 // s_w / s_idx (shared memory, indexed like the outputs) the results are also kept
-// there, and the finishing pass reads the raw logits back from s_w instead of w_out.
-template <int EP>
+// there.
+//
+// Selection is a two-level tournament over groups of 8 experts: the group maxima
+// live in shared memory after the rows, the maxima of 4 consecutive groups
+// ("supers") in registers. A round takes the largest super, then its first group
+// holding that value, then the group's first expert holding it (scans in
+// ascending index, so equal values go to the lower expert, as the page's strict
+// '>' does), marks that expert taken (-inf; logits are finite) and refreshes its
+// group's and super's maxima. Every choice is a select, not a branch: all threads
+// of a warp run the same instructions.
+//
+// TO_COL (k <= kRegSel, EP >= 2 kRegSel): instead of w_out / idx_out, the results go
+// to the row's own column: weight j to col[j], index j (bits) to col[kRegSel + j].
+template <int EP, bool TO_COL = false>
 __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E, int k, int norm,
                                                 float* __restrict__ w_out, int32_t* __restrict__ idx_out,
                                                 float* s_w = nullptr, int32_t* s_idx = nullptr) {
-  constexpr int G = EP / 8;
+  static_assert(!TO_COL || EP >= 2 * kRegSel, "the parked results need 2 kRegSel slots");
+  constexpr int G = EP / 8;          // groups of 8 experts
+  constexpr int S = (G + 3) / 4;     // supers of 4 groups
+  float* gcol = col + EP * kStageLd;
   auto at = [&](int i) -> float& { return col[i * kStageLd + r]; };
-  float gv[G];
-  int gi[G];
+  auto gat = [&](int g) -> float& { return gcol[g * kStageLd + r]; };
+  float sm[S];
+#pragma unroll
+  for (int q = 0; q < S; ++q) sm[q] = -INFINITY;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float bv = at(8 * g);
-    int bi = 8 * g;
+    float x = at(8 * g);
 #pragma unroll
-    for (int c = 1; c < 8; ++c) {
-      const float x = at(8 * g + c);
-      if (x > bv) { bv = x; bi = 8 * g + c; }
-    }
-    gv[g] = bv;
-    gi[g] = bi;
+    for (int c = 1; c < 8; ++c) x = fmaxf(x, at(8 * g + c));
+    gat(g) = x;
+    sm[g / 4] = fmaxf(sm[g / 4], x);
   }
-  float m = gv[0];
+  float m = sm[0];
 #pragma unroll
-  for (int g = 1; g < G; ++g) m = fmaxf(m, gv[g]);
+  for (int q = 1; q < S; ++q) m = fmaxf(m, sm[q]);
   float hi = 0.0f, lo = 0.0f;
   if (!norm) {   // four independent compensated sums (a quarter of the dependent chain), then merged
     float h[4] = {0.0f, 0.0f, 0.0f, 0.0f}, l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -336,41 +354,64 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
       lo += l[a];
     }
   }
-  // one round: the best remaining (value, expert); its group is rescanned
-  auto take = [&](float& bv, int& bi) {
-    bv = gv[0];
-    bi = gi[0];
-    int bg = 0;
+  // one round: the largest remaining value and its lowest expert; refreshes the maxima
+  auto take = [&](float& v, int& e) {
+    v = sm[0];
 #pragma unroll
-    for (int g = 1; g < G; ++g)
-      if (gv[g] > bv) { bv = gv[g]; bi = gi[g]; bg = g; }
-    at(bi) = -INFINITY;
-    float nv = at(8 * bg);
-    int ni = 8 * bg;
+    for (int q = 1; q < S; ++q) v = fmaxf(v, sm[q]);
+    int bs = 0;
 #pragma unroll
-    for (int c = 1; c < 8; ++c) {
-      const float x = at(8 * bg + c);
-      if (x > nv) { nv = x; ni = 8 * bg + c; }
-    }
+    for (int q = S - 1; q >= 0; --q) bs = sm[q] == v ? q : bs;
+    float gv[4];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (g == bg) { gv[g] = nv; gi[g] = ni; }
+    for (int i = 0; i < 4; ++i) gv[i] = (G % 4 == 0 || 4 * bs + i < G) ? gat(4 * bs + i) : -INFINITY;
+    int bi = 0;
+#pragma unroll
+    for (int i = 3; i >= 0; --i) bi = gv[i] == v ? i : bi;
+    const int bg = 4 * bs + bi;
+    float x[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = at(8 * bg + c);
+    int bc = 0;
+#pragma unroll
+    for (int c = 7; c >= 0; --c) bc = x[c] == v ? c : bc;
+    e = 8 * bg + bc;
+    at(e) = -INFINITY;
+    float nm = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) nm = fmaxf(nm, c == bc ? -INFINITY : x[c]);
+    gat(bg) = nm;
+    float ns = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ns = fmaxf(ns, i == bi ? nm : gv[i]);
+#pragma unroll
+    for (int q = 0; q < S; ++q) sm[q] = q == bs ? ns : sm[q];
   };
-  if (!s_w && k <= kRegSel) {   // the selected logits stay in registers until the weights are formed
+  if (TO_COL || k <= kRegSel) {   // the selected logits stay in registers until the weights are formed
     float sel[kRegSel];
+    int sid[kRegSel];
 #pragma unroll
     for (int j = 0; j < kRegSel; ++j) {
       if (j < k) {
-        int bi;
-        take(sel[j], bi);
+        take(sel[j], sid[j]);
         if (norm) two_sum_add(hi, lo, exp_diff(sel[j], m));
-        idx_out[t * k + j] = bi;
       }
     }
     const float denom = hi + lo;
 #pragma unroll
     for (int j = 0; j < kRegSel; ++j)
-      if (j < k) w_out[t * k + j] = __fdiv_rn(exp_diff(sel[j], m), denom);
+      if (j < k) {
+        const float wj = __fdiv_rn(exp_diff(sel[j], m), denom);
+        if (TO_COL) {
+          at(j) = wj;
+          at(kRegSel + j) = __int_as_float(sid[j]);
+        } else {
+          w_out[t * k + j] = wj;
+          idx_out[t * k + j] = sid[j];
+          if (s_w) s_w[t * k + j] = wj;
+          if (s_idx) s_idx[t * k + j] = sid[j];
+        }
+      }
     return;
   }
   for (int j = 0; j < k; ++j) {

@@ -36,23 +36,37 @@ __global__ void __launch_bounds__(kBlock) gating_kernel(const In* __restrict__ l
 // shared memory and runs gate::topk_staged_row on them (gating_device.cuh).
 constexpr int kSmemGateThreads = gate::kStageRows;
 
-template <int EP, typename In>
+template <int EP, typename In, int U = 8>
 __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
     const In* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
     int32_t* __restrict__ idx_out) {
-  extern __shared__ float col[];                   // [EP][kStageLd]
+  extern __shared__ float col[];                   // gate::stage_floats<EP>()
   const int tid = threadIdx.x;
   const long t0 = (long)blockIdx.x * kSmemGateThreads;
   const int nt = (int)min((long)kSmemGateThreads, (long)T - t0);
-  gate::stage_rows<EP, In>(logits, t0, nt, E, col, tid, kSmemGateThreads);
+  gate::stage_rows<EP, In, U>(logits, t0, nt, E, col, tid, kSmemGateThreads);
   __syncthreads();
-  if (tid < nt) gate::topk_staged_row<EP>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
+  if (k > gate::kRegSel) {
+    if (tid < nt) gate::topk_staged_row<EP>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
+    return;
+  }
+  // Each thread touches only its own row's column, so it parks its k weights and
+  // indices there (slots 0..k-1 and kRegSel..kRegSel+k-1); after the barrier the
+  // block writes its rows' outputs out contiguously.
+  if (tid < nt) gate::topk_staged_row<EP, true>(col, tid, tid, E, k, norm, nullptr, nullptr);
+  __syncthreads();
+  const int n = nt * k;
+  for (int f = tid; f < n; f += kSmemGateThreads) {
+    const int r = (int)((uint32_t)f / (uint32_t)k), j = f - r * k;
+    w_out[t0 * k + f] = col[j * gate::kStageLd + r];
+    idx_out[t0 * k + f] = __float_as_int(col[(gate::kRegSel + j) * gate::kStageLd + r]);
+  }
 }
 
 template <int EP, typename In>
 int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
-  const size_t smem = (size_t)EP * gate::kStageLd * sizeof(float);
+  const size_t smem = (size_t)gate::stage_floats<EP>() * sizeof(float);
   if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
   gating_smem_kernel<EP, In><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
       logits, T, E, k, norm, w, idx);
@@ -522,8 +536,8 @@ __global__ void __launch_bounds__(kSmemGroupThreads) group_topk_smem_kernel(
   const long t0 = (long)blockIdx.x * kSmemGroupThreads;
   const int nt = (int)min((long)kSmemGroupThreads, (long)T - t0);
   const float* blk = scores + t0 * (long)E;
-  if ((E & 3) == 0) {   // kStageBatch loads in flight per thread, then their stores
-    constexpr int U = gate::kStageBatch;
+  if ((E & 3) == 0) {   // U loads in flight per thread, then their stores
+    constexpr int U = 8;
     const int n4 = nt * E / 4;
     const float4* src = reinterpret_cast<const float4*>(blk);
     for (int f0 = tid; f0 < n4; f0 += U * kSmemGroupThreads) {
