@@ -145,13 +145,42 @@ ProfScope::~ProfScope() {
 
 namespace {
 
+// Device-memory check of a tensor argument. The allocation ranges already seen
+// to be device (or managed) memory are remembered, so the driver is asked once
+// per allocation rather than once per argument of every call. Device virtual
+// addresses are never handed out as host memory, so a remembered range stays
+// device memory (possibly another allocation) for the life of the process.
+typedef CUresult (*MemGetAddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
+struct DevRange {
+  uintptr_t lo, hi;
+};
+std::mutex g_range_mu;
+DevRange g_ranges[64];
+int g_nranges = 0, g_next_range = 0;
+
 bool is_device_ptr(const void* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  {
+    std::lock_guard<std::mutex> lk(g_range_mu);
+    for (int i = 0; i < g_nranges; ++i)
+      if (a >= g_ranges[i].lo && a < g_ranges[i].hi) return true;
+  }
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return false;
+  static MemGetAddressRangeFn range_fn = driver_fn<MemGetAddressRangeFn>("cuMemGetAddressRange");
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (range_fn && range_fn(&base, &size, (CUdeviceptr)a) == CUDA_SUCCESS && size > 0) {
+    std::lock_guard<std::mutex> lk(g_range_mu);
+    g_ranges[g_next_range] = DevRange{(uintptr_t)base, (uintptr_t)base + size};
+    g_next_range = (g_next_range + 1) % 64;
+    if (g_nranges < 64) ++g_nranges;
+  }
+  return true;
 }
 
 #define REQUIRE(cond, ...)                                   \

@@ -59,6 +59,19 @@ __device__ __forceinline__ float exp_diff(float a, float b) {
   return fmaf(e, err, e);
 }
 
+// exp_diff with the fast exponential (CUDA's __expf: at most 2 + floor(1.173 |x|)
+// ulp). For the terms of the full-row softmax denominator, all at x = a - b <= 0:
+// a term's error grows with |x| but its weight falls as e^x, so the sum's relative
+// error stays near that of the largest terms (|x| < 1: <= 3 ulp, 1.8e-7); the k
+// selected numerators keep exp_diff.
+__device__ __forceinline__ float exp_diff_fast(float a, float b) {
+  const float s = a - b;
+  const float bb = s - a;
+  const float err = (a - (s - bb)) + (-b - bb);
+  const float e = __expf(s);
+  return fmaf(e, err, e);
+}
+
 // Order-preserving map of a finite float to an unsigned key (larger float ->
 // larger key; -0 and +0 share a key; 0 is below every finite float's key).
 __device__ __forceinline__ unsigned okey(float x) {
@@ -232,7 +245,15 @@ __host__ __device__ constexpr int kStageBatch(int nthr) {
   return per < 1 ? 1 : (per > 32 ? 32 : per);
 }
 
-// Widen one 16-byte vector of logits (4 float32 or 8 bf16) into row r, experts e0.., of the stage.
+// Staged logits are kept as float32, or for bf16 logits as their 16-bit
+// patterns (half the shared memory per row, so more rows fit per SM); either
+// way a value read back is the exact float32 of the logit.
+__device__ __forceinline__ float st_get(const float* p) { return *p; }
+__device__ __forceinline__ float st_get(const uint16_t* p) { return __uint_as_float((uint32_t)*p << 16); }
+__device__ __forceinline__ void st_neg_inf(float* p) { *p = -INFINITY; }
+__device__ __forceinline__ void st_neg_inf(uint16_t* p) { *p = 0xff80u; }   // bf16 -inf
+
+// One 16-byte vector of logits (4 float32 or 8 bf16) into row r, experts e0.., of the stage.
 __device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, float) {
   col[e0 * kStageLd + r] = __uint_as_float(q.x);
   col[(e0 + 1) * kStageLd + r] = __uint_as_float(q.y);
@@ -247,10 +268,23 @@ __device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& 
     col[(e0 + 2 * i + 1) * kStageLd + r] = hi_bf16(w[i]);
   }
 }
+__device__ __forceinline__ void put_vec(uint16_t* col, int e0, int r, const uint4& q, __nv_bfloat16) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    col[(e0 + 2 * i) * kStageLd + r] = (uint16_t)(w[i] & 0xffffu);
+    col[(e0 + 2 * i + 1) * kStageLd + r] = (uint16_t)(w[i] >> 16);
+  }
+}
+__device__ __forceinline__ void put_one(float* p, const float* src) { *p = __ldg(src); }
+__device__ __forceinline__ void put_one(float* p, const __nv_bfloat16* src) { *p = load_logit(src); }
+__device__ __forceinline__ void put_one(uint16_t* p, const __nv_bfloat16* src) {
+  *p = __ldg(reinterpret_cast<const unsigned short*>(src));
+}
 
-template <int EP, typename In = float, int U = 8>
+template <int EP, typename In = float, int U = 8, typename St = float>
 __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t0, int nt, int E,
-                                           float* col, int tid, int nthr) {
+                                           St* col, int tid, int nthr) {
   constexpr int VEC = 16 / (int)sizeof(In);   // logits per 16-byte vector
   const In* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
   if (E % VEC == 0) {
@@ -288,17 +322,22 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
   } else {
     for (int f = tid; f < nt * E; f += nthr) {
       const int r = f / E;
-      col[(f - r * E) * kStageLd + r] = load_logit(blk + f);
+      put_one(col + (f - r * E) * kStageLd + r, blk + f);
     }
   }
   if (tid < kStageRows)
-    for (int e = E; e < EP; ++e) col[e * kStageLd + tid] = -INFINITY;
+    for (int e = E; e < EP; ++e) st_neg_inf(col + e * kStageLd + tid);
 }
 
-// Shared memory (floats) of a stage of kStageRows rows padded to EP experts:
-// the rows [EP][kStageLd], then the maxima of their groups of 8 [EP / 8][kStageLd].
+// Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: the
+// rows [EP][kStageLd] of St, then (4-byte aligned) the float maxima of their
+// groups of 8 [EP / 8][kStageLd].
+template <int EP, typename St = float>
+__host__ __device__ constexpr int stage_rows_bytes() { return (EP * kStageLd * (int)sizeof(St) + 3) / 4 * 4; }
+template <int EP, typename St = float>
+__host__ __device__ constexpr int stage_bytes() { return stage_rows_bytes<EP, St>() + EP / 8 * kStageLd * 4; }
 template <int EP>
-__host__ __device__ constexpr int stage_floats() { return (EP + EP / 8) * kStageLd; }
+__host__ __device__ constexpr int stage_floats() { return stage_bytes<EP, float>() / 4; }
 
 // Top-k and softmax of staged row r (called by one thread), written as token t. With
 // s_w / s_idx (shared memory, indexed like the outputs) the results are also kept
@@ -313,18 +352,29 @@ __host__ __device__ constexpr int stage_floats() { return (EP + EP / 8) * kStage
 // group's and super's maxima. Every choice is a select, not a branch: all threads
 // of a warp run the same instructions.
 //
-// TO_COL (k <= kRegSel, EP >= 2 kRegSel): instead of w_out / idx_out, the results go
-// to the row's own column: weight j to col[j], index j (bits) to col[kRegSel + j].
-template <int EP, bool TO_COL = false>
-__device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E, int k, int norm,
+// TO_COL (k <= kRegSel): instead of w_out / idx_out, the results go to the row's
+// own column: weight j and index j (bits) to slots j and kRegSel + j of a float
+// column, or as 16-bit halves to slots 2j, 2j+1 and 2 kRegSel + 2j, +1 of a
+// 16-bit column.
+template <int EP, bool TO_COL = false, typename St = float>
+__device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, int k, int norm,
                                                 float* __restrict__ w_out, int32_t* __restrict__ idx_out,
                                                 float* s_w = nullptr, int32_t* s_idx = nullptr) {
-  static_assert(!TO_COL || EP >= 2 * kRegSel, "the parked results need 2 kRegSel slots");
+  constexpr bool kHalf = sizeof(St) == 2;
+  static_assert(!TO_COL || EP >= (kHalf ? 4 : 2) * kRegSel, "room for the parked results");
   constexpr int G = EP / 8;          // groups of 8 experts
   constexpr int S = (G + 3) / 4;     // supers of 4 groups
-  float* gcol = col + EP * kStageLd;
-  auto at = [&](int i) -> float& { return col[i * kStageLd + r]; };
+  float* gcol = reinterpret_cast<float*>(reinterpret_cast<char*>(col) + stage_rows_bytes<EP, St>());
+  auto at = [&](int i) -> float { return st_get(col + i * kStageLd + r); };
   auto gat = [&](int g) -> float& { return gcol[g * kStageLd + r]; };
+  auto put32 = [&](int slot, uint32_t v) {   // a 32-bit result into parking slot `slot`
+    if constexpr (kHalf) {
+      col[(2 * slot) * kStageLd + r] = (St)(v & 0xffffu);
+      col[(2 * slot + 1) * kStageLd + r] = (St)(v >> 16);
+    } else {
+      col[slot * kStageLd + r] = __uint_as_float(v);
+    }
+  };
   float sm[S];
 #pragma unroll
   for (int q = 0; q < S; ++q) sm[q] = -INFINITY;
@@ -345,9 +395,9 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
     int i = 0;
     for (; i + 4 <= E; i += 4) {
 #pragma unroll
-      for (int a = 0; a < 4; ++a) two_sum_add(h[a], l[a], exp_diff(at(i + a), m));
+      for (int a = 0; a < 4; ++a) two_sum_add(h[a], l[a], exp_diff_fast(at(i + a), m));
     }
-    for (; i < E; ++i) two_sum_add(h[0], l[0], exp_diff(at(i), m));
+    for (; i < E; ++i) two_sum_add(h[0], l[0], exp_diff_fast(at(i), m));
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       two_sum_add(hi, lo, h[a]);
@@ -376,7 +426,7 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
 #pragma unroll
     for (int c = 7; c >= 0; --c) bc = x[c] == v ? c : bc;
     e = 8 * bg + bc;
-    at(e) = -INFINITY;
+    st_neg_inf(col + e * kStageLd + r);
     float nm = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 8; ++c) nm = fmaxf(nm, c == bc ? -INFINITY : x[c]);
@@ -403,8 +453,8 @@ __device__ __forceinline__ void topk_staged_row(float* col, int r, long t, int E
       if (j < k) {
         const float wj = __fdiv_rn(exp_diff(sel[j], m), denom);
         if (TO_COL) {
-          at(j) = wj;
-          at(kRegSel + j) = __int_as_float(sid[j]);
+          put32(j, __float_as_uint(wj));
+          put32(kRegSel + j, (uint32_t)sid[j]);
         } else {
           w_out[t * k + j] = wj;
           idx_out[t * k + j] = sid[j];

@@ -36,37 +36,49 @@ __global__ void __launch_bounds__(kBlock) gating_kernel(const In* __restrict__ l
 // shared memory and runs gate::topk_staged_row on them (gating_device.cuh).
 constexpr int kSmemGateThreads = gate::kStageRows;
 
+// Staged as 16-bit patterns: bf16 logits with at least 64 experts.
+template <int EP, typename In>
+using StageT = typename std::conditional<!std::is_same<In, float>::value && EP >= 64, uint16_t, float>::type;
+
 template <int EP, typename In, int U = 8>
 __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
     const In* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
     int32_t* __restrict__ idx_out) {
-  extern __shared__ float col[];                   // gate::stage_floats<EP>()
+  using St = StageT<EP, In>;
+  extern __shared__ __align__(16) uint8_t stage_raw[];   // gate::stage_bytes<EP, St>()
+  St* col = reinterpret_cast<St*>(stage_raw);
   const int tid = threadIdx.x;
   const long t0 = (long)blockIdx.x * kSmemGateThreads;
   const int nt = (int)min((long)kSmemGateThreads, (long)T - t0);
-  gate::stage_rows<EP, In, U>(logits, t0, nt, E, col, tid, kSmemGateThreads);
+  gate::stage_rows<EP, In, U, St>(logits, t0, nt, E, col, tid, kSmemGateThreads);
   __syncthreads();
   if (k > gate::kRegSel) {
-    if (tid < nt) gate::topk_staged_row<EP>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
+    if (tid < nt) gate::topk_staged_row<EP, false, St>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
     return;
   }
   // Each thread touches only its own row's column, so it parks its k weights and
-  // indices there (slots 0..k-1 and kRegSel..kRegSel+k-1); after the barrier the
-  // block writes its rows' outputs out contiguously.
-  if (tid < nt) gate::topk_staged_row<EP, true>(col, tid, tid, E, k, norm, nullptr, nullptr);
+  // indices there; after the barrier the block writes its rows' outputs out
+  // contiguously.
+  if (tid < nt) gate::topk_staged_row<EP, true, St>(col, tid, tid, E, k, norm, nullptr, nullptr);
   __syncthreads();
+  auto get32 = [&](int slot, int r) -> uint32_t {
+    if constexpr (sizeof(St) == 2)
+      return (uint32_t)col[(2 * slot) * gate::kStageLd + r] | ((uint32_t)col[(2 * slot + 1) * gate::kStageLd + r] << 16);
+    else
+      return __float_as_uint(col[slot * gate::kStageLd + r]);
+  };
   const int n = nt * k;
   for (int f = tid; f < n; f += kSmemGateThreads) {
     const int r = (int)((uint32_t)f / (uint32_t)k), j = f - r * k;
-    w_out[t0 * k + f] = col[j * gate::kStageLd + r];
-    idx_out[t0 * k + f] = __float_as_int(col[(gate::kRegSel + j) * gate::kStageLd + r]);
+    w_out[t0 * k + f] = __uint_as_float(get32(j, r));
+    idx_out[t0 * k + f] = (int32_t)get32(gate::kRegSel + j, r);
   }
 }
 
 template <int EP, typename In>
 int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
-  const size_t smem = (size_t)gate::stage_floats<EP>() * sizeof(float);
+  const size_t smem = (size_t)gate::stage_bytes<EP, StageT<EP, In>>();
   if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
   gating_smem_kernel<EP, In><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
       logits, T, E, k, norm, w, idx);
