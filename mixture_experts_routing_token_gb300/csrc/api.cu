@@ -217,6 +217,7 @@ struct FfnWs {
   void* act;
   void* staging;
   void* xs;
+  int32_t* pos;
 };
 
 size_t dsize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
@@ -227,6 +228,7 @@ FfnWs carve_ffn(Carver& c, int dtype, int T, long S, int H, int I) {
   w.staging = c.take<char>((size_t)S * H * (staging_is_bf16(dtype, T, H, I) ? 2 : 4));
   const size_t xs = ffn_uses_tensor_cores(dtype, H, I) ? ffn_tc_extra_bytes(S, H) : 0;
   w.xs = xs ? c.take<char>(xs) : nullptr;
+  w.pos = xs ? c.take<int32_t>(ffn_tc_pos_bytes(S) / sizeof(int32_t)) : nullptr;
   return w;
 }
 
@@ -263,7 +265,7 @@ int run_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int 
             const float* sw, const int32_t* rev, void* out, const FfnWs& w, int32_t* status,
             cudaStream_t s, bool may_drop = true, const float* logits = nullptr, int norm = 0) {
   FfnArgs a{hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, ids, sw, rev,
-            out, w.act, w.staging, w.xs, status, logits, norm};
+            out, w.act, w.staging, w.xs, w.pos, status, logits, norm};
   if (may_drop) {   // caller routing may hold indices outside [0, E)
     const int rc = launch_zero_dropped(offsets, E, (long)T * k, H, w.staging,
                                        staging_is_bf16(dtype, T, H, I) ? 2 : 4, s);

@@ -113,6 +113,7 @@ struct FfnArgs {
   void* act;        // [S, I] dtype
   void* staging;    // [S, H]: bf16 on the tensor-core prefill path (staging_is_bf16), else float32
   void* xs;         // [S, H] dtype: expert-sorted copy of hidden (the FC1 A operand)
+  int32_t* pos;     // [S]: sorted row of every slot (tensor-core prefill path)
   int32_t* status;
   // Router logits [T, E] (or null): with them the decode FC1 kernel derives the
   // routing of its tokens itself (the same top-k and expert order as the routing
@@ -178,6 +179,7 @@ int launch_ffn_backward(const FfnBwdArgs& a, cudaStream_t s);
 
 bool ffn_uses_tensor_cores(int dtype, int H, int I);
 size_t ffn_tc_extra_bytes(long S, int H);
+size_t ffn_tc_pos_bytes(long S);
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
 int launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
 // The FFN's weighted slot rows ([S, H] staging) are bf16 on the tensor-core

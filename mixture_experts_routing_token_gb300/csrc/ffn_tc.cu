@@ -110,6 +110,84 @@ __global__ void __launch_bounds__(kBulkWarps * 32) gather_rows_bulk_kernel(
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// pos[reverse[p]] = p for the routed rows p < offsets[E]: the sorted row of every
+// slot. Slots the align step dropped keep whatever the buffer held; readers check
+// reverse[pos[s]] == s before they use an entry.
+__global__ void __launch_bounds__(256) slot_rows_kernel(const int32_t* __restrict__ reverse,
+                                                        const int32_t* __restrict__ offsets, int E,
+                                                        int32_t* __restrict__ pos) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = __ldg(offsets + E);
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n; p += gridDim.x * blockDim.x)
+    pos[__ldg(reverse + p)] = p;
+}
+
+// The expert-sorted copy of the token rows in token order: warp w takes batches
+// of R consecutive tokens; lane 0 loads their rows of `hidden` into the warp's
+// shared-memory slots with bulk copies (one mbarrier per slot, bounded waits),
+// then each lane writes one of the batch's R*k slots: a bulk store of the
+// token's row to x_sorted[pos[slot]]. Every row of `hidden` is read once (a
+// walk over the sorted rows reads a token's row once per slot, k times, mostly
+// from DRAM when `hidden` exceeds L2).
+__global__ void __launch_bounds__(kBulkWarps * 32) gather_by_token_kernel(
+    const uint8_t* __restrict__ hidden, const int32_t* __restrict__ pos, const int32_t* __restrict__ reverse,
+    const int32_t* __restrict__ offsets, int E, int T, int k, int row_bytes, int R, uint8_t* __restrict__ xs,
+    int32_t* status) {
+  extern __shared__ __align__(128) uint8_t slots[];   // [kBulkWarps][R][row_bytes]
+  __shared__ __align__(8) uint64_t bar[kBulkWarps][kBulkMaxR];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (lane == 0)
+    for (int r = 0; r < R; ++r) ptx::mbar_init(ptx::smem_u32(&bar[warp][r]), 1);
+  ptx::fence_mbar_init();
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  volatile int* abort_p = &abort_flag;
+  const int n = __ldg(offsets + E);
+  const int nw = gridDim.x * kBulkWarps;
+  const uint32_t my = ptx::smem_u32(slots) + (uint32_t)(warp * R * row_bytes);
+  const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;
+  uint32_t ph = 0;
+  for (int t0 = (blockIdx.x * kBulkWarps + warp) * R; t0 < T; t0 += nw * R) {
+    const int nr = min(R, T - t0);
+    if (lane == 0)
+      for (int r = 0; r < nr; ++r) {
+        const uint32_t b = ptx::smem_u32(&bar[warp][r]);
+        ptx::mbar_arrive_expect_tx(b, (uint32_t)row_bytes);
+        bulk_load(my + (uint32_t)(r * row_bytes), hidden + (long)(t0 + r) * row_bytes, (uint32_t)row_bytes, b);
+      }
+    bool ok = true;   // every lane sees the rows land before it stores from them
+    for (int r = 0; r < nr && ok; ++r) ok = ptx::mbar_wait(ptx::smem_u32(&bar[warp][r]), ph, abort_p, kBulkWaitNs);
+    if (!__all_sync(0xffffffffu, ok)) {   // let the loads still in flight land (bounded) before the slots go away
+      if (lane == 0) {
+        for (int r = 0; r < nr; ++r) {
+          int dummy = 0;
+          ptx::mbar_wait(ptx::smem_u32(&bar[warp][r]), ph, &dummy, kBulkWaitNs / 2);
+        }
+        if (status) atomicOr(status, MOE_STATUS_TIMEOUT);
+      }
+      break;
+    }
+    for (int l = lane; l < nr * k; l += 32) {
+      const int r = kshift >= 0 ? l >> kshift : l / k;
+      const int s = (t0 + r) * k + (l - r * k);
+      const int p = __ldg(pos + s);
+      if (p >= 0 && p < n && __ldg(reverse + p) == s)
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(xs + (long)p * row_bytes),
+                     "r"(my + (uint32_t)(r * row_bytes)), "r"((uint32_t)row_bytes)
+                     : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // this lane's stores have read the slots
+    __syncwarp();                                                      // ... and every lane's: refill
+    ph ^= 1u;
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---- host -------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -201,6 +279,7 @@ bool staging_is_bf16(int dtype, int T, int H, int I) {
 }
 
 size_t ffn_tc_extra_bytes(long S, int H) { return (size_t)S * H * 2; }
+size_t ffn_tc_pos_bytes(long S) { return (size_t)S * sizeof(int32_t); }
 
 int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   const long S = (long)a.T * a.k;
@@ -208,7 +287,27 @@ int launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   if (a.T <= kDecodeMaxTokens) return launch_ffn_decode(a, s);
   CUtensorMap tA1, tB1, tA2, tB2, tS2;
   int rc;
-  if ((rc = launch_gather_rows(a.hidden, a.sorted_ids, a.offsets, a.E, a.H * 2, a.xs, a.status, s))) return rc;
+  const int row_bytes = a.H * 2;
+  if (row_bytes <= kBulkRowMax) {
+    {
+      ProfScope ps("slot_rows", s);
+      const int grid = (int)std::max(1L, std::min((long)num_sms() * 4, (S + 255) / 256));
+      const cudaError_t e = launch_pdl(slot_rows_kernel, grid, 256, 0, s, a.reverse, a.offsets, a.E, a.pos);
+      if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "slot_rows: %s", cudaGetErrorString(e));
+      if ((rc = check_launch("slot_rows"))) return rc;
+    }
+    ProfScope ps("gather_rows", s);
+    if ((rc = ensure_smem_limit(gather_by_token_kernel, kBulkSmem, "gather_rows"))) return rc;
+    const int R = std::min(kBulkMaxR, kBulkRowMax / row_bytes);
+    const cudaError_t e =
+        launch_pdl(gather_by_token_kernel, num_sms(), kBulkWarps * 32, (size_t)kBulkWarps * R * row_bytes, s,
+                   static_cast<const uint8_t*>(a.hidden), a.pos, a.reverse, a.offsets, a.E, a.T, a.k, row_bytes, R,
+                   static_cast<uint8_t*>(a.xs), a.status);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gather_rows: %s", cudaGetErrorString(e));
+    if ((rc = check_launch("gather_rows"))) return rc;
+  } else if ((rc = launch_gather_rows(a.hidden, a.sorted_ids, a.offsets, a.E, row_bytes, a.xs, a.status, s))) {
+    return rc;
+  }
   if ((rc = make_tmap(&tA1, a.xs, (uint64_t)S, (uint64_t)a.H, 128))) return rc;
   if ((rc = make_tmap(&tB1, a.w13, (uint64_t)a.E * 2 * a.I, (uint64_t)a.H, 128))) return rc;
   if ((rc = make_tmap(&tA2, a.act, (uint64_t)S, (uint64_t)a.I, 128))) return rc;
