@@ -87,8 +87,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device):
     if stream is None:
+        if _raw_stream is not None:      # the current stream's handle without a Stream object
+            return ctypes.c_void_p(_raw_stream(device.index if device.index is not None else
+                                               torch.cuda.current_device()))
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
@@ -350,8 +356,8 @@ def moe_layer_forward(hidden, router_logits, w13, w2, k, norm_topk_prob=True, ou
         _out(topk_weights, (T, k), torch.float32, d, "topk_weights")
     if topk_indices is not None:
         _out(topk_indices, (T, k), torch.int32, d, "topk_indices")
-    need = moe_layer_workspace_size(dt, T, H, I, E, k)
     if workspace is None:
+        need = moe_layer_workspace_size(dt, T, H, I, E, k)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=d)
     _check("moe_layer_forward", lib().moe_layer_forward(
         _ptr(hidden), _ptr(router_logits), _ptr(w13), _ptr(w2), dt, T, H, I, E, k,
