@@ -447,54 +447,61 @@ __global__ void __launch_bounds__(kGroupWarps * 32) group_topk_kernel(
   }
 }
 
-// Lane-per-group form (n_group <= 32, group size <= 32): lane g of a group of
-// L lanes holds expert group g (contiguous, gs experts) and its bias for the
-// whole token loop; the group score is lane-local, topk_group rounds then k
-// rounds of butterfly arg-max pick groups and experts.
-template <int L, int V>
-__global__ void __launch_bounds__(kBlock) group_topk_lane_kernel(
+// Groups of at most 32 experts, L >= n_group lanes per token (one per group). Lane g
+// parks its group's choice scores in its own shared-memory row (32 + 1 floats:
+// conflict-free) and keeps the maxima of the group's sub-groups of 8 in
+// registers. The group score (max, or the sum of the two largest, computed with
+// min/max only) and the topk_group best groups come first; then each of the k
+// rounds takes every lane's best remaining (value, expert) from its sub-group
+// maxima, merges the token's lanes with a butterfly on (value desc, expert asc),
+// and only the lane owning the winner marks it taken (-inf) and rescans that
+// sub-group. 8 lanes per token share the token's 1 KB of scores, so many warps
+// fit per SM.
+constexpr int kLaneSmemLd = 33;
+
+template <int L>
+__global__ void __launch_bounds__(kBlock) group_topk_lane_smem_kernel(
     const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k, int n_group,
     int topk_group, int noaux, float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  __shared__ float park[kBlock * kLaneSmemLd];
   const int g = threadIdx.x & (L - 1);
   const unsigned gm = group_mask<L>();
+  float* my = park + threadIdx.x * kLaneSmemLd;
   const int gs = E / n_group;
   const bool has = g < n_group;
   const int base = g * gs;
-  const bool vec = (gs & 3) == 0;
+  const int nsub = (gs + 7) / 8;
   const long step = (long)gridDim.x * (kBlock / L);
   for (long t = (long)blockIdx.x * (kBlock / L) + threadIdx.x / L; t < T; t += step) {
     const float* row = scores + t * (long)E + base;
-    float cv[V];
-    if (vec) {
-#pragma unroll
-      for (int q = 0; q < V / 4; ++q) {
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (has && 4 * q < gs) {
-          x = __ldg(reinterpret_cast<const float4*>(row) + q);
-          if (noaux) {
-            const float4 b = __ldg(reinterpret_cast<const float4*>(bias + base) + q);
-            x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
-          }
-        }
-        cv[4 * q] = x.x; cv[4 * q + 1] = x.y; cv[4 * q + 2] = x.z; cv[4 * q + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < V; ++i)
-        cv[i] = (has && i < gs) ? (noaux ? __ldg(row + i) + __ldg(bias + base + i) : __ldg(row + i)) : 0.0f;
-    }
-    unsigned taken = 0;
     float b1 = -FLT_MAX, b2 = -FLT_MAX;
+    if (has && (gs & 3) == 0) {
+      for (int q = 0; q < gs / 4; ++q) {
+        float4 x = __ldg(reinterpret_cast<const float4*>(row) + q);
+        if (noaux) {
+          const float4 b = __ldg(reinterpret_cast<const float4*>(bias + base) + q);
+          x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+        }
+        const float v[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      if (!has || i >= gs) {
-        taken |= 1u << i;
-      } else {
-        const float x = cv[i];
-        if (x > b1) { b2 = b1; b1 = x; }
-        else if (x > b2) b2 = x;
+        for (int i = 0; i < 4; ++i) {
+          my[4 * q + i] = v[i];
+          const float lo = fminf(b1, v[i]);
+          b1 = fmaxf(b1, v[i]);
+          b2 = fmaxf(b2, lo);
+        }
+      }
+    } else if (has) {
+      for (int i = 0; i < gs; ++i) {
+        const float v = noaux ? __ldg(row + i) + __ldg(bias + base + i) : __ldg(row + i);
+        my[i] = v;
+        const float lo = fminf(b1, v);
+        b1 = fmaxf(b1, v);
+        b2 = fmaxf(b2, lo);
       }
     }
+    if (has)
+      for (int i = gs; i < 8 * nsub; ++i) my[i] = -INFINITY;
     const float gscore = noaux ? b1 + b2 : b1;
     unsigned gsel = 0;
     for (int j = 0; j < topk_group; ++j) {
@@ -508,20 +515,58 @@ __global__ void __launch_bounds__(kBlock) group_topk_lane_kernel(
       }
       gsel |= 1u << bi;
     }
-    if (!((gsel >> g) & 1u)) taken = 0xffffffffu;
-    for (int j = 0; j < k; ++j) {
-      float bv = 0.0f;
-      int bi = kNone;
+    const bool live = has && ((gsel >> g) & 1u);
+    // sub-group maxima (value, first expert holding it)
+    float sv[4];
+    int si[4];
 #pragma unroll
-      for (int i = 0; i < V; ++i)
-        if (!((taken >> i) & 1u) && (bi == kNone || cv[i] > bv)) { bv = cv[i]; bi = base + i; }
+    for (int q = 0; q < 4; ++q) {
+      float v = -INFINITY;
+      int i0 = kNone;
+      if (live && q < nsub) {
+        v = my[8 * q];
+        i0 = base + 8 * q;
+#pragma unroll
+        for (int c = 1; c < 8; ++c) {
+          const float x = my[8 * q + c];
+          i0 = x > v ? base + 8 * q + c : i0;
+          v = fmaxf(v, x);
+        }
+      }
+      sv[q] = v;
+      si[q] = i0;
+    }
+    for (int j = 0; j < k; ++j) {
+      float bv = sv[0];
+      int bi = si[0];
+#pragma unroll
+      for (int q = 1; q < 4; ++q) {   // sub-groups in ascending expert order: strict > keeps the lower
+        const bool b = sv[q] > bv;
+        bv = b ? sv[q] : bv;
+        bi = b ? si[q] : bi;
+      }
+      if (bi != kNone && bv == -INFINITY) bi = kNone;   // a dead or exhausted lane offers nothing
 #pragma unroll
       for (int off = L / 2; off >= 1; off >>= 1) {
         const float ov = __shfl_xor_sync(gm, bv, off, L);
         const int oi = __shfl_xor_sync(gm, bi, off, L);
         if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
       }
-      if (bi >= base && bi < base + gs) taken |= 1u << (bi - base);
+      if (bi >= base && bi < base + gs) {   // this lane owns the winner: take it, rescan its sub-group
+        const int q = (bi - base) >> 3;
+        my[bi - base] = -INFINITY;
+        float v = my[8 * q];
+        int i0 = base + 8 * q;
+#pragma unroll
+        for (int c = 1; c < 8; ++c) {
+          const float x = my[8 * q + c];
+          i0 = x > v ? base + 8 * q + c : i0;
+          v = fmaxf(v, x);
+        }
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+          if (qq == q) { sv[qq] = v; si[qq] = i0; }
+      }
       if ((j & (L - 1)) == g) {
         // noaux_tc reports the un-biased score of the chosen expert (a cached re-read)
         w_out[t * k + j] = noaux ? __ldg(scores + t * (long)E + bi) : bv;
@@ -654,26 +699,15 @@ int launch_group_smem(const float* scores, const float* bias, int T, int E, int 
   return check_launch("group_limited_topk");
 }
 
-template <int L, int V>
-int launch_group_lane_t(const float* scores, const float* bias, int T, int E, int k, int n_group,
-                        int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
+template <int L>
+int launch_group_lane_smem(const float* scores, const float* bias, int T, int E, int k, int n_group, int topk_group,
+                           int noaux, float* w, int32_t* idx, cudaStream_t s) {
   const int tpb = kBlock / L;
-  long blocks = ((long)T + tpb - 1) / tpb;
+  const long blocks = ((long)T + tpb - 1) / tpb;
   const long cap = (long)num_sms() * 16;
-  group_topk_lane_kernel<L, V><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
+  group_topk_lane_smem_kernel<L><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
       scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
   return check_launch("group_limited_topk");
-}
-
-template <int V>
-int launch_group_lane_v(const float* scores, const float* bias, int T, int E, int k, int n_group,
-                        int topk_group, int noaux, float* w, int32_t* idx, cudaStream_t s) {
-  if (n_group <= 1) return launch_group_lane_t<1, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (n_group <= 2) return launch_group_lane_t<2, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (n_group <= 4) return launch_group_lane_t<4, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (n_group <= 8) return launch_group_lane_t<8, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (n_group <= 16) return launch_group_lane_t<16, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  return launch_group_lane_t<32, V>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
 }
 
 template <int V>
@@ -755,12 +789,15 @@ int launch_group_limited_topk(const float* scores, const float* bias, int T, int
   if (T == 0) return MOE_OK;
   ProfScope ps("group_limited_topk", s);
   const int gs = E / n_group;
+  if (gs <= 32) {   // one lane per group (measured 1.7x faster than a thread per token at E = 256)
+    if (n_group <= 4) return launch_group_lane_smem<4>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+    if (n_group <= 8) return launch_group_lane_smem<8>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+    if (n_group <= 16) return launch_group_lane_smem<16>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+    return launch_group_lane_smem<32>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  }
   if (E <= 64) return launch_group_smem<64>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 128) return launch_group_smem<128>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 256) return launch_group_smem<256>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (gs <= 8) return launch_group_lane_v<8>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (gs <= 16) return launch_group_lane_v<16>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
-  if (gs <= 32) return launch_group_lane_v<32>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 32) return launch_group_t<1>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 64) return launch_group_t<2>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
   if (E <= 128) return launch_group_t<4>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
