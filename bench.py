@@ -154,7 +154,21 @@ def make_device_inputs(wl, device, seed=0):
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed)
-    T, H, I, E = wl.T, wl.H, wl.I, wl.E
+    hidden, logits = draw_tokens(wl, device, g, seed)
+    H, I, E = wl.H, wl.I, wl.E
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    w13 = torch.empty((E, 2 * I, H), device=device, dtype=dt)
+    w2 = torch.empty((E, H, I), device=device, dtype=dt)
+    for e in range(E):   # one expert at a time keeps the fp32 temporaries small
+        w13[e] = (torch.randn((2 * I, H), generator=g, device=device) / H ** 0.5).to(dt)
+        w2[e] = (torch.randn((H, I), generator=g, device=device) / I ** 0.5).to(dt)
+    return hidden, logits, w13, w2
+
+
+def draw_tokens(wl, device, g, seed):
+    """hidden [T, H] and router logits [T, E] of one batch from generator g."""
+    import torch
+    T, H, E = wl.T, wl.H, wl.E
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     hidden = torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(dt)
     bias = torch.zeros(E, device=device, dtype=torch.float32)
@@ -175,12 +189,14 @@ def make_device_inputs(wl, device, seed=0):
         if bad.numel() == 0:
             break
         logits[bad] = torch.randn((bad.numel(), E), generator=g, device=device, dtype=torch.float32) + bias
-    w13 = torch.empty((E, 2 * I, H), device=device, dtype=dt)
-    w2 = torch.empty((E, H, I), device=device, dtype=dt)
-    for e in range(E):   # one expert at a time keeps the fp32 temporaries small
-        w13[e] = (torch.randn((2 * I, H), generator=g, device=device) / H ** 0.5).to(dt)
-        w2[e] = (torch.randn((H, I), generator=g, device=device) / I ** 0.5).to(dt)
-    return hidden, logits, w13, w2
+    return hidden, logits
+
+
+# Decode batches (T <= DECODE_T) rotate over this many token batches, one per step, so
+# that consecutive steps route to different experts, as consecutive decode steps do:
+# with one batch repeated, the ~L2-sized set of expert rows a step reads would partly
+# stay in L2 from the step before.
+DECODE_T, DECODE_BATCHES = 64, 8
 
 
 def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
@@ -432,25 +448,47 @@ def fp32_simt_peak_tflops():
 def dominant_roofline(moe, wl, kern, logits, peaks, step_ms):
     """Roofline of the kernel that bounds the workload, from the per-kernel CUDA-event times.
 
-    decode (T <= 64): ffn_fc1_decode streams the weight rows of the experts the batch
-    routes to: algorithmic bytes = those rows + the token rows + the activations written;
-    the layer step's bandwidth over all active expert weights (w13 and w2) is added.
+    decode, one kernel (T <= 2 inside the layer call): ffn_decode_layer streams every
+    active expert's w13 and w2 rows; algorithmic bytes = those rows + the token rows +
+    the activations written and read back + the output.
+    decode, two kernels (T <= 64): ffn_fc1_gemv (T <= 2, CUDA-core matrix-vector
+    products) or ffn_fc1_decode (tensor cores) streams the weight rows of the experts
+    the batch routes to: algorithmic bytes = those rows + the token rows + the
+    activations written. Both add the layer step's bandwidth over all active expert
+    weights (w13 and w2).
     prefill bf16: ffn_fc1_tc, 2 S H 2I flops per launch against the measured bf16 burst peak.
     float32 (CUDA cores): ffn_fc1_simt, the same flops against the FP32 FMA rate.
     """
     import torch
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
     S = T * k
-    dec = kern.get("ffn_fc1_decode")
-    if dec and dec["launches"]:
+    lay = kern.get("ffn_decode_layer")
+    if lay and lay["launches"]:
+        # one kernel for the whole FFN: every active expert's w13 and w2 rows, the
+        # token rows, the activations written and read back, the output written
+        _, ti = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
+        active = int(torch.unique(ti).numel())
+        nbytes = float(active * 3 * I * H * 2 + T * H * 2 + 2 * S * I * 2 + T * H * 2)
+        lay_ms = lay["total_ms"] / lay["launches"]
+        gbs = nbytes / (lay_ms / 1e3) / 1e9
+        step_bytes = float(active * 3 * I * H * 2)
+        return {"bound": "hbm", "kernel": "ffn_decode_layer", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": kernel_traffic("ffn_decode_layer", wl.name),
+                "peak_source": peaks["source"] + " (copy bandwidth)", "active_experts": active,
+                "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": lay_ms,
+                "layer_step_weight_GBps": step_bytes / (step_ms / 1e3) / 1e9,
+                "layer_step_weight_frac": step_bytes / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    dname = next((n for n in ("ffn_fc1_gemv", "ffn_fc1_decode") if kern.get(n) and kern[n]["launches"]), None)
+    if dname:
+        dec = kern[dname]
         _, ti = moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob)
         active = int(torch.unique(ti).numel())
         nbytes = float(active * 2 * I * H * 2 + T * H * 2 + S * I * 2)
         dec_ms = dec["total_ms"] / dec["launches"]
         gbs = nbytes / (dec_ms / 1e3) / 1e9
         step_bytes = float(active * 3 * I * H * 2)
-        return {"bound": "hbm", "kernel": "ffn_fc1_decode", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": kernel_traffic("ffn_fc1_decode", wl.name),
+        return {"bound": "hbm", "kernel": dname, "achieved": gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": kernel_traffic(dname, wl.name),
                 "peak_source": peaks["source"] + " (copy bandwidth)", "active_experts": active,
                 "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": dec_ms,
                 "layer_step_weight_GBps": step_bytes / (step_ms / 1e3) / 1e9,
@@ -480,42 +518,57 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
     import torch
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
     hidden, logits, w13, w2 = make_device_inputs(wl, dev, seed=seed)
+    nb = DECODE_BATCHES if T <= DECODE_T else 1
+    hiddens, logitss = [hidden], [logits]
+    for r in range(1, nb):
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed * 1000 + r)
+        h_r, l_r = draw_tokens(wl, dev, g, seed)
+        hiddens.append(h_r)
+        logitss.append(l_r)
     dcode = moe.MOE_BF16 if wl.dtype == "bf16" else moe.MOE_F32
     ws = torch.empty(moe.moe_layer_workspace_size(dcode, T, H, I, E, k), dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=hidden.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
+    count = [0]
 
-    def step():
-        moe.moe_layer_forward(hidden, logits, w13, w2, k, wl.norm_topk_prob, out=out, workspace=ws,
-                              stream=stream)
+    def step(s=stream):
+        r = count[0] % nb
+        count[0] += 1
+        moe.moe_layer_forward(hiddens[r], logitss[r], w13, w2, k, wl.norm_topk_prob, out=out, workspace=ws,
+                              stream=s)
 
     for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
 
     use_graph = graph_mode == "on" or (graph_mode == "auto" and T <= 64)
-    graph = None
+    graphs = []
     if use_graph:
-        # one layer step captured once; the timed region replays it (what a decode loop does)
+        # each batch's layer step captured once; the timed region replays them in turn
+        # (what a decode loop does)
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            step_side = lambda: moe.moe_layer_forward(hidden, logits, w13, w2, k, wl.norm_topk_prob, out=out,
-                                                      workspace=ws, stream=side)
-            step_side()
-            torch.cuda.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
-                step_side()
+            for r in range(nb):
+                count[0] = r
+                step(side)
+                torch.cuda.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                count[0] = r
+                with torch.cuda.graph(gr, stream=side, capture_error_mode="thread_local"):
+                    step(side)
+                graphs.append(gr)
         torch.cuda.synchronize()
-        for _ in range(3):
-            graph.replay()
+        for gr in graphs:
+            gr.replay()
         torch.cuda.synchronize()
 
     def run(n):
         for _ in range(n):
             if use_graph:
-                graph.replay()
+                graphs[count[0] % nb].replay()
+                count[0] += 1
             else:
                 step()
 
@@ -569,38 +622,46 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
     e2e = None
     if with_e2e and use_graph:
         # decode batches: the whole step (pinned host inputs -> device, the layer call,
-        # the output -> pinned host) captured once and replayed every step
-        h_hidden = hidden.cpu().pin_memory()
-        h_logits = logits.cpu().pin_memory()
+        # the output -> pinned host) captured once per batch and replayed in turn
+        h_hidden = [h.cpu().pin_memory() for h in hiddens]
+        h_logits = [x.cpu().pin_memory() for x in logitss]
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         d_hidden, d_logits, d_out = torch.empty_like(hidden), torch.empty_like(logits), torch.empty_like(out)
         gs = torch.cuda.Stream(dev)
         gs.wait_stream(stream)
 
-        def e2e_once():
-            d_hidden.copy_(h_hidden, non_blocking=True)
-            d_logits.copy_(h_logits, non_blocking=True)
+        def e2e_once(r):
+            d_hidden.copy_(h_hidden[r], non_blocking=True)
+            d_logits.copy_(h_logits[r], non_blocking=True)
             moe.moe_layer_forward(d_hidden, d_logits, w13, w2, k, wl.norm_topk_prob, out=d_out, workspace=ws,
                                   stream=gs)
             h_out.copy_(d_out, non_blocking=True)
 
+        g_e2e = []
         with torch.cuda.stream(gs):
-            e2e_once()
-            torch.cuda.synchronize()
-            g_e2e = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_e2e, stream=gs, capture_error_mode="thread_local"):
-                e2e_once()
+            for r in range(nb):
+                e2e_once(r)
+                torch.cuda.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=gs, capture_error_mode="thread_local"):
+                    e2e_once(r)
+                g_e2e.append(gr)
         torch.cuda.synchronize()
-        for _ in range(3):
-            g_e2e.replay()
+        for gr in g_e2e:
+            gr.replay()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(steps):
-            g_e2e.replay()
+        for i in range(steps):
+            g_e2e[i % nb].replay()
         b.record(stream)
         torch.cuda.synchronize()
-        assert torch.equal(h_out, out.cpu())      # the copied-back result is the layer's output
+        last = (steps - 1) % nb                   # the copied-back result is the last step's output
+        moe.moe_layer_forward(hiddens[last], logitss[last], w13, w2, k, wl.norm_topk_prob, out=out,
+                              workspace=ws, stream=stream)
+        torch.cuda.synchronize()
+        assert torch.equal(h_out, out.cpu())
+        h_hidden, h_logits = h_hidden[0], h_logits[0]   # per-step copy sizes below
         e_ms = max_over_ranks(a.elapsed_time(b), dev)
         e2e = {"value": whole_job_rate(T, world, steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size() + h_logits.numel() * 4,
@@ -667,7 +728,7 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
            "layer_tflops": 6.0 * T * k * H * I / (ms / 1e3) / 1e12,
            "roofline": dominant_roofline(moe, wl, kern, logits, peaks, ms), "kernels": per_kernel,
            "gpu_launches_per_step": launches, "clocks": clk_rec, "e2e": e2e,
-           "timing": ("CUDA graph replay of one layer step" if use_graph else "eager steps") +
+           "timing": ("CUDA graph replay of one layer step per step" if use_graph else "eager steps") +
                      "; per-kernel CUDA events (roofline, kernels) from a timed pass of %d eager steps just "
                      "before, since events between launches serialise the programmatic dependent launches" % n_prof,
            }
@@ -680,8 +741,10 @@ def workload_config(wl, world):
     return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
             "norm_topk_prob": wl.norm_topk_prob, "dtype": wl.dtype,
             "parallelism": "replicas" if world > 1 else "single",
-            "l2": "inputs larger than L2 (weights %.2f GB)" % weights_gb if weights_gb > 0.2 else
-                  "inputs smaller than L2: L2-warm steps (latency-bound workload)"}
+            "l2": ("inputs larger than L2 (weights %.2f GB)" % weights_gb +
+                   ("; steps rotate over %d token batches, so consecutive steps route to different experts"
+                    % DECODE_BATCHES if wl.T <= DECODE_T else ""))
+                  if weights_gb > 0.2 else "inputs smaller than L2: L2-warm steps (latency-bound workload)"}
 
 
 INPUTS_NOTE = "seeded torch RNG on device (N(0,1); weights N(0,1/sqrt(fan_in)); distinct logits)"

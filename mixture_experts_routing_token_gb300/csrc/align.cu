@@ -321,9 +321,10 @@ template <int EP>
 __global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
     const float* logits, int T, int E, int k, int norm, float* w_out, int32_t* idx_out,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
-    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
+    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
   extern __shared__ int sm[];
   pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
+  if (clear && threadIdx.x == 0) *clear = 0;
   float* col = reinterpret_cast<float*>(sm);
   int* asm_ = sm + gate::stage_floats<EP>();                  // align_chunk's shared memory
   int32_t* s_idx = asm_ + align_smem_bytes(E) / sizeof(int);  // shared copies of the routing
@@ -341,9 +342,10 @@ template <int L, int V>
 __global__ void __launch_bounds__(kThreads) route_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int norm, float* w_out, int32_t* idx_out,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
-    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
+    float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
   extern __shared__ int sm[];
   pdl_trigger();
+  if (clear && threadIdx.x == 0) *clear = 0;
   constexpr int groups = kThreads / L;
   for (long t = threadIdx.x / L; t < T; t += groups)
     gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);
@@ -356,32 +358,32 @@ template <typename Kernel>
 int launch_route_small_k(Kernel kernel, size_t smem, size_t smem_max, const float* logits, int T, int E,
                          int k, int norm, float* w, int32_t* idx, int32_t* counts, int32_t* offsets,
                          int32_t* sorted_ids, float* sorted_w, int32_t* reverse, int32_t* status,
-                         cudaStream_t s) {
+                         int32_t* clear, cudaStream_t s) {
   if (int rc = ensure_smem_limit(kernel, smem_max, "route_small")) return rc;
   ProfScope ps("route_small", s);
   kernel<<<1, kThreads, smem, s>>>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w,
-                                   reverse, status);
+                                   reverse, status, clear);
   return check_launch("route_small");
 }
 
 template <int EP>
 int launch_route_staged(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
-                        int32_t* reverse, int32_t* status, cudaStream_t s) {
+                        int32_t* reverse, int32_t* status, int32_t* clear, cudaStream_t s) {
   const size_t stage = (size_t)gate::stage_floats<EP>() * sizeof(float);
   const size_t copies = (size_t)T * k * (sizeof(int32_t) + sizeof(float));
   return launch_route_small_k(route_small_staged_kernel<EP>, stage + align_smem_bytes(E) + copies,
                               stage + align_smem_bytes(EP) + (size_t)kChunk * 8, logits, T, E, k, norm, w, idx,
-                              counts, offsets, sorted_ids, sorted_w, reverse, status, s);
+                              counts, offsets, sorted_ids, sorted_w, reverse, status, clear, s);
 }
 
 template <int V>
 int launch_route_warp(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                       int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
-                      int32_t* reverse, int32_t* status, cudaStream_t s) {
+                      int32_t* reverse, int32_t* status, int32_t* clear, cudaStream_t s) {
   return launch_route_small_k(route_small_kernel<32, V>, align_smem_bytes(E), align_smem_bytes(MOE_MAX_EXPERTS),
                               logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse,
-                              status, s);
+                              status, clear, s);
 }
 
 }  // namespace
@@ -390,11 +392,13 @@ bool route_is_small(int T, int k) { return T <= gate::kStageRows && (long)T * k 
 
 int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
-                       int32_t* reverse, int32_t* status, cudaStream_t s) {
+                       int32_t* reverse, int32_t* status, int32_t* clear, cudaStream_t s) {
 #define MOE_ROUTE_STAGED(EP) \
-  return launch_route_staged<EP>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, status, s)
+  return launch_route_staged<EP>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, \
+                                 status, clear, s)
 #define MOE_ROUTE_WARP(V) \
-  return launch_route_warp<V>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, status, s)
+  return launch_route_warp<V>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w, reverse, \
+                              status, clear, s)
   if (E <= 8) MOE_ROUTE_STAGED(8);
   if (E <= 16) MOE_ROUTE_STAGED(16);
   if (E <= 32) MOE_ROUTE_STAGED(32);

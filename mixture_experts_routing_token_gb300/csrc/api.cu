@@ -218,6 +218,7 @@ struct FfnWs {
   void* staging;
   void* xs;
   int32_t* pos;
+  int32_t* sync;
 };
 
 size_t dsize(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
@@ -229,6 +230,7 @@ FfnWs carve_ffn(Carver& c, int dtype, int T, long S, int H, int I) {
   const size_t xs = ffn_uses_tensor_cores(dtype, H, I) ? ffn_tc_extra_bytes(S, H) : 0;
   w.xs = xs ? c.take<char>(xs) : nullptr;
   w.pos = xs ? c.take<int32_t>(ffn_tc_pos_bytes(S) / sizeof(int32_t)) : nullptr;
+  w.sync = c.take<int32_t>(1);
   return w;
 }
 
@@ -263,10 +265,13 @@ int check_ws(void* ws, size_t have, size_t need) {
 int run_ffn(const void* hidden, const void* w13, const void* w2, int dtype, int T, int H, int I,
             int E, int k, const int32_t* counts, const int32_t* offsets, const int32_t* ids,
             const float* sw, const int32_t* rev, void* out, const FfnWs& w, int32_t* status,
-            cudaStream_t s, bool may_drop = true, const float* logits = nullptr, int norm = 0) {
+            cudaStream_t s, bool may_drop = true, const float* logits = nullptr, int norm = 0,
+            int32_t* sync = nullptr) {
   FfnArgs a{hidden, w13, w2, dtype, T, H, I, E, k, counts, offsets, ids, sw, rev,
-            out, w.act, w.staging, w.xs, w.pos, status, logits, norm};
-  if (may_drop) {   // caller routing may hold indices outside [0, E)
+            out, w.act, w.staging, w.xs, w.pos, status, logits, norm, sync};
+  // caller routing may hold indices outside [0, E): their staging rows are zero (the
+  // matrix-vector path has no staging rows: it skips dropped slots itself)
+  if (may_drop && !ffn_gemv_applies(dtype, T, H, I, k)) {
     const int rc = launch_zero_dropped(offsets, E, (long)T * k, H, w.staging,
                                        staging_is_bf16(dtype, T, H, I) ? 2 : 4, s);
     if (rc) return rc;
@@ -576,9 +581,10 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
   const AlignWs al = carve_align(c, S, E);
   const FfnWs fw = carve_ffn(c, dtype, T, S, H, I);
 
-  if (route_is_small(T, k)) {
+  const bool small = route_is_small(T, k);
+  if (small) {
     if ((rc = launch_route_small(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, al.counts, al.offsets,
-                                 al.sorted_ids, al.sorted_w, al.reverse, status, s)))
+                                 al.sorted_ids, al.sorted_w, al.reverse, status, fw.sync, s)))
       return rc;
   } else {
     if ((rc = launch_gating(router_logits, T, E, k, norm_topk_prob != 0, tw, ti, s))) return rc;
@@ -587,10 +593,11 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
       return rc;
   }
   // the layer's own gating only produces indices in [0, E): no slot is dropped. The
-  // logits let the decode kernels start on the experts' weights before routing ends.
+  // logits let the decode kernels start on the experts' weights before routing ends;
+  // the word the small-batch routing kernel zeroes serves the decode FFN's grid barrier.
   return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, al.counts, al.offsets, al.sorted_ids,
                  al.sorted_w, al.reverse, out, fw, status, s, /*may_drop=*/false, router_logits,
-                 norm_topk_prob != 0);
+                 norm_topk_prob != 0, small ? fw.sync : nullptr);
 }
 
 MOE_API int moe_gather_rows(const void* hidden, const int32_t* sorted_token_ids, const int32_t* offsets,

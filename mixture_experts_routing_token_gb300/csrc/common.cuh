@@ -87,11 +87,11 @@ int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E
 
 size_t align_scratch_bytes(long S, int E);
 // Gating + align in one single-CTA launch, for at most 128 tokens whose T*k
-// slots fit one align chunk.
+// slots fit one align chunk; it also zeroes *clear (when not null).
 bool route_is_small(int T, int k);
 int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
-                       int32_t* reverse, int32_t* status, cudaStream_t s);
+                       int32_t* reverse, int32_t* status, int32_t* clear, cudaStream_t s);
 int launch_align_noalloc(const int32_t* idx, const float* w, int T, int k, int E, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, float* sorted_w, int32_t* reverse,
                          int32_t* status, cudaStream_t s);
@@ -120,6 +120,9 @@ struct FfnArgs {
   // kernel, whose outputs it then waits for only before FC2 may start).
   const float* logits;
   int norm;
+  // A word zeroed by the routing kernel launched just before (or null): the grid
+  // barrier of the one-kernel decode FFN (ffn_gemv.cu).
+  int32_t* sync;
 };
 
 // bf16 matrix [rows, cols] row-major as a TMA tensor map: box = box_rows x 64
@@ -137,6 +140,13 @@ int launch_ep_combine(const void* y, const float* w, const int32_t* reverse, con
 // Token-count threshold at or below which the weight-streaming decode kernels run.
 constexpr int kDecodeMaxTokens = 64;
 int launch_ffn_decode(const FfnArgs& a, cudaStream_t s);
+// Batches of at most kGemvMaxTokens tokens: matrix-vector products on the CUDA
+// cores with the combine folded into FC2 (ffn_gemv.cu); token rows and
+// activation rows must fit kGemvSmemMax bytes of shared memory.
+constexpr int kGemvMaxTokens = 2;
+constexpr size_t kGemvSmemMax = 96 * 1024;
+bool ffn_gemv_applies(int dtype, int T, int H, int I, int k);
+int launch_ffn_gemv(const FfnArgs& a, cudaStream_t s);
 // FC1 and FC2 on 2-SM clusters (tcgen05 cta_group::2), given the five tensor
 // maps (A: 128-row boxes of x_sorted / act; B: 128-row boxes of w13 / w2;
 // S2: 32-row boxes of act for FC2's swapped remainder tiles).

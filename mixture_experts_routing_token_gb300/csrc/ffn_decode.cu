@@ -157,59 +157,8 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   // from two launches back and are complete once FC1 has triggered.
   if (MODE == DEC_FC1 && !local) pdl_wait();
   if (!local) pdl_trigger();
-  if (kCanRoute && local) {
-    // the routing of the batch, as the routing kernel computes it: top-k experts of
-    // each token, then each slot's rank among the earlier slots of its expert
-    const int S = P.T * P.k;
-    for (int t = warp; t < P.T; t += DTHREADS / 32) {   // a warp per token: lane l holds experts l, l + 32
-      const float* row = P.logits + (long)t * P.E;
-      unsigned key[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) key[i] = lane + 32 * i < P.E ? gate::okey(__ldg(row + lane + 32 * i)) : 0u;
-      unsigned taken = 0;
-      for (int j = 0; j < P.k; ++j) {   // largest value, then the lower expert among equal values
-        unsigned kv;
-        const int e = gate::warp_argmax_round<2>(key, taken, lane, &kv);
-        if ((e & 31) == lane) taken |= 1u << (e >> 5);
-        if (lane == 0) l_idx[t * P.k + j] = e;
-      }
-    }
-    for (int e = tid; e < P.E; e += DTHREADS) l_cnt[e] = 0;
-    __syncthreads();
-    for (int q = tid; q < S; q += DTHREADS) atomicAdd(&l_cnt[l_idx[q]], 1);
-    __syncthreads();
-    if (warp == 0) {   // exclusive offsets, two experts per lane (E <= 64)
-      const int a = 2 * lane < P.E ? l_cnt[2 * lane] : 0, b = 2 * lane + 1 < P.E ? l_cnt[2 * lane + 1] : 0;
-      int incl = a + b;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
-      }
-      if (2 * lane < P.E) l_off[2 * lane] = incl - a - b;
-      if (2 * lane + 1 < P.E) l_off[2 * lane + 1] = incl - b;
-      if (lane == 31) l_off[P.E] = incl;
-    }
-    __syncthreads();
-    if (warp == 0) {   // stable expert order: rounds of 32 slots, ranked by __match_any_sync
-      for (int e = lane; e < P.E; e += 32) l_run[e] = 0;
-      __syncwarp();
-      for (int q0 = 0; q0 < S; q0 += 32) {
-        const int q = q0 + lane;
-        const int e = q < S ? l_idx[q] : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int below = __popc(peers & ((1u << lane) - 1u));
-        const int prior = e >= 0 ? l_run[e] : 0;
-        __syncwarp();
-        if (e >= 0) {
-          l_ids[l_off[e] + prior + below] = q / P.k;
-          if (below == 0) l_run[e] = prior + __popc(peers);
-        }
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-  }
+  // the routing of the batch, as the routing kernel computes it
+  if (kCanRoute && local) gate::route_block(P.logits, P.T, P.E, P.k, l_idx, l_cnt, l_off, l_ids, l_run);
   if (warp == 2) {   // tile_start[e] = sum over e' < e of ceil(count / NTOK) * NTW
     const int per = (P.E + 31) / 32;
     const int e0 = min(P.E, lane * per), e1 = min(P.E, e0 + per);
@@ -439,6 +388,7 @@ int run_decode(const FfnArgs& a, cudaStream_t s) {
 
 int launch_ffn_decode(const FfnArgs& a, cudaStream_t s) {
   if ((long)a.T * a.k == 0) return MOE_OK;
+  if (ffn_gemv_applies(a.dtype, a.T, a.H, a.I, a.k)) return launch_ffn_gemv(a, s);
   if (a.T <= 16) return run_decode<16>(a, s);
   if (a.T <= 32) return run_decode<32>(a, s);
   return run_decode<64>(a, s);

@@ -486,6 +486,69 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
   }
 }
 
+// Routing of a small batch inside one CTA, every thread of the block taking
+// part: the top-k experts of each of the T tokens (a warp per token, experts l
+// and l + 32 in lane l, so E <= 64; largest logit first, the lower expert among
+// equal logits, as the routing kernels choose), then every expert's count, its
+// offset and its tokens in slot order (the stable expert order of the align
+// step). All arrays in shared memory: idx[T*k], cnt[E], off[E+1], ids[T*k], run[E],
+// and (when not null) pos[T*k]: the sorted position of every slot.
+__device__ __forceinline__ void route_block(const float* __restrict__ logits, int T, int E, int k,
+                                            int32_t* idx, int32_t* cnt, int32_t* off, int32_t* ids,
+                                            int32_t* run, int32_t* pos = nullptr) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const int S = T * k;
+  for (int t = warp; t < T; t += nwarps) {
+    const float* row = logits + (long)t * E;
+    unsigned key[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) key[i] = lane + 32 * i < E ? okey(__ldg(row + lane + 32 * i)) : 0u;
+    unsigned taken = 0;
+    for (int j = 0; j < k; ++j) {
+      unsigned kv;
+      const int e = warp_argmax_round<2>(key, taken, lane, &kv);
+      if ((e & 31) == lane) taken |= 1u << (e >> 5);
+      if (lane == 0) idx[t * k + j] = e;
+    }
+  }
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int q = tid; q < S; q += blockDim.x) atomicAdd(&cnt[idx[q]], 1);
+  __syncthreads();
+  if (warp == 0) {   // exclusive offsets, two experts per lane
+    const int a = 2 * lane < E ? cnt[2 * lane] : 0, b = 2 * lane + 1 < E ? cnt[2 * lane + 1] : 0;
+    int incl = a + b;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    if (2 * lane < E) off[2 * lane] = incl - a - b;
+    if (2 * lane + 1 < E) off[2 * lane + 1] = incl - b;
+    if (lane == 31) off[E] = incl;
+  }
+  __syncthreads();
+  if (warp == 0) {   // rounds of 32 slots, ranked within their expert by __match_any_sync
+    for (int e = lane; e < E; e += 32) run[e] = 0;
+    __syncwarp();
+    for (int q0 = 0; q0 < S; q0 += 32) {
+      const int q = q0 + lane;
+      const int e = q < S ? idx[q] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int below = __popc(peers & ((1u << lane) - 1u));
+      const int prior = e >= 0 ? run[e] : 0;
+      __syncwarp();
+      if (e >= 0) {
+        ids[off[e] + prior + below] = q / k;
+        if (pos) pos[q] = off[e] + prior + below;
+        if (below == 0) run[e] = prior + __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+}
+
 }  // namespace gate
 }  // namespace moe
 

@@ -85,6 +85,21 @@ def test_layer_decode_shapes(T, H, I, E, k, norm):
                                        logits="distinct", seed=T * 7))
 
 
+# matrix-vector path (bf16, T <= 2): rows longer than one round of a warp's pieces (H > 2048),
+# piece counts that are not a multiple of 32 (I = 1408, 448), rows of only 8 pieces
+# (H = I = 64), experts shared by both tokens, routing inside each CTA (E <= 64) and from
+# the routing kernel (E > 64), 64 slots (k = 32)
+@pytest.mark.parametrize("T,H,I,E,k,norm", [
+    (1, 2112, 1408, 4, 4, True), (2, 2112, 448, 4, 3, False), (1, 64, 64, 8, 8, True),
+    (2, 64, 192, 3, 3, True), (2, 256, 128, 100, 8, True), (2, 128, 128, 64, 32, False),
+    (1, 128, 320, 200, 32, True),
+])
+def test_layer_matrix_vector_shapes(T, H, I, E, k, norm):
+    moe = need_gpu()
+    _full_check(moe, make_layer_inputs(T=T, H=H, I=I, E=E, k=k, norm_topk_prob=norm, dtype="bf16",
+                                       logits="distinct", seed=T * 11 + E))
+
+
 # CUDA-core path: float32, and bf16 shapes the tensor path does not take
 @pytest.mark.parametrize("T,H,I,E,k,dtype", [
     (64, 128, 256, 8, 2, "f32"),
@@ -177,7 +192,8 @@ def test_grouped_ffn_remainders_after_full_tiles(H, I):
     assert_close_rel_max(got[rem], ref[rem], 2e-2, "remainder rows")
 
 
-@pytest.mark.parametrize("T,H,I,E,k", [(300, 256, 256, 8, 2), (40, 128, 128, 16, 4), (90, 40, 24, 5, 2)])
+@pytest.mark.parametrize("T,H,I,E,k", [(300, 256, 256, 8, 2), (40, 128, 128, 16, 4), (90, 40, 24, 5, 2),
+                                       (1, 256, 256, 8, 6), (2, 128, 192, 16, 8)])
 def test_grouped_ffn_dropped_slots_contribute_nothing(T, H, I, E, k):
     """Slots whose expert index is outside [0, E) are dropped by the align step; the FFN must
     ignore them even when the workspace holds stale data (filled with NaN bytes here)."""

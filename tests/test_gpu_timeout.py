@@ -6,7 +6,8 @@ issued finish, free its tensor memory, report MOE_STATUS_TIMEOUT in the call's
 status word and return. The context must stay usable: with the default limit
 restored, the next call matches the oracle and reports nothing.
 No GPU fault is involved: the waits that run out are the kernels' own
-mbarrier waits on their other roles.
+mbarrier waits on their other roles, or (one token) the wait of the
+one-kernel decode FFN's CTAs for each other at its grid barrier.
 """
 import numpy as np
 import pytest
@@ -19,7 +20,8 @@ from oracle import ffn
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [600, 8])      # prefill pair kernels; decode weight-streaming kernels
+# prefill pair kernels; decode weight-streaming kernels; the one-kernel decode FFN's grid barrier
+@pytest.mark.parametrize("T", [600, 8, 1])
 def test_expired_waits_report_timeout_and_leave_the_context_usable(T):
     moe = need_gpu()
     H, I, E, k = 256, 256, 8, 2
