@@ -56,6 +56,18 @@ __device__ __forceinline__ unsigned same_expert_lanes(int e, int bits) {
   return m;
 }
 
+// The same with the number of bits fixed at compile time (the ballots unrolled).
+template <int BITS>
+__device__ __forceinline__ unsigned same_expert_lanes_t(int e) {
+  unsigned m = __ballot_sync(0xffffffffu, e >= 0);
+#pragma unroll
+  for (int b = 0; b < BITS; ++b) {
+    const unsigned bal = __ballot_sync(0xffffffffu, (e >> b) & 1);
+    m &= ((e >> b) & 1) ? bal : ~bal;
+  }
+  return m;
+}
+
 // Dynamic shared memory of align_chunk for E experts.
 __host__ __device__ inline size_t align_smem_bytes(int E) {
   return (size_t)(3 * E + 2 + kWarps * E + 4 * kChunk) * sizeof(int);
@@ -88,8 +100,17 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t* __restrict__ 
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (nchunks + 1023) / 1024;
   const int c0 = min(nchunks, tid * per), c1 = min(nchunks, c0 + per);
+  constexpr int kKeep = 4;   // runs this short stay in registers between the two passes
+  int v[kKeep];
   int run = 0;
-  for (int c = c0; c < c1; ++c) run += chunk_hist[(long)c * E + e];
+  if (per <= kKeep) {
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) v[i] = c0 + i < c1 ? chunk_hist[(long)(c0 + i) * E + e] : 0;
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) run += v[i];
+  } else {
+    for (int c = c0; c < c1; ++c) run += chunk_hist[(long)c * E + e];
+  }
   int incl = run;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -109,9 +130,18 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t* __restrict__ 
   }
   __syncthreads();
   int acc = (warp ? wsum[warp - 1] : 0) + incl - run;
-  for (int c = c0; c < c1; ++c) {
-    acc += chunk_hist[(long)c * E + e];
-    chunk_hist[(long)c * E + e] = acc;
+  if (per <= kKeep) {
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i)
+      if (c0 + i < c1) {
+        acc += v[i];
+        chunk_hist[(long)(c0 + i) * E + e] = acc;
+      }
+  } else {
+    for (int c = c0; c < c1; ++c) {
+      acc += chunk_hist[(long)c * E + e];
+      chunk_hist[(long)c * E + e] = acc;
+    }
   }
 }
 
@@ -160,7 +190,7 @@ __device__ __forceinline__ int warp0_exclusive_scan(int* v, int n) {
 // staging arrays in expert-sorted order together with their global position,
 // then copied out by consecutive threads (each expert's run is contiguous in
 // both orders: coalesced stores). Slot indices are 32-bit (T*k < 2^31).
-template <int SRC>
+template <int SRC, int EB = 0>
 __device__ __forceinline__ void align_chunk(
     int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
     const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -255,8 +285,9 @@ __device__ __forceinline__ void align_chunk(
 #pragma unroll
   for (int u = 0; u < kSub; ++u) {
     const int e = valid_expert(eu[u], E);
-    const unsigned peers =
-        SRC == kSrcGlobal && ebits > 4 ? same_expert_lanes(e, ebits) : __match_any_sync(0xffffffffu, e);
+    const unsigned peers = EB > 0 ? same_expert_lanes_t<EB>(e)
+                           : SRC == kSrcGlobal && ebits > 4 ? same_expert_lanes(e, ebits)
+                                                            : __match_any_sync(0xffffffffu, e);
     const int below = __popc(peers & ((1u << lane) - 1u));
     const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
     __syncwarp();
@@ -301,13 +332,15 @@ __device__ __forceinline__ void align_chunk(
   }
 }
 
+// EB: bits of E - 1 (5..10, the per-bit ballots unrolled), or 0 (E <= 16: __match_any_sync).
+template <int EB>
 __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ wts, long S, int k, int E,
     int nchunks, int hist_is_prefix, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
   extern __shared__ int sm[];
-  align_chunk<kSrcGlobal>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
+  align_chunk<kSrcGlobal, EB>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
                      sorted_ids, sorted_w, reverse, status, sm);
 }
 
@@ -422,8 +455,7 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
   const long S = (long)T * k;
   const int nchunks = (int)((S + kChunk - 1) / kChunk);
   const size_t smem = align_smem_bytes(E);
-  if (int rc = ensure_smem_limit(align_scatter_kernel, align_smem_bytes(MOE_MAX_EXPERTS), "align_scatter"))
-    return rc;
+  const int ebits = 32 - __builtin_clz((unsigned)(E > 1 ? E - 1 : 1));
   int32_t* hist = nullptr;
   if (nchunks > 1) {
     hist = static_cast<int32_t*>(scratch);
@@ -439,10 +471,22 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
     int rc = check_launch("align_scan");
     if (rc) return rc;
   }
-  ProfScope ps("align_scatter", s);
-  align_scatter_kernel<<<nchunks > 0 ? nchunks : 1, kThreads, smem, s>>>(
-      idx, w, S, k, E, nchunks, prefix, hist, counts, offsets, sorted_ids, sorted_w, reverse, status);
-  return check_launch("align_scatter");
+  auto scatter = [&](auto kernel) -> int {
+    if (int rc = ensure_smem_limit(kernel, align_smem_bytes(MOE_MAX_EXPERTS), "align_scatter")) return rc;
+    ProfScope ps("align_scatter", s);
+    kernel<<<nchunks > 0 ? nchunks : 1, kThreads, smem, s>>>(idx, w, S, k, E, nchunks, prefix, hist, counts,
+                                                              offsets, sorted_ids, sorted_w, reverse, status);
+    return check_launch("align_scatter");
+  };
+  switch (ebits) {
+    case 5: return scatter(align_scatter_kernel<5>);
+    case 6: return scatter(align_scatter_kernel<6>);
+    case 7: return scatter(align_scatter_kernel<7>);
+    case 8: return scatter(align_scatter_kernel<8>);
+    case 9: return scatter(align_scatter_kernel<9>);
+    case 10: return scatter(align_scatter_kernel<10>);
+    default: return scatter(align_scatter_kernel<0>);
+  }
 }
 
 // ---- fixed scratch for callers that cannot allocate --------------------------

@@ -295,14 +295,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int t = cluster_id; t < total; t += nclusters) {
+      // the tile's row data first: these loads do not wait for the accumulator
       const PTile ti = ptile(t, tile_start, P.counts, P.E, P.NT, P.NTs);
+      const int cnt = __ldg(P.counts + ti.e);
+      const long pe = (long)__ldg(P.offsets + ti.e);
+      const int r = ti.m_tile * (2 * PBM) + (int)rank * PBM + row;
+      const bool valid = r < cnt;
+      float wt = 0.0f;
+      long dst_row = 0;
+      if (MODE == PAIR_FC2 && !ti.swap_n && valid) {
+        wt = __ldg(P.sorted_w + pe + r);
+        dst_row = (long)__ldg(P.reverse + pe + r);
+      }
       if (!ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aph, abort_p, P.wait_ns)) break;
       ptx::tc_fence_after();
-      const int cnt = __ldg(P.counts + ti.e);
       if (MODE == PAIR_FC2 && ti.swap_n) {
         // lane = output feature f of this SM's 128; TMEM column j = act row r0 + j
         const int r0 = ti.m_tile * (2 * PBM);
-        const long p0 = (long)__ldg(P.offsets + ti.e) + r0;
+        const long p0 = pe + r0;
         const int f = ti.n_tile * (2 * PBM) + (int)rank * PBM + row;
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PBN);
         const int H = P.N_out;
@@ -328,9 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         if (++acc == 2) { acc = 0; aph ^= 1u; }
         continue;
       }
-      const int r = ti.m_tile * (2 * PBM) + (int)rank * PBM + row;
-      const bool valid = r < cnt;
-      const long p = (long)__ldg(P.offsets + ti.e) + r;
+      const long p = pe + r;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PBN);
       if (MODE == PAIR_FC1) {
         const int I = P.N_out;
@@ -360,23 +368,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       } else {
         const int H = P.N_out;
         __nv_bfloat16* staging = static_cast<__nv_bfloat16*>(P.out);
-        const float wt = valid ? __ldg(P.sorted_w + p) : 0.0f;
-        const long dst_row = valid ? (long)__ldg(P.reverse + p) : 0;
 #pragma unroll 1
-        for (int c = 0; c < PBN / 32; ++c) {
-          uint32_t y[32];
-          ptx::tmem_ld32(taddr + c * 32, y);
+        for (int c = 0; c < PBN / 32; c += 2) {   // two 32-column chunks per TMEM wait
+          uint32_t y[2][32];
+          ptx::tmem_ld32(taddr + c * 32, y[0]);
+          ptx::tmem_ld32(taddr + c * 32 + 32, y[1]);
           ptx::tmem_ld_wait();
-          const int col0 = ti.n_tile * PBN + c * 32;
-          if (valid && col0 < H) {   // 32 bf16 = two whole 32-byte sectors
-            uint32_t lo8[8], hi8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              lo8[i] = pack2(__uint_as_float(y[2 * i]) * wt, __uint_as_float(y[2 * i + 1]) * wt);
-              hi8[i] = pack2(__uint_as_float(y[16 + 2 * i]) * wt, __uint_as_float(y[17 + 2 * i]) * wt);
+          for (int h = 0; h < 2; ++h) {
+            const int col0 = ti.n_tile * PBN + (c + h) * 32;
+            if (valid && col0 < H) {   // 32 bf16 = two whole 32-byte sectors
+              uint32_t lo8[8], hi8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                lo8[i] = pack2(__uint_as_float(y[h][2 * i]) * wt, __uint_as_float(y[h][2 * i + 1]) * wt);
+                hi8[i] = pack2(__uint_as_float(y[h][16 + 2 * i]) * wt, __uint_as_float(y[h][17 + 2 * i]) * wt);
+              }
+              st_v8(staging + dst_row * H + col0, lo8);
+              st_v8(staging + dst_row * H + col0 + 16, hi8);
             }
-            st_v8(staging + dst_row * H + col0, lo8);
-            st_v8(staging + dst_row * H + col0 + 16, hi8);
           }
         }
       }

@@ -228,11 +228,16 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
 // ---- thread-per-token top-k over rows parked in shared memory (E <= EP <= 128)
 //
 // A block of up to kStageRows rows is stored column-major, element e of row r at
-// col[e * kStageLd + r] (padded stride: every access below is bank-conflict
-// free); the thread of row r selects with the tournament of topk_staged_row.
+// col[e * kStageLd + r] (padded stride: the selection's reads, a warp's lanes
+// reading one expert of consecutive rows, are bank-conflict free); the thread of
+// row r selects with the tournament of topk_staged_row.
 // Weights as in gate_one_token.
 constexpr int kStageRows = 128;
 constexpr int kStageLd = kStageRows + 1;
+
+// Element e of staged row r.
+template <typename St>
+__host__ __device__ constexpr int sofs(int e, int r) { return e * kStageLd + r; }
 
 // Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into col[EP][kStageLd],
 // experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows); the
@@ -255,25 +260,25 @@ __device__ __forceinline__ void st_neg_inf(uint16_t* p) { *p = 0xff80u; }   // b
 
 // One 16-byte vector of logits (4 float32 or 8 bf16) into row r, experts e0.., of the stage.
 __device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, float) {
-  col[e0 * kStageLd + r] = __uint_as_float(q.x);
-  col[(e0 + 1) * kStageLd + r] = __uint_as_float(q.y);
-  col[(e0 + 2) * kStageLd + r] = __uint_as_float(q.z);
-  col[(e0 + 3) * kStageLd + r] = __uint_as_float(q.w);
+  col[sofs<float>(e0, r)] = __uint_as_float(q.x);
+  col[sofs<float>(e0 + 1, r)] = __uint_as_float(q.y);
+  col[sofs<float>(e0 + 2, r)] = __uint_as_float(q.z);
+  col[sofs<float>(e0 + 3, r)] = __uint_as_float(q.w);
 }
 __device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, __nv_bfloat16) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    col[(e0 + 2 * i) * kStageLd + r] = lo_bf16(w[i]);
-    col[(e0 + 2 * i + 1) * kStageLd + r] = hi_bf16(w[i]);
+    col[sofs<float>(e0 + 2 * i, r)] = lo_bf16(w[i]);
+    col[sofs<float>(e0 + 2 * i + 1, r)] = hi_bf16(w[i]);
   }
 }
 __device__ __forceinline__ void put_vec(uint16_t* col, int e0, int r, const uint4& q, __nv_bfloat16) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    col[(e0 + 2 * i) * kStageLd + r] = (uint16_t)(w[i] & 0xffffu);
-    col[(e0 + 2 * i + 1) * kStageLd + r] = (uint16_t)(w[i] >> 16);
+    col[sofs<uint16_t>(e0 + 2 * i, r)] = (uint16_t)(w[i] & 0xffffu);
+    col[sofs<uint16_t>(e0 + 2 * i + 1, r)] = (uint16_t)(w[i] >> 16);
   }
 }
 __device__ __forceinline__ void put_one(float* p, const float* src) { *p = __ldg(src); }
@@ -322,11 +327,11 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
   } else {
     for (int f = tid; f < nt * E; f += nthr) {
       const int r = f / E;
-      put_one(col + (f - r * E) * kStageLd + r, blk + f);
+      put_one(col + sofs<St>(f - r * E, r), blk + f);
     }
   }
   if (tid < kStageRows)
-    for (int e = E; e < EP; ++e) st_neg_inf(col + e * kStageLd + tid);
+    for (int e = E; e < EP; ++e) st_neg_inf(col + sofs<St>(e, tid));
 }
 
 // Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: the
@@ -365,14 +370,14 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
   constexpr int G = EP / 8;          // groups of 8 experts
   constexpr int S = (G + 3) / 4;     // supers of 4 groups
   float* gcol = reinterpret_cast<float*>(reinterpret_cast<char*>(col) + stage_rows_bytes<EP, St>());
-  auto at = [&](int i) -> float { return st_get(col + i * kStageLd + r); };
+  auto at = [&](int i) -> float { return st_get(col + sofs<St>(i, r)); };
   auto gat = [&](int g) -> float& { return gcol[g * kStageLd + r]; };
   auto put32 = [&](int slot, uint32_t v) {   // a 32-bit result into parking slot `slot`
     if constexpr (kHalf) {
-      col[(2 * slot) * kStageLd + r] = (St)(v & 0xffffu);
-      col[(2 * slot + 1) * kStageLd + r] = (St)(v >> 16);
+      col[sofs<St>(2 * slot, r)] = (St)(v & 0xffffu);
+      col[sofs<St>(2 * slot + 1, r)] = (St)(v >> 16);
     } else {
-      col[slot * kStageLd + r] = __uint_as_float(v);
+      col[sofs<St>(slot, r)] = __uint_as_float(v);
     }
   };
   float sm[S];
@@ -426,7 +431,7 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
 #pragma unroll
     for (int c = 7; c >= 0; --c) bc = x[c] == v ? c : bc;
     e = 8 * bg + bc;
-    st_neg_inf(col + e * kStageLd + r);
+    st_neg_inf(col + sofs<St>(e, r));
     float nm = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 8; ++c) nm = fmaxf(nm, c == bc ? -INFINITY : x[c]);
@@ -438,20 +443,21 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
     for (int q = 0; q < S; ++q) sm[q] = q == bs ? ns : sm[q];
   };
   if (TO_COL || k <= kRegSel) {   // the selected logits stay in registers until the weights are formed
-    float sel[kRegSel];
+    float sel[kRegSel], ex[kRegSel];
     int sid[kRegSel];
 #pragma unroll
     for (int j = 0; j < kRegSel; ++j) {
       if (j < k) {
         take(sel[j], sid[j]);
-        if (norm) two_sum_add(hi, lo, exp_diff(sel[j], m));
+        ex[j] = exp_diff(sel[j], m);
+        if (norm) two_sum_add(hi, lo, ex[j]);
       }
     }
     const float denom = hi + lo;
 #pragma unroll
     for (int j = 0; j < kRegSel; ++j)
       if (j < k) {
-        const float wj = __fdiv_rn(exp_diff(sel[j], m), denom);
+        const float wj = __fdiv_rn(ex[j], denom);
         if (TO_COL) {
           put32(j, __float_as_uint(wj));
           put32(kRegSel + j, (uint32_t)sid[j]);

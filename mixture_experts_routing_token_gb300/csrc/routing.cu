@@ -63,13 +63,14 @@ __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
   __syncthreads();
   auto get32 = [&](int slot, int r) -> uint32_t {
     if constexpr (sizeof(St) == 2)
-      return (uint32_t)col[(2 * slot) * gate::kStageLd + r] | ((uint32_t)col[(2 * slot + 1) * gate::kStageLd + r] << 16);
+      return (uint32_t)col[gate::sofs<St>(2 * slot, r)] | ((uint32_t)col[gate::sofs<St>(2 * slot + 1, r)] << 16);
     else
-      return __float_as_uint(col[slot * gate::kStageLd + r]);
+      return __float_as_uint(col[gate::sofs<St>(slot, r)]);
   };
   const int n = nt * k;
+  const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // row of output f: f >> kshift, or f / k
   for (int f = tid; f < n; f += kSmemGateThreads) {
-    const int r = (int)((uint32_t)f / (uint32_t)k), j = f - r * k;
+    const int r = kshift >= 0 ? f >> kshift : (int)((uint32_t)f / (uint32_t)k), j = f - r * k;
     w_out[t0 * k + f] = __uint_as_float(get32(j, r));
     idx_out[t0 * k + f] = (int32_t)get32(gate::kRegSel + j, r);
   }
