@@ -29,11 +29,11 @@
 // FC1: the first eight units into the buffers of eight warps, the rest into L2),
 // so that DRAM streams FC2's weights together with FC1's; it then meets the other
 // CTAs at a grid barrier (a counter that the routing kernel just before it
-// zeroed, polled with a time limit) and runs FC2: the buffered units, and
-// meanwhile the later units by the warps without a buffer, straight from L2. Its
-// grid leaves one SM to the routing kernel it overlaps, so that every CTA of the
-// barrier is resident. Elsewhere (routing given by the caller, or E > 64) FC1
-// and FC2 are two kernels.
+// zeroed, polled with a time limit) and runs FC2 on the tensor cores (mma.sync
+// on pairs of units, the later units copied into the buffers as the first ones
+// are done). Its grid leaves one SM to the routing kernel it overlaps, so that
+// every CTA of the barrier is resident. Elsewhere (routing given by the caller,
+// or E > 64) FC1 and FC2 are two kernels, FC2 on the CUDA cores.
 #include "common.cuh"
 #include "gating_device.cuh"
 #include "sm100_ptx.cuh"   // smem_u32, globaltimer
@@ -50,7 +50,7 @@ constexpr int kFc2Buffers = 8;                           // FC2 warps with a row
 constexpr int kFc2Threads = kFc2Buffers * 32;            // FC2 kernel
 constexpr size_t kFc2SmemMax = 200 * 1024;               // FC2 kernel: buffers + activation rows
 constexpr size_t kLayerSmemMax = 216 * 1024;             // layer kernel: buffers + activations + token rows
-constexpr int kLayerWarps = kLayerThreads / 32;
+constexpr int kMaxPairs = 4;                             // layer kernel: FC2 unit pairs per round (four warps each)
 
 struct GemvParams {
   const uint4* hidden;   // [T, H] bf16
@@ -79,8 +79,12 @@ struct Fc2Layout {
 
 __host__ __device__ inline Fc2Layout fc2_layout(int T, int k, int H, int I, bool with_x) {
   Fc2Layout L;
-  L.slot = ((size_t)k * I * 2 + 127) & ~(size_t)127;
-  L.act = ((size_t)T * k * I * 2 + 127) & ~(size_t)127;
+  // the layer kernel's rows are one 16-byte piece longer: a row of I bf16 is a
+  // multiple of 128 bytes, so without it the eight rows an ldmatrix reads would
+  // all start on the same banks
+  const size_t row = (size_t)I * 2 + (with_x ? 16 : 0);
+  L.slot = ((size_t)k * row + 127) & ~(size_t)127;
+  L.act = ((size_t)T * k * row + 127) & ~(size_t)127;
   L.x = with_x ? (size_t)T * H * 4 : 0;
   const size_t cap = with_x ? kLayerSmemMax : kFc2SmemMax;
   const size_t room = cap > L.act + L.x ? cap - L.act - L.x : 0;
@@ -242,14 +246,16 @@ __device__ __forceinline__ const uint4* fc2_row(const GemvParams& P, const int32
 
 // FC2 unit u = c * T + t: the weight rows of the token's valid slots (s_e[q] >= 0)
 // into buf [k][I / 8], asynchronously, by the calling warp.
-__device__ __forceinline__ void fc2_fetch(const GemvParams& P, const int32_t* s_e, long u, uint4* buf) {
+__device__ __forceinline__ void fc2_fetch(const GemvParams& P, const int32_t* s_e, long u, uint4* buf,
+                                          int ld = 0, int j0 = 0, int jstep = 1) {
   const int lane = threadIdx.x & 31, nch = P.I >> 3;
+  if (ld == 0) ld = nch;   // row stride of buf in 16-byte pieces; rows j0, j0 + jstep, ...
   const int c = (int)(u / P.T), t = (int)(u - (long)c * P.T);
-  for (int j = 0; j < P.k; ++j) {
+  for (int j = j0; j < P.k; j += jstep) {
     const int e = s_e[t * P.k + j];
     if (e < 0) continue;
     const uint4* src = P.w2 + ((long)e * P.H + c) * nch;
-    for (int pc = lane; pc < nch; pc += 32) cp_async16(buf + j * nch + pc, src + pc);
+    for (int pc = lane; pc < nch; pc += 32) cp_async16(buf + j * ld + pc, src + pc);
   }
   cp_async_commit();
 }
@@ -282,43 +288,56 @@ __device__ __forceinline__ void fc2_units(const GemvParams& P, const int32_t* s_
   }
 }
 
-// FC2 unit u read straight from global memory (its rows already asked of L2), two
-// of the token's rows at a time, kPieces 16-byte pieces of each in flight per lane.
-__device__ __forceinline__ void fc2_unit_direct(const GemvParams& P, const int32_t* s_pos, const int32_t* s_e,
-                                                const float* s_w, const uint4* act_s, long u) {
-  const int lane = threadIdx.x & 31, nch = P.I >> 3;
-  const int c = (int)(u / P.T), t = (int)(u - (long)c * P.T);
-  const uint4* wc = P.w2 + (long)c * nch + lane;   // this lane's pieces of row c: + e * H * nch + 32 m
-  const long estride = (long)P.H * nch;
-  const uint64_t pol = evict_first_policy();
-  float acc = 0.0f;
-  for (int j = 0; j < P.k; j += 2) {
-    const int q0 = t * P.k + j;
-    const int e0 = s_e[q0], e1 = j + 1 < P.k ? s_e[q0 + 1] : -1;
-    const uint4* a0 = act_s + (long)max(s_pos[q0], 0) * nch + lane;
-    const uint4* a1 = act_s + (long)(j + 1 < P.k ? max(s_pos[q0 + 1], 0) : 0) * nch + lane;
-    float s0 = 0.0f, s1 = 0.0f;
-    for (int m0 = 0; m0 * 32 < nch; m0 += kPieces) {
-      uint4 va[kPieces], vb[kPieces];
-#pragma unroll
-      for (int m = 0; m < kPieces; ++m) {
-        const bool in = (m0 + m) * 32 + lane < nch;
-        if (in && e0 >= 0) va[m] = ld_stream(wc + e0 * estride + (m0 + m) * 32, pol);
-        if (in && e1 >= 0) vb[m] = ld_stream(wc + e1 * estride + (m0 + m) * 32, pol);
-      }
-#pragma unroll
-      for (int m = 0; m < kPieces; ++m) {
-        if ((m0 + m) * 32 + lane < nch) {
-          if (e0 >= 0) s0 = dot8(va[m], a0[(m0 + m) * 32], s0);
-          if (e1 >= 0) s1 = dot8(vb[m], a1[(m0 + m) * 32], s1);
-        }
-      }
+// ---- tensor-core FC2 of the layer kernel ------------------------------------
+// Eight 8x8 bf16 matrices' worth of rows: ldmatrix with one row address per lane.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+// D (16x8, f32) += A (16x16, bf16, row-major) * B (16x8, bf16, column-major).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Steps [s0, s1) of K of the FC2 products of units ua and ub = ua + T (the same
+// token t), whose k weight rows sit in the shared buffers at sa and sb (rows ld
+// pieces apart; the activation rows in act likewise), for experts jb .. jb + 7,
+// by one warp on the tensor cores: A = rows j of unit ua then of unit ub (16 x K),
+// B = the token's activation rows of the same eight experts (K x 8); the products
+// wanted are D's diagonal, D[8h + j][j] = row j of unit h . act row of expert j.
+// Lane 4j + j/2 returns them: [0] for unit ua, [1] for unit ub (expert jb + j).
+__device__ __forceinline__ float2 fc2_pair_mma(const GemvParams& P, const int32_t* s_pos, uint32_t sa,
+                                               uint32_t sb, uint32_t act, int ld, int t, int jb, int s0,
+                                               int s1) {
+  const int lane = threadIdx.x & 31;
+  // A: lane l gives row (l & 15) (rows 8..15 from unit ub) at k half (l >> 4)
+  const int ja = min(jb + (lane & 7), P.k - 1);   // rows past k: any valid row, unused
+  const uint32_t arow = ((lane & 8) ? sb : sa) + (uint32_t)(ja * ld * 16) + (uint32_t)((lane >> 4) * 16);
+  // B: lane l (0..15) gives the activation row of expert jb + (l & 7) at k half (l >> 3) & 1
+  const uint32_t brow = act + (uint32_t)(s_pos[t * P.k + ja] * ld * 16) + (uint32_t)(((lane >> 3) & 1) * 16);
+  float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // even / odd steps
+  for (int st = s0; st < s1; st += 2) {
+    uint32_t a[4], b0, b1;
+    ldsm_x4(arow + st * 32, a);
+    ldsm_x2(brow + st * 32, b0, b1);
+    mma_16816(d0, a, b0, b1);
+    if (st + 1 < s1) {
+      ldsm_x4(arow + (st + 1) * 32, a);
+      ldsm_x2(brow + (st + 1) * 32, b0, b1);
+      mma_16816(d1, a, b0, b1);
     }
-    if (e0 >= 0) acc = fmaf(s_w[q0], s0, acc);
-    if (e1 >= 0) acc = fmaf(s_w[q0 + 1], s1, acc);
   }
-  acc = warp_sum(acc);
-  if (lane == 0) P.out[(long)t * P.H + c] = __float2bfloat16_rn(acc);
+  // D[8h + j][j] sits in lane 4j + j/2, register 2h + (j & 1); in the other lanes: unused
+  const bool odd = (lane >> 2) & 1;   // j & 1 for the lane holding expert j = lane / 4
+  return make_float2(odd ? d0[1] + d1[1] : d0[0] + d1[0], odd ? d0[3] + d1[3] : d0[2] + d1[2]);
 }
 
 // Ask L2 for the 128-byte line holding p.
@@ -328,10 +347,18 @@ __device__ __forceinline__ void prefetch_line_l2(const void* p) {
 
 // Rows [0, n) of the activations (bf16, written by other CTAs or the previous
 // kernel) into shared memory, read through L2.
-__device__ __forceinline__ void stage_act(const GemvParams& P, int n, uint4* act_s) {
+__device__ __forceinline__ void stage_act(const GemvParams& P, int n, uint4* act_s, int ld = 0) {
   const uint4* act = reinterpret_cast<const uint4*>(P.act);
-  const long m = (long)n * (P.I >> 3);
-  for (long x = threadIdx.x; x < m; x += blockDim.x) act_s[x] = __ldcg(act + x);
+  const int nch = P.I >> 3;
+  if (ld == 0 || ld == nch) {
+    const long m = (long)n * nch;
+    for (long x = threadIdx.x; x < m; x += blockDim.x) act_s[x] = __ldcg(act + x);
+  } else {   // rows ld pieces apart
+    for (long x = threadIdx.x; x < (long)n * nch; x += blockDim.x) {
+      const long r = x / nch;
+      act_s[r * ld + (x - r * nch)] = __ldcg(act + x);
+    }
+  }
 }
 
 template <int TT>
@@ -442,8 +469,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_layer_kernel(const Ge
   __shared__ int32_t a_e[kMaxSlots];
   __shared__ int32_t s_pos[kMaxSlots];
   __shared__ float s_w[kMaxSlots];
+  __shared__ float part[kMaxPairs * 4 * 16];
   __shared__ int a_n, go;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = P.T * P.k;
   const Fc2Layout L = fc2_layout(P.T, P.k, P.H, P.I, true);
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lay_raw) + 127) & ~uintptr_t(127));
@@ -466,7 +494,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_layer_kernel(const Ge
   // ---- FC2 weight rows (they do not depend on FC1), requested now so that DRAM
   // streams them together with FC1's: the first unit of each FC2 warp into its
   // buffer, the rows of the CTA's later units into L2
-  if (warp < L.buffers && warp < nloc) fc2_fetch(P, l_idx, u0 + warp, buf);
+  const int ld = (P.I >> 3) + 1;   // row stride of the buffers and activation rows, 16-byte pieces
+  if (warp < L.buffers && warp < nloc) fc2_fetch(P, l_idx, u0 + warp, buf, ld);
   {
     const int lpr = P.I / 64;   // 128-byte lines per row
     const long nl = (long)max(nloc - L.buffers, 0) * P.k * lpr;
@@ -492,15 +521,59 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_layer_kernel(const Ge
   }
   __syncthreads();
   if (!go) return;
-  stage_act(P, S, act_s);
+  stage_act(P, S, act_s, ld);
   __syncthreads();
-  // ---- FC2: the buffered first units, and meanwhile the later units (rows in L2)
-  // by the warps without a buffer
-  if (warp < L.buffers) {
-    fc2_units(P, s_pos, l_idx, s_w, act_s, buf, u0, min(nloc, L.buffers), L.buffers);
-  } else {
-    for (int i = L.buffers + (warp - L.buffers); i < nloc; i += kLayerWarps - L.buffers)
-      fc2_unit_direct(P, s_pos, l_idx, s_w, act_s, u0 + i);
+  // ---- FC2 on the tensor cores, in rounds of L.buffers units (unit r0 + b in
+  // buffer b): the pairs of units (b, b + T) of one token, each pair by four warps
+  // (a quarter of K each), which own the pair's two buffers: after a round they
+  // refill them with the pair's units of the next round (rows asked of L2 at the
+  // start) while the other pairs compute.
+  const int B = L.buffers, T2 = 2 * P.T;
+  const int npairs = (B + T2 - 1) / T2 * P.T;
+  const int pr = warp >> 2, qw = warp & 3;       // pair of this warp, its quarter
+  const int ksteps = (P.I >> 3) >> 1;            // 16 bf16 per step
+  if (pr < npairs && pr < kMaxPairs) {
+    const int b0 = pr / P.T * T2 + pr % P.T, b1 = b0 + P.T;
+    uint4* buf0 = reinterpret_cast<uint4*>(base + (size_t)b0 * L.slot);
+    uint4* buf1 = reinterpret_cast<uint4*>(base + (size_t)b1 * L.slot);
+    const int s0 = ksteps * qw / 4, s1 = ksteps * (qw + 1) / 4;
+    float* dg = part + pr * 4 * 16;              // [quarter][h * 8 + j]
+    for (int r0 = 0; r0 < nloc && b0 < B; r0 += B) {
+      const int nr = min(B, nloc - r0);
+      if (b0 >= nr) break;
+      const bool two = b1 < nr;
+      const long ua = u0 + r0 + b0;
+      const int t = (int)(ua % P.T);
+      if (r0 > 0) {   // rows qw, qw + 4, ... of both units
+        fc2_fetch(P, l_idx, ua, buf0, ld, qw, 4);
+        if (two) fc2_fetch(P, l_idx, ua + P.T, buf1, ld, qw, 4);
+        cp_async_wait_all();
+        ptx::named_bar_sync(1 + pr, 128);
+      }
+      float acc0 = 0.0f, acc1 = 0.0f;
+      for (int jb = 0; jb < P.k; jb += 8) {
+        const float2 d = fc2_pair_mma(P, s_pos, ptx::smem_u32(buf0), ptx::smem_u32(two ? buf1 : buf0),
+                                      ptx::smem_u32(act_s), ld, t, jb, s0, s1);
+        const int j = lane >> 2;
+        if ((lane & 3) == (j >> 1)) {   // lane 4j + j/2 holds expert j's products
+          dg[qw * 16 + j] = d.x;
+          dg[qw * 16 + 8 + j] = d.y;
+        }
+        ptx::named_bar_sync(1 + pr, 128);
+        if (qw == 0 && lane == 0)
+          for (int jj = 0; jj < 8 && jb + jj < P.k; ++jj) {
+            const float w = s_w[t * P.k + jb + jj];
+            acc0 = fmaf(w, (dg[jj] + dg[16 + jj]) + (dg[32 + jj] + dg[48 + jj]), acc0);
+            acc1 = fmaf(w, (dg[8 + jj] + dg[24 + jj]) + (dg[40 + jj] + dg[56 + jj]), acc1);
+          }
+        ptx::named_bar_sync(1 + pr, 128);   // dg and the buffers are free again
+      }
+      if (qw == 0 && lane == 0) {
+        const int ca = (int)(ua / P.T);
+        P.out[(long)t * P.H + ca] = __float2bfloat16_rn(acc0);
+        if (two) P.out[(long)t * P.H + ca + 1] = __float2bfloat16_rn(acc1);
+      }
+    }
   }
 }
 
