@@ -180,16 +180,17 @@ __device__ __forceinline__ void active_experts(const int32_t* counts, int E, int
   if (lane == 0) *a_n = min(n, kMaxSlots);
 }
 
-// FC1 units [u0, u1) (unit u = a * I + i), taken in turn by the block's warps.
+// FC1 units u0, u0 + ustride, ... < u1 (unit u = a * I + i), taken in turn by the
+// block's warps.
 // TT: most tokens an expert can have (the batch size bound).
 template <int TT, int PIECES = kPieces>
 __device__ __forceinline__ void fc1_units(const GemvParams& P, const float4* xs, const int32_t* a_e,
                                           const int32_t* counts, const int32_t* offsets,
-                                          const int32_t* sorted_ids, long u0, long u1) {
+                                          const int32_t* sorted_ids, long u0, long u1, long ustride = 1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int nch = P.H >> 3;
   const uint64_t pol = evict_first_policy();
-  for (long u = u0 + warp; u < u1; u += nwarps) {
+  for (long u = u0 + warp * ustride; u < u1; u += nwarps * ustride) {
     const int a = (int)(u / P.I), i = (int)(u - (long)a * P.I);
     const int e = a_e[a];
     const int cnt = min(counts[e], TT);
@@ -507,7 +508,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_layer_kernel(const Ge
   }
   // ---- FC1
   const long U1 = (long)a_n * P.I;
-  fc1_units<TT>(P, xs, a_e, l_cnt, l_off, l_ids, U1 * blockIdx.x / G, U1 * (blockIdx.x + 1) / G);
+  fc1_units<TT>(P, xs, a_e, l_cnt, l_off, l_ids, blockIdx.x, U1, G);   // units b, b + G, ... of CTA b
   // ---- the routing kernel is complete (barrier counter zeroed, routing weights
   // written); then every CTA's activations
   pdl_wait();
