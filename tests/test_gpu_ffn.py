@@ -88,11 +88,13 @@ def test_layer_decode_shapes(T, H, I, E, k, norm):
 # matrix-vector path (bf16, T <= 2): rows longer than one round of a warp's pieces (H > 2048),
 # piece counts that are not a multiple of 32 (I = 1408, 448), rows of only 8 pieces
 # (H = I = 64), experts shared by both tokens, routing inside each CTA (E <= 64) and from
-# the routing kernel (E > 64), 64 slots (k = 32)
+# the routing kernel (E > 64), 64 slots (k = 32); in the one-kernel form, output columns
+# enough for many rounds of FC2 buffers per CTA (H = 8192 / 4096) and an odd H / 64
 @pytest.mark.parametrize("T,H,I,E,k,norm", [
     (1, 2112, 1408, 4, 4, True), (2, 2112, 448, 4, 3, False), (1, 64, 64, 8, 8, True),
     (2, 64, 192, 3, 3, True), (2, 256, 128, 100, 8, True), (2, 128, 128, 64, 32, False),
-    (1, 128, 320, 200, 32, True),
+    (1, 128, 320, 200, 32, True), (1, 8192, 64, 4, 2, True), (2, 4096, 128, 8, 5, False),
+    (1, 4160, 192, 16, 9, True),
 ])
 def test_layer_matrix_vector_shapes(T, H, I, E, k, norm):
     moe = need_gpu()
