@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
     const float* logits, int T, int E, int k, int norm, float* w_out, int32_t* idx_out,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
-  extern __shared__ int sm[];
+  extern __shared__ __align__(16) int sm[];
   pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
   if (clear && threadIdx.x == 0) *clear = 0;
   float* col = reinterpret_cast<float*>(sm);

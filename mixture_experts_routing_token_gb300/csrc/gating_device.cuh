@@ -227,27 +227,25 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
 
 // ---- thread-per-token top-k over rows parked in shared memory (E <= EP <= 128)
 //
-// A block of up to kStageRows rows is stored column-major, element e of row r at
-// col[e * kStageLd + r] (padded stride: the selection's reads, a warp's lanes
-// reading one expert of consecutive rows, are bank-conflict free); the thread of
-// row r selects with the tournament of topk_staged_row.
+// A block of up to kStageRows rows is stored in 16-byte chunks: chunk q of row r
+// (its elements q*VE .. q*VE + VE - 1, VE = 16 / sizeof(St)) sits at chunk index
+// q * kStageLd + r. The padded stride makes both access patterns bank-conflict
+// free per quarter warp: the staging writes (8 lanes, 8 consecutive chunks of one
+// row) and the passes over a row (8 lanes, the same chunk of consecutive rows),
+// so each is one 16-byte access per lane instead of VE scalar ones. The thread
+// of row r selects with the tournament of topk_staged_row.
 // Weights as in gate_one_token.
 constexpr int kStageRows = 128;
 constexpr int kStageLd = kStageRows + 1;
 
+// Elements of a stage element type per 16-byte chunk.
+template <typename St>
+__host__ __device__ constexpr int chunk_elems() { return 16 / (int)sizeof(St); }
+
 // Element e of staged row r.
 template <typename St>
-__host__ __device__ constexpr int sofs(int e, int r) { return e * kStageLd + r; }
-
-// Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into col[EP][kStageLd],
-// experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows); the
-// caller synchronises before reading. Each thread issues U 16-byte loads before
-// it stores any of them; with U = the vectors per thread of a full stage
-// (kStageBatch<EP, In>(nthr)), a whole stage is one round trip to memory.
-template <int EP, typename In>
-__host__ __device__ constexpr int kStageBatch(int nthr) {
-  const int per = EP * kStageRows / (16 / (int)sizeof(In)) / nthr;
-  return per < 1 ? 1 : (per > 32 ? 32 : per);
+__host__ __device__ constexpr int sofs(int e, int r) {
+  return ((e / chunk_elems<St>()) * kStageLd + r) * chunk_elems<St>() + e % chunk_elems<St>();
 }
 
 // Staged logits are kept as float32, or for bf16 logits as their 16-bit
@@ -257,72 +255,63 @@ __device__ __forceinline__ float st_get(const float* p) { return *p; }
 __device__ __forceinline__ float st_get(const uint16_t* p) { return __uint_as_float((uint32_t)*p << 16); }
 __device__ __forceinline__ void st_neg_inf(float* p) { *p = -INFINITY; }
 __device__ __forceinline__ void st_neg_inf(uint16_t* p) { *p = 0xff80u; }   // bf16 -inf
-
-// One 16-byte vector of logits (4 float32 or 8 bf16) into row r, experts e0.., of the stage.
-__device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, float) {
-  col[sofs<float>(e0, r)] = __uint_as_float(q.x);
-  col[sofs<float>(e0 + 1, r)] = __uint_as_float(q.y);
-  col[sofs<float>(e0 + 2, r)] = __uint_as_float(q.z);
-  col[sofs<float>(e0 + 3, r)] = __uint_as_float(q.w);
-}
-__device__ __forceinline__ void put_vec(float* col, int e0, int r, const uint4& q, __nv_bfloat16) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    col[sofs<float>(e0 + 2 * i, r)] = lo_bf16(w[i]);
-    col[sofs<float>(e0 + 2 * i + 1, r)] = hi_bf16(w[i]);
-  }
-}
-__device__ __forceinline__ void put_vec(uint16_t* col, int e0, int r, const uint4& q, __nv_bfloat16) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    col[sofs<uint16_t>(e0 + 2 * i, r)] = (uint16_t)(w[i] & 0xffffu);
-    col[sofs<uint16_t>(e0 + 2 * i + 1, r)] = (uint16_t)(w[i] >> 16);
-  }
-}
 __device__ __forceinline__ void put_one(float* p, const float* src) { *p = __ldg(src); }
 __device__ __forceinline__ void put_one(float* p, const __nv_bfloat16* src) { *p = load_logit(src); }
 __device__ __forceinline__ void put_one(uint16_t* p, const __nv_bfloat16* src) {
   *p = __ldg(reinterpret_cast<const unsigned short*>(src));
 }
 
+// 16-byte global -> shared copy without a register round trip (L2 only).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into the chunked stage,
+// experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows, a
+// multiple of 32); the caller synchronises before reading. With 16-byte rows
+// vectors (E a multiple of 4 float32 / 8 bf16 logits) a warp moves tiles of 4
+// rows x 8 vectors (4 full 128-byte segments of global memory): by cp.async when
+// a vector is one stage chunk (all of a thread's copies in flight at once), else
+// (bf16 widened to float32) through registers, U vectors per round trip.
 template <int EP, typename In = float, int U = 8, typename St = float>
 __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t0, int nt, int E,
                                            St* col, int tid, int nthr) {
   constexpr int VEC = 16 / (int)sizeof(In);   // logits per 16-byte vector
-  const In* blk = logits + t0 * (long)E;   // the block's rows are contiguous: coalesced loads
+  const In* blk = logits + t0 * (long)E;   // the block's rows are contiguous
   if (E % VEC == 0) {
     const int R = E / VEC;                   // vectors per row
     const uint4* src = reinterpret_cast<const uint4*>(blk);
-    if (nthr % R == 0) {
-      // every vector of this thread is column c of a row: no division per vector
-      const int c = tid % R, e0 = c * VEC, dr = nthr / R;
-      for (int r0 = tid / R; r0 < nt; r0 += U * dr) {
-        uint4 q[U];
+    const int lane = tid & 31, w = tid >> 5, nw = nthr >> 5;
+    const int nrt = (nt + 3) >> 2;           // tiles of 4 rows
+    if constexpr (sizeof(In) == sizeof(St)) {
+      uint4* dst = reinterpret_cast<uint4*>(col);
+      for (int c = lane & 7; c < ((R + 7) & ~7); c += 8)
+        for (int rt = w; rt < nrt; rt += nw) {
+          const int r = 4 * rt + (lane >> 3);
+          if (c < R && r < nt) cp_async16(dst + c * kStageLd + r, src + r * R + c);
+        }
+      cp_async_wait_all();
+    } else {   // 8 bf16 -> two float32 chunks
+      float4* dst = reinterpret_cast<float4*>(col);
+      for (int c = lane & 7; c < ((R + 7) & ~7); c += 8)
+        for (int rt0 = w; rt0 < nrt; rt0 += U * nw) {
+          uint4 q[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (r0 + u * dr < nt) q[u] = __ldg(src + (r0 + u * dr) * R + c);
+          for (int u = 0; u < U; ++u) {
+            const int r = 4 * (rt0 + u * nw) + (lane >> 3);
+            if (c < R && r < nt) q[u] = __ldg(src + r * R + c);
+          }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (r0 + u * dr < nt) put_vec(col, e0, r0 + u * dr, q[u], In());
-      }
-    } else {
-      const int n = nt * R;
-      for (int f0 = tid; f0 < n; f0 += U * nthr) {
-        uint4 q[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (f0 + u * nthr < n) q[u] = __ldg(src + f0 + u * nthr);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int f = f0 + u * nthr;
-          if (f < n) {
-            const int r = (int)((uint32_t)f / (uint32_t)R);
-            put_vec(col, (f - r * R) * VEC, r, q[u], In());
+          for (int u = 0; u < U; ++u) {
+            const int r = 4 * (rt0 + u * nw) + (lane >> 3);
+            if (c < R && r < nt) {
+              dst[(2 * c) * kStageLd + r] = make_float4(lo_bf16(q[u].x), hi_bf16(q[u].x), lo_bf16(q[u].y), hi_bf16(q[u].y));
+              dst[(2 * c + 1) * kStageLd + r] = make_float4(lo_bf16(q[u].z), hi_bf16(q[u].z), lo_bf16(q[u].w), hi_bf16(q[u].w));
+            }
           }
         }
-      }
     }
   } else {
     for (int f = tid; f < nt * E; f += nthr) {
@@ -334,13 +323,26 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
     for (int e = E; e < EP; ++e) st_neg_inf(col + sofs<St>(e, tid));
 }
 
-// Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: the
-// rows [EP][kStageLd] of St, then (4-byte aligned) the float maxima of their
-// groups of 8 [EP / 8][kStageLd].
+// The 8 staged values of group g (experts 8g .. 8g + 7) of row r: two float32
+// chunks, or one chunk of 16-bit patterns.
+__device__ __forceinline__ void load_group8(const float* col, int g, int r, float (&x)[8]) {
+  const float4* c4 = reinterpret_cast<const float4*>(col);
+  const float4 a = c4[(2 * g) * kStageLd + r], b = c4[(2 * g + 1) * kStageLd + r];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load_group8(const uint16_t* col, int g, int r, float (&x)[8]) {
+  const uint4 q = reinterpret_cast<const uint4*>(col)[g * kStageLd + r];
+  x[0] = lo_bf16(q.x); x[1] = hi_bf16(q.x); x[2] = lo_bf16(q.y); x[3] = hi_bf16(q.y);
+  x[4] = lo_bf16(q.z); x[5] = hi_bf16(q.z); x[6] = lo_bf16(q.w); x[7] = hi_bf16(q.w);
+}
+
+// Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: EP / VE
+// chunk columns of kStageLd 16-byte chunks, then (RM false) the float maxima of
+// the rows' groups of 8 [EP / 8][kStageLd].
 template <int EP, typename St = float>
-__host__ __device__ constexpr int stage_rows_bytes() { return (EP * kStageLd * (int)sizeof(St) + 3) / 4 * 4; }
-template <int EP, typename St = float>
-__host__ __device__ constexpr int stage_bytes() { return stage_rows_bytes<EP, St>() + EP / 8 * kStageLd * 4; }
+__host__ __device__ constexpr int stage_rows_bytes() { return EP * kStageLd * (int)sizeof(St); }
+template <int EP, typename St = float, bool RM = false>
+__host__ __device__ constexpr int stage_bytes() { return stage_rows_bytes<EP, St>() + (RM ? 0 : EP / 8 * kStageLd * 4); }
 template <int EP>
 __host__ __device__ constexpr int stage_floats() { return stage_bytes<EP, float>() / 4; }
 
@@ -348,47 +350,50 @@ __host__ __device__ constexpr int stage_floats() { return stage_bytes<EP, float>
 // s_w / s_idx (shared memory, indexed like the outputs) the results are also kept
 // there.
 //
-// Selection is a two-level tournament over groups of 8 experts: the group maxima
-// live in shared memory after the rows, the maxima of 4 consecutive groups
-// ("supers") in registers. A round takes the largest super, then its first group
-// holding that value, then the group's first expert holding it (scans in
+// Selection is a tournament over groups of 8 experts. A round finds the largest
+// group maximum and its first group holding it, reads that group's 8 values (one
+// or two 16-byte reads), takes its first expert holding the value (scans in
 // ascending index, so equal values go to the lower expert, as the page's strict
-// '>' does), marks that expert taken (-inf; logits are finite) and refreshes its
-// group's and super's maxima. Every choice is a select, not a branch: all threads
-// of a warp run the same instructions.
+// '>' does), marks it taken (-inf; logits are finite) and refreshes the group's
+// maximum. RM true: the group maxima live in registers and the first group is
+// found by an arg-max tree (a right node wins only when strictly larger); the
+// group read is the round's only shared-memory round trip (measured faster for
+// float32 rows of 128 experts, which are latency-bound at 3 blocks per SM).
+// RM false: the group maxima live in shared memory after the rows and the maxima
+// of 4 consecutive groups ("supers") in registers (fewer instructions: faster
+// where the kernel is issue-bound, the norm = False exponentials and 16-bit
+// stages). Every choice is a select, not a branch: all threads of a warp run the
+// same instructions.
 //
 // TO_COL (k <= kRegSel): instead of w_out / idx_out, the results go to the row's
-// own column: weight j and index j (bits) to slots j and kRegSel + j of a float
-// column, or as 16-bit halves to slots 2j, 2j+1 and 2 kRegSel + 2j, +1 of a
-// 16-bit column.
-template <int EP, bool TO_COL = false, typename St = float>
+// own first four chunks (its logits are no longer needed): weight j and index j
+// (bits) as the 32-bit words j and kRegSel + j, word s being word s % 4 of chunk
+// s / 4 for either element type.
+template <int EP, bool TO_COL = false, typename St = float, bool RM = false>
 __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, int k, int norm,
                                                 float* __restrict__ w_out, int32_t* __restrict__ idx_out,
                                                 float* s_w = nullptr, int32_t* s_idx = nullptr) {
   constexpr bool kHalf = sizeof(St) == 2;
   static_assert(!TO_COL || EP >= (kHalf ? 4 : 2) * kRegSel, "room for the parked results");
   constexpr int G = EP / 8;          // groups of 8 experts
-  constexpr int S = (G + 3) / 4;     // supers of 4 groups
-  float* gcol = reinterpret_cast<float*>(reinterpret_cast<char*>(col) + stage_rows_bytes<EP, St>());
+  static_assert((G & (G - 1)) == 0, "a power-of-two number of groups");
+  constexpr int S = (G + 3) / 4;     // supers of 4 groups (RM false)
   auto at = [&](int i) -> float { return st_get(col + sofs<St>(i, r)); };
+  float* gcol = reinterpret_cast<float*>(reinterpret_cast<char*>(col) + stage_rows_bytes<EP, St>());
   auto gat = [&](int g) -> float& { return gcol[g * kStageLd + r]; };
-  auto put32 = [&](int slot, uint32_t v) {   // a 32-bit result into parking slot `slot`
-    if constexpr (kHalf) {
-      col[sofs<St>(2 * slot, r)] = (St)(v & 0xffffu);
-      col[sofs<St>(2 * slot + 1, r)] = (St)(v >> 16);
-    } else {
-      col[sofs<St>(slot, r)] = __uint_as_float(v);
-    }
-  };
+  float gmx[RM ? G : 1];
   float sm[S];
 #pragma unroll
   for (int q = 0; q < S; ++q) sm[q] = -INFINITY;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float x = at(8 * g);
+    float y[8];
+    load_group8(col, g, r, y);
+    float x = y[0];
 #pragma unroll
-    for (int c = 1; c < 8; ++c) x = fmaxf(x, at(8 * g + c));
-    gat(g) = x;
+    for (int c = 1; c < 8; ++c) x = fmaxf(x, y[c]);
+    if constexpr (RM) gmx[g] = x;
+    else gat(g) = x;
     sm[g / 4] = fmaxf(sm[g / 4], x);
   }
   float m = sm[0];
@@ -398,6 +403,12 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
   if (!norm) {   // four independent compensated sums (a quarter of the dependent chain), then merged
     float h[4] = {0.0f, 0.0f, 0.0f, 0.0f}, l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int i = 0;
+    for (; i + 8 <= E; i += 8) {   // whole groups: one or two 16-byte reads
+      float y[8];
+      load_group8(col, i / 8, r, y);
+#pragma unroll
+      for (int a = 0; a < 8; ++a) two_sum_add(h[a & 3], l[a & 3], exp_diff_fast(y[a], m));
+    }
     for (; i + 4 <= E; i += 4) {
 #pragma unroll
       for (int a = 0; a < 4; ++a) two_sum_add(h[a], l[a], exp_diff_fast(at(i + a), m));
@@ -411,22 +422,37 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
   }
   // one round: the largest remaining value and its lowest expert; refreshes the maxima
   auto take = [&](float& v, int& e) {
-    v = sm[0];
-#pragma unroll
-    for (int q = 1; q < S; ++q) v = fmaxf(v, sm[q]);
-    int bs = 0;
-#pragma unroll
-    for (int q = S - 1; q >= 0; --q) bs = sm[q] == v ? q : bs;
+    int bg, bs = 0, bi = 0;
     float gv[4];
+    if constexpr (RM) {
+      float tv[G];
+      int ti[G];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) gv[i] = (G % 4 == 0 || 4 * bs + i < G) ? gat(4 * bs + i) : -INFINITY;
-    int bi = 0;
+      for (int g = 0; g < G; ++g) { tv[g] = gmx[g]; ti[g] = g; }
 #pragma unroll
-    for (int i = 3; i >= 0; --i) bi = gv[i] == v ? i : bi;
-    const int bg = 4 * bs + bi;
+      for (int w = 1; w < G; w *= 2)
+#pragma unroll
+        for (int g = 0; g + w < G; g += 2 * w) {
+          const bool right = tv[g + w] > tv[g];
+          tv[g] = right ? tv[g + w] : tv[g];
+          ti[g] = right ? ti[g + w] : ti[g];
+        }
+      v = tv[0];
+      bg = ti[0];
+    } else {
+      v = sm[0];
+#pragma unroll
+      for (int q = 1; q < S; ++q) v = fmaxf(v, sm[q]);
+#pragma unroll
+      for (int q = S - 1; q >= 0; --q) bs = sm[q] == v ? q : bs;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gv[i] = (G % 4 == 0 || 4 * bs + i < G) ? gat(4 * bs + i) : -INFINITY;
+#pragma unroll
+      for (int i = 3; i >= 0; --i) bi = gv[i] == v ? i : bi;
+      bg = 4 * bs + bi;
+    }
     float x[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) x[c] = at(8 * bg + c);
+    load_group8(col, bg, r, x);
     int bc = 0;
 #pragma unroll
     for (int c = 7; c >= 0; --c) bc = x[c] == v ? c : bc;
@@ -435,12 +461,17 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
     float nm = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 8; ++c) nm = fmaxf(nm, c == bc ? -INFINITY : x[c]);
-    gat(bg) = nm;
-    float ns = -INFINITY;
+    if constexpr (RM) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ns = fmaxf(ns, i == bi ? nm : gv[i]);
+      for (int g = 0; g < G; ++g) gmx[g] = g == bg ? nm : gmx[g];
+    } else {
+      gat(bg) = nm;
+      float ns = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < S; ++q) sm[q] = q == bs ? ns : sm[q];
+      for (int i = 0; i < 4; ++i) ns = fmaxf(ns, i == bi ? nm : gv[i]);
+#pragma unroll
+      for (int q = 0; q < S; ++q) sm[q] = q == bs ? ns : sm[q];
+    }
   };
   if (TO_COL || k <= kRegSel) {   // the selected logits stay in registers until the weights are formed
     float sel[kRegSel], ex[kRegSel];
@@ -454,41 +485,51 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
       }
     }
     const float denom = hi + lo;
+    if constexpr (TO_COL) {
+      uint32_t pw[2 * kRegSel];
 #pragma unroll
-    for (int j = 0; j < kRegSel; ++j)
-      if (j < k) {
-        const float wj = __fdiv_rn(ex[j], denom);
-        if (TO_COL) {
-          put32(j, __float_as_uint(wj));
-          put32(kRegSel + j, (uint32_t)sid[j]);
-        } else {
+      for (int j = 0; j < kRegSel; ++j) {
+        pw[j] = j < k ? __float_as_uint(__fdiv_rn(ex[j], denom)) : 0u;
+        pw[kRegSel + j] = j < k ? (uint32_t)sid[j] : 0u;
+      }
+      uint4* c4 = reinterpret_cast<uint4*>(col);
+#pragma unroll
+      for (int h = 0; h < 2 * kRegSel / 4; ++h)
+        c4[h * kStageLd + r] = make_uint4(pw[4 * h], pw[4 * h + 1], pw[4 * h + 2], pw[4 * h + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRegSel; ++j)
+        if (j < k) {
+          const float wj = __fdiv_rn(ex[j], denom);
           w_out[t * k + j] = wj;
           idx_out[t * k + j] = sid[j];
           if (s_w) s_w[t * k + j] = wj;
           if (s_idx) s_idx[t * k + j] = sid[j];
         }
-      }
+    }
     return;
   }
-  for (int j = 0; j < k; ++j) {
-    float bv;
-    int bi;
-    take(bv, bi);
-    if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
-    idx_out[t * k + j] = bi;
-    if (s_w) {
-      s_idx[t * k + j] = bi;
-      s_w[t * k + j] = bv;
-    } else {
-      w_out[t * k + j] = bv;
+  if constexpr (!TO_COL) {   // k > kRegSel: the weights are formed in place after the k rounds
+    for (int j = 0; j < k; ++j) {
+      float bv;
+      int bi;
+      take(bv, bi);
+      if (norm) two_sum_add(hi, lo, exp_diff(bv, m));
+      idx_out[t * k + j] = bi;
+      if (s_w) {
+        s_idx[t * k + j] = bi;
+        s_w[t * k + j] = bv;
+      } else {
+        w_out[t * k + j] = bv;
+      }
     }
-  }
-  const float denom = hi + lo;
-  for (int j = 0; j < k; ++j) {
-    const float x = s_w ? s_w[t * k + j] : w_out[t * k + j];
-    const float wj = __fdiv_rn(exp_diff(x, m), denom);
-    w_out[t * k + j] = wj;
-    if (s_w) s_w[t * k + j] = wj;
+    const float denom = hi + lo;
+    for (int j = 0; j < k; ++j) {
+      const float x = s_w ? s_w[t * k + j] : w_out[t * k + j];
+      const float wj = __fdiv_rn(exp_diff(x, m), denom);
+      w_out[t * k + j] = wj;
+      if (s_w) s_w[t * k + j] = wj;
+    }
   }
 }
 

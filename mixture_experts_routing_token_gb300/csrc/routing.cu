@@ -39,13 +39,17 @@ constexpr int kSmemGateThreads = gate::kStageRows;
 // Staged as 16-bit patterns: bf16 logits with at least 64 experts.
 template <int EP, typename In>
 using StageT = typename std::conditional<!std::is_same<In, float>::value && EP >= 64, uint16_t, float>::type;
+// Group maxima in registers (gate::topk_staged_row): float32 rows of up to 128 experts.
+template <int EP, typename In>
+constexpr bool kRegMax = std::is_same<StageT<EP, In>, float>::value && EP == 128;
 
 template <int EP, typename In, int U = 8>
 __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
     const In* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
     int32_t* __restrict__ idx_out) {
   using St = StageT<EP, In>;
-  extern __shared__ __align__(16) uint8_t stage_raw[];   // gate::stage_bytes<EP, St>()
+  constexpr bool RM = kRegMax<EP, In>;
+  extern __shared__ __align__(16) uint8_t stage_raw[];   // gate::stage_bytes<EP, St, RM>()
   St* col = reinterpret_cast<St*>(stage_raw);
   const int tid = threadIdx.x;
   const long t0 = (long)blockIdx.x * kSmemGateThreads;
@@ -53,19 +57,26 @@ __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
   gate::stage_rows<EP, In, U, St>(logits, t0, nt, E, col, tid, kSmemGateThreads);
   __syncthreads();
   if (k > gate::kRegSel) {
-    if (tid < nt) gate::topk_staged_row<EP, false, St>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
+    if (tid < nt) gate::topk_staged_row<EP, false, St, RM>(col, tid, t0 + tid, E, k, norm, w_out, idx_out);
     return;
   }
   // Each thread touches only its own row's column, so it parks its k weights and
   // indices there; after the barrier the block writes its rows' outputs out
   // contiguously.
-  if (tid < nt) gate::topk_staged_row<EP, true, St>(col, tid, tid, E, k, norm, nullptr, nullptr);
+  if (tid < nt) gate::topk_staged_row<EP, true, St, RM>(col, tid, tid, E, k, norm, nullptr, nullptr);
   __syncthreads();
-  auto get32 = [&](int slot, int r) -> uint32_t {
-    if constexpr (sizeof(St) == 2)
-      return (uint32_t)col[gate::sofs<St>(2 * slot, r)] | ((uint32_t)col[gate::sofs<St>(2 * slot + 1, r)] << 16);
-    else
-      return __float_as_uint(col[gate::sofs<St>(slot, r)]);
+  if (k == 8 || k == 4) {   // whole 16-byte chunks: weights words 0..k-1, indices words 8..8+k-1
+    const uint4* c4 = reinterpret_cast<const uint4*>(col);
+    const int hs = k >> 3;   // chunks per row's weights, minus one
+    for (int f = tid; f < (nt << hs); f += kSmemGateThreads) {
+      const int r = f >> hs, h = f & hs;
+      reinterpret_cast<uint4*>(w_out + (t0 + r) * k)[h] = c4[h * gate::kStageLd + r];
+      reinterpret_cast<uint4*>(idx_out + (t0 + r) * k)[h] = c4[(2 + h) * gate::kStageLd + r];
+    }
+    return;
+  }
+  auto get32 = [&](int slot, int r) -> uint32_t {   // word `slot` of the row's parking chunks
+    return reinterpret_cast<const uint32_t*>(col)[((slot >> 2) * gate::kStageLd + r) * 4 + (slot & 3)];
   };
   const int n = nt * k;
   const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // row of output f: f >> kshift, or f / k
@@ -79,7 +90,7 @@ __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
 template <int EP, typename In>
 int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
-  const size_t smem = (size_t)gate::stage_bytes<EP, StageT<EP, In>>();
+  const size_t smem = (size_t)gate::stage_bytes<EP, StageT<EP, In>, kRegMax<EP, In>>();
   if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
   gating_smem_kernel<EP, In><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
       logits, T, E, k, norm, w, idx);
@@ -477,8 +488,16 @@ __global__ void __launch_bounds__(kBlock) group_topk_lane_smem_kernel(
     const float* row = scores + t * (long)E + base;
     float b1 = -FLT_MAX, b2 = -FLT_MAX;
     if (has && (gs & 3) == 0) {
-      for (int q = 0; q < gs / 4; ++q) {
-        float4 x = __ldg(reinterpret_cast<const float4*>(row) + q);
+      // all of the group's vectors (gs <= 32: at most 8) are requested before the
+      // first is used: one memory round trip per token instead of one per vector
+      float4 xq[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < gs / 4) xq[q] = __ldg(reinterpret_cast<const float4*>(row) + q);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (q >= gs / 4) break;
+        float4 x = xq[q];
         if (noaux) {
           const float4 b = __ldg(reinterpret_cast<const float4*>(bias + base) + q);
           x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
@@ -575,6 +594,169 @@ __global__ void __launch_bounds__(kBlock) group_topk_lane_smem_kernel(
       }
     }
   }
+}
+
+// Groups of exactly 32 experts (DeepSeek-V3: 8 groups of 32), L >= n_group lanes
+// per token, lane g owning group g. The token's lanes read its row as
+// consecutive 16-byte vectors (a warp instruction covers whole 128-byte lines),
+// add the bias from a padded shared-memory copy and drop each vector into the
+// parked row of the lane owning its group (36-float rows: every 16-byte access
+// pattern below is conflict-free per quarter warp). Each lane then reads its
+// group back as 16-byte vectors, forms the group score and the maxima of its
+// four sub-groups of 8 in one pass, and the selection runs as in
+// group_topk_lane_smem_kernel, with absent or taken candidates as (-inf, kNone)
+// so a merge step is two compares.
+constexpr int kG32Ld = 36;
+
+__device__ __forceinline__ bool g32_better(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+template <int L>
+__global__ void __launch_bounds__(kBlock) group_topk_g32_kernel(
+    const float* __restrict__ scores, const float* __restrict__ bias, int T, int E, int k, int n_group,
+    int topk_group, int noaux, float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  __shared__ __align__(16) float park[kBlock * kG32Ld];
+  __shared__ __align__(16) float sbias[32 * kG32Ld];
+  const int g = threadIdx.x & (L - 1);
+  const unsigned gm = group_mask<L>();
+  const bool has = g < n_group;
+  const int nv = E >> 2;   // 16-byte vectors per row, 8 per group
+  for (int f = threadIdx.x; f < n_group * 32; f += kBlock)
+    sbias[(f >> 5) * kG32Ld + (f & 31)] = noaux ? __ldg(bias + f) : 0.0f;
+  __syncthreads();
+  float* my = park + threadIdx.x * kG32Ld;
+  float* tp = park + (threadIdx.x & ~(L - 1)) * kG32Ld;   // the token's first parked row
+  const long step = (long)gridDim.x * (kBlock / L);
+  for (long t = (long)blockIdx.x * (kBlock / L) + threadIdx.x / L; t < T; t += step) {
+    const float4* row4 = reinterpret_cast<const float4*>(scores + t * (long)E);
+    float4 xq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (g + L * i < nv) xq[i] = __ldg(row4 + g + L * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = g + L * i;
+      if (v < nv) {
+        const int at = (v >> 3) * kG32Ld + (v & 7) * 4;
+        float4 x = xq[i];
+        if (noaux) {
+          const float4 b = *reinterpret_cast<const float4*>(sbias + at);
+          x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+        }
+        *reinterpret_cast<float4*>(tp + at) = x;
+      }
+    }
+    __syncwarp(gm);
+    // group score (max, or the float32 sum of the two largest) and sub-group maxima
+    float b1 = -FLT_MAX, b2 = -FLT_MAX;
+    float sv[4];
+    int si[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sv[q] = -INFINITY;
+      si[q] = kNone;
+    }
+    if (has) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 a = *reinterpret_cast<const float4*>(my + 8 * q);
+        const float4 c = *reinterpret_cast<const float4*>(my + 8 * q + 4);
+        const float x[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        float v = x[0];
+        int i0 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j > 0) {
+            i0 = x[j] > v ? j : i0;
+            v = fmaxf(v, x[j]);
+          }
+          const float lo = fminf(b1, x[j]);
+          b1 = fmaxf(b1, x[j]);
+          b2 = fmaxf(b2, lo);
+        }
+        sv[q] = v;
+        si[q] = 32 * g + 8 * q + i0;
+      }
+    }
+    const float gscore = noaux ? b1 + b2 : b1;
+    unsigned gsel = 0;
+    for (int j = 0; j < topk_group; ++j) {
+      const bool avail = has && !((gsel >> g) & 1u);
+      float bv = avail ? gscore : -INFINITY;
+      int bi = avail ? g : kNone;
+#pragma unroll
+      for (int off = L / 2; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(gm, bv, off, L);
+        const int oi = __shfl_xor_sync(gm, bi, off, L);
+        const bool b = g32_better(ov, oi, bv, bi);
+        bv = b ? ov : bv;
+        bi = b ? oi : bi;
+      }
+      gsel |= 1u << bi;
+    }
+    if (!(has && ((gsel >> g) & 1u))) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sv[q] = -INFINITY;
+        si[q] = kNone;
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      float bv = sv[0];
+      int bi = si[0];
+#pragma unroll
+      for (int q = 1; q < 4; ++q) {   // sub-groups in ascending expert order: strict > keeps the lower
+        const bool b = sv[q] > bv;
+        bv = b ? sv[q] : bv;
+        bi = b ? si[q] : bi;
+      }
+#pragma unroll
+      for (int off = L / 2; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(gm, bv, off, L);
+        const int oi = __shfl_xor_sync(gm, bi, off, L);
+        const bool b = g32_better(ov, oi, bv, bi);
+        bv = b ? ov : bv;
+        bi = b ? oi : bi;
+      }
+      if ((bi >> 5) == g) {   // this lane owns the winner: take it, rescan its sub-group
+        const int q = (bi >> 3) & 3;
+        my[bi & 31] = -INFINITY;
+        const float4 a = *reinterpret_cast<const float4*>(my + 8 * q);
+        const float4 c = *reinterpret_cast<const float4*>(my + 8 * q + 4);
+        const float x[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        float v = x[0];
+        int i0 = 0;
+#pragma unroll
+        for (int cc = 1; cc < 8; ++cc) {
+          i0 = x[cc] > v ? cc : i0;
+          v = fmaxf(v, x[cc]);
+        }
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          sv[qq] = qq == q ? v : sv[qq];
+          si[qq] = qq == q ? 32 * g + 8 * q + i0 : si[qq];
+        }
+      }
+      if ((j & (L - 1)) == g) {
+        // noaux_tc reports the un-biased score of the chosen expert (a cached re-read)
+        w_out[t * k + j] = noaux ? __ldg(scores + t * (long)E + bi) : bv;
+        idx_out[t * k + j] = bi;
+      }
+    }
+    __syncwarp(gm);   // the parked rows are rewritten by the next token's vectors
+  }
+}
+
+template <int L>
+int launch_group_g32(const float* scores, const float* bias, int T, int E, int k, int n_group, int topk_group,
+                     int noaux, float* w, int32_t* idx, cudaStream_t s) {
+  const int tpb = kBlock / L;
+  const long blocks = ((long)T + tpb - 1) / tpb;
+  const long cap = (long)num_sms() * 8;
+  group_topk_g32_kernel<L><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(
+      scores, bias, T, E, k, n_group, topk_group, noaux, w, idx);
+  return check_launch("group_limited_topk");
 }
 
 // Thread-per-token form for E <= 256: the choice row and the group scores live in
@@ -790,6 +972,12 @@ int launch_group_limited_topk(const float* scores, const float* bias, int T, int
   if (T == 0) return MOE_OK;
   ProfScope ps("group_limited_topk", s);
   const int gs = E / n_group;
+  if (gs == 32) {   // groups of 32: coalesced row reads, one lane per group
+    if (n_group <= 4) return launch_group_g32<4>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+    if (n_group <= 8) return launch_group_g32<8>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+    if (n_group <= 16) return launch_group_g32<16>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+    return launch_group_g32<32>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
+  }
   if (gs <= 32) {   // one lane per group (measured 1.7x faster than a thread per token at E = 256)
     if (n_group <= 4) return launch_group_lane_smem<4>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
     if (n_group <= 8) return launch_group_lane_smem<8>(scores, bias, T, E, k, n_group, topk_group, noaux, w, idx, s);
