@@ -603,14 +603,12 @@ __global__ void __launch_bounds__(kBlock) group_topk_lane_smem_kernel(
 // parked row of the lane owning its group (36-float rows: every 16-byte access
 // pattern below is conflict-free per quarter warp). Each lane then reads its
 // group back as 16-byte vectors, forms the group score and the maxima of its
-// four sub-groups of 8 in one pass, and the selection runs as in
-// group_topk_lane_smem_kernel, with absent or taken candidates as (-inf, kNone)
-// so a merge step is two compares.
+// four sub-groups of 8. The topk_group groups are those of rank < topk_group
+// among the token's group scores (score desc, group asc); each of the k rounds
+// takes the token's largest offered value (a max butterfly), then the lowest
+// expert offering it (a min butterfly), and the owning lane rescans one
+// sub-group, as in group_topk_lane_smem_kernel.
 constexpr int kG32Ld = 36;
-
-__device__ __forceinline__ bool g32_better(float av, int ai, float bv, int bi) {
-  return av > bv || (av == bv && ai < bi);
-}
 
 template <int L>
 __global__ void __launch_bounds__(kBlock) group_topk_g32_kernel(
@@ -648,8 +646,7 @@ __global__ void __launch_bounds__(kBlock) group_topk_g32_kernel(
       }
     }
     __syncwarp(gm);
-    // group score (max, or the float32 sum of the two largest) and sub-group maxima
-    float b1 = -FLT_MAX, b2 = -FLT_MAX;
+    // sub-group maxima (value, first expert holding it) from the parked group
     float sv[4];
     int si[4];
 #pragma unroll
@@ -666,36 +663,45 @@ __global__ void __launch_bounds__(kBlock) group_topk_g32_kernel(
         float v = x[0];
         int i0 = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j > 0) {
-            i0 = x[j] > v ? j : i0;
-            v = fmaxf(v, x[j]);
-          }
-          const float lo = fminf(b1, x[j]);
-          b1 = fmaxf(b1, x[j]);
-          b2 = fmaxf(b2, lo);
+        for (int j = 1; j < 8; ++j) {
+          i0 = x[j] > v ? j : i0;
+          v = fmaxf(v, x[j]);
         }
         sv[q] = v;
         si[q] = 32 * g + 8 * q + i0;
       }
     }
-    const float gscore = noaux ? b1 + b2 : b1;
-    unsigned gsel = 0;
-    for (int j = 0; j < topk_group; ++j) {
-      const bool avail = has && !((gsel >> g) & 1u);
-      float bv = avail ? gscore : -INFINITY;
-      int bi = avail ? g : kNone;
+    // group score: its largest value, or (noaux_tc) the float32 sum of its two
+    // largest: the largest of the other sub-groups' maxima and of the first
+    // holding sub-group without its arg-max
+    const float b1 = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    float gscore = has ? b1 : -INFINITY;
+    if (noaux && has) {
+      int qs = 3;
 #pragma unroll
-      for (int off = L / 2; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(gm, bv, off, L);
-        const int oi = __shfl_xor_sync(gm, bi, off, L);
-        const bool b = g32_better(ov, oi, bv, bi);
-        bv = b ? ov : bv;
-        bi = b ? oi : bi;
+      for (int q = 2; q >= 0; --q) qs = sv[q] == b1 ? q : qs;
+      float b2 = -INFINITY;
+      int ia = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        b2 = fmaxf(b2, q == qs ? -INFINITY : sv[q]);
+        ia = q == qs ? si[q] & 7 : ia;
       }
-      gsel |= 1u << bi;
+      const float4 a = *reinterpret_cast<const float4*>(my + 8 * qs);
+      const float4 c = *reinterpret_cast<const float4*>(my + 8 * qs + 4);
+      const float x[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) b2 = fmaxf(b2, j == ia ? -INFINITY : x[j]);
+      gscore = b1 + b2;
     }
-    if (!(has && ((gsel >> g) & 1u))) {
+    // the topk_group best groups (score desc, group asc): a group's rank among the token's lanes
+    int rank = 0;
+#pragma unroll
+    for (int gg = 0; gg < L; ++gg) {
+      const float o = __shfl_sync(gm, gscore, gg, L);
+      rank += (o > gscore || (o == gscore && gg < g)) ? 1 : 0;
+    }
+    if (!(has && rank < topk_group)) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         sv[q] = -INFINITY;
@@ -711,14 +717,15 @@ __global__ void __launch_bounds__(kBlock) group_topk_g32_kernel(
         bv = b ? sv[q] : bv;
         bi = b ? si[q] : bi;
       }
+      // the token's largest offer, then the lowest expert offering it
+      float mx = bv;
 #pragma unroll
-      for (int off = L / 2; off >= 1; off >>= 1) {
-        const float ov = __shfl_xor_sync(gm, bv, off, L);
-        const int oi = __shfl_xor_sync(gm, bi, off, L);
-        const bool b = g32_better(ov, oi, bv, bi);
-        bv = b ? ov : bv;
-        bi = b ? oi : bi;
-      }
+      for (int off = L / 2; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(gm, mx, off, L));
+      int ci = bv == mx ? bi : kNone;
+#pragma unroll
+      for (int off = L / 2; off >= 1; off >>= 1) ci = min(ci, __shfl_xor_sync(gm, ci, off, L));
+      bv = mx;
+      bi = ci;
       if ((bi >> 5) == g) {   // this lane owns the winner: take it, rescan its sub-group
         const int q = (bi >> 3) & 3;
         my[bi & 31] = -INFINITY;
