@@ -268,6 +268,28 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// The cp.async copies of rows [t0, t0 + nt) into the chunked stage (one 16-byte
+// logits vector per stage chunk: E % (16 / sizeof(In)) == 0 and sizeof(In) ==
+// sizeof(St)), issued by threads tid = 0..nthr-1 (a multiple of 32) without
+// waiting: a warp moves tiles of 4 rows x 8 vectors (4 full 128-byte segments of
+// global memory, 8 conflict-free chunk stores per quarter warp).
+template <typename In, typename St>
+__device__ __forceinline__ void stage_rows_async(const In* __restrict__ logits, long t0, int nt, int E, St* col,
+                                                 int tid, int nthr) {
+  static_assert(sizeof(In) == sizeof(St), "one logits vector per stage chunk");
+  constexpr int VEC = 16 / (int)sizeof(In);
+  const int R = E / VEC;   // vectors per row
+  const uint4* src = reinterpret_cast<const uint4*>(logits + t0 * (long)E);
+  uint4* dst = reinterpret_cast<uint4*>(col);
+  const int lane = tid & 31, w = tid >> 5, nw = nthr >> 5;
+  const int nrt = (nt + 3) >> 2;   // tiles of 4 rows
+  for (int c = lane & 7; c < ((R + 7) & ~7); c += 8)
+    for (int rt = w; rt < nrt; rt += nw) {
+      const int r = 4 * rt + (lane >> 3);
+      if (c < R && r < nt) cp_async16(dst + c * kStageLd + r, src + r * R + c);
+    }
+}
+
 // Stage rows [t0, t0 + nt) of logits (nt <= kStageRows) into the chunked stage,
 // experts E..EP-1 as -inf, by threads tid = 0..nthr-1 (nthr >= kStageRows, a
 // multiple of 32); the caller synchronises before reading. With 16-byte rows
@@ -286,12 +308,7 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
     const int lane = tid & 31, w = tid >> 5, nw = nthr >> 5;
     const int nrt = (nt + 3) >> 2;           // tiles of 4 rows
     if constexpr (sizeof(In) == sizeof(St)) {
-      uint4* dst = reinterpret_cast<uint4*>(col);
-      for (int c = lane & 7; c < ((R + 7) & ~7); c += 8)
-        for (int rt = w; rt < nrt; rt += nw) {
-          const int r = 4 * rt + (lane >> 3);
-          if (c < R && r < nt) cp_async16(dst + c * kStageLd + r, src + r * R + c);
-        }
+      stage_rows_async(logits, t0, nt, E, col, tid, nthr);
       cp_async_wait_all();
     } else {   // 8 bf16 -> two float32 chunks
       float4* dst = reinterpret_cast<float4*>(col);

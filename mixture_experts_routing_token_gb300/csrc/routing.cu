@@ -43,6 +43,34 @@ using StageT = typename std::conditional<!std::is_same<In, float>::value && EP >
 template <int EP, typename In>
 constexpr bool kRegMax = std::is_same<StageT<EP, In>, float>::value && EP == 128;
 
+// The parked results of the block's rows (gate::topk_staged_row<TO_COL>: weights
+// as words 0..k-1, indices as words 8..8+k-1 of each row's first chunks) written
+// out contiguously.
+template <typename St>
+__device__ __forceinline__ void copy_out_parked(const St* col, long t0, int nt, int k, float* __restrict__ w_out,
+                                                int32_t* __restrict__ idx_out, int tid, int nthr) {
+  if (k == 8 || k == 4) {   // whole 16-byte chunks
+    const uint4* c4 = reinterpret_cast<const uint4*>(col);
+    const int hs = k >> 3;   // chunks per row's weights, minus one
+    for (int f = tid; f < (nt << hs); f += nthr) {
+      const int r = f >> hs, h = f & hs;
+      reinterpret_cast<uint4*>(w_out + (t0 + r) * k)[h] = c4[h * gate::kStageLd + r];
+      reinterpret_cast<uint4*>(idx_out + (t0 + r) * k)[h] = c4[(2 + h) * gate::kStageLd + r];
+    }
+    return;
+  }
+  auto get32 = [&](int slot, int r) -> uint32_t {   // word `slot` of the row's parking chunks
+    return reinterpret_cast<const uint32_t*>(col)[((slot >> 2) * gate::kStageLd + r) * 4 + (slot & 3)];
+  };
+  const int n = nt * k;
+  const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // row of output f: f >> kshift, or f / k
+  for (int f = tid; f < n; f += nthr) {
+    const int r = kshift >= 0 ? f >> kshift : (int)((uint32_t)f / (uint32_t)k), j = f - r * k;
+    w_out[t0 * k + f] = __uint_as_float(get32(j, r));
+    idx_out[t0 * k + f] = (int32_t)get32(gate::kRegSel + j, r);
+  }
+}
+
 template <int EP, typename In, int U = 8>
 __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
     const In* __restrict__ logits, int T, int E, int k, int norm, float* __restrict__ w_out,
@@ -65,35 +93,16 @@ __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
   // contiguously.
   if (tid < nt) gate::topk_staged_row<EP, true, St, RM>(col, tid, tid, E, k, norm, nullptr, nullptr);
   __syncthreads();
-  if (k == 8 || k == 4) {   // whole 16-byte chunks: weights words 0..k-1, indices words 8..8+k-1
-    const uint4* c4 = reinterpret_cast<const uint4*>(col);
-    const int hs = k >> 3;   // chunks per row's weights, minus one
-    for (int f = tid; f < (nt << hs); f += kSmemGateThreads) {
-      const int r = f >> hs, h = f & hs;
-      reinterpret_cast<uint4*>(w_out + (t0 + r) * k)[h] = c4[h * gate::kStageLd + r];
-      reinterpret_cast<uint4*>(idx_out + (t0 + r) * k)[h] = c4[(2 + h) * gate::kStageLd + r];
-    }
-    return;
-  }
-  auto get32 = [&](int slot, int r) -> uint32_t {   // word `slot` of the row's parking chunks
-    return reinterpret_cast<const uint32_t*>(col)[((slot >> 2) * gate::kStageLd + r) * 4 + (slot & 3)];
-  };
-  const int n = nt * k;
-  const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // row of output f: f >> kshift, or f / k
-  for (int f = tid; f < n; f += kSmemGateThreads) {
-    const int r = kshift >= 0 ? f >> kshift : (int)((uint32_t)f / (uint32_t)k), j = f - r * k;
-    w_out[t0 * k + f] = __uint_as_float(get32(j, r));
-    idx_out[t0 * k + f] = (int32_t)get32(gate::kRegSel + j, r);
-  }
+  copy_out_parked(col, t0, nt, k, w_out, idx_out, tid, kSmemGateThreads);
 }
 
 template <int EP, typename In>
 int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
+  const unsigned grid = (unsigned)((T + kSmemGateThreads - 1) / kSmemGateThreads);
   const size_t smem = (size_t)gate::stage_bytes<EP, StageT<EP, In>, kRegMax<EP, In>>();
   if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
-  gating_smem_kernel<EP, In><<<(T + kSmemGateThreads - 1) / kSmemGateThreads, kSmemGateThreads, smem, s>>>(
-      logits, T, E, k, norm, w, idx);
+  gating_smem_kernel<EP, In><<<grid, kSmemGateThreads, smem, s>>>(logits, T, E, k, norm, w, idx);
   return check_launch("gating_softmax_topk");
 }
 
