@@ -189,8 +189,21 @@ __device__ __forceinline__ int warp0_exclusive_scan(int* v, int n) {
 // number of e's slots in the chunk's warps before w. Slots are ranked into the
 // staging arrays in expert-sorted order together with their global position,
 // then copied out by consecutive threads (each expert's run is contiguous in
-// both orders: coalesced stores). Slot indices are 32-bit (T*k < 2^31).
-template <int SRC, int EB = 0>
+// both orders: coalesced stores). Slot indices are 32-bit (T*k < 2^31). With
+// a power-of-two k the token of a staged slot is derived from the slot.
+//
+// Ranking. K8 (k == 8, a chunk is 512 tokens, one per thread): thread t holds
+// token t's 8 slots, which name distinct experts, so a slot's rank among its
+// warp's slots of the same expert is the number of lower lanes whose token
+// names that expert: each lane sets its bit in the warp's 32-bit mask of every
+// expert it names (shared-memory atomicOr), and the rank is the population
+// count of the mask below the lane. A repeated expert within a row (outside
+// what top-k routing produces; detected when the lane's bit was already set)
+// sends the whole CTA to the general ranking. General: warp w takes the
+// chunk's slots [w * 32 * kSub, (w + 1) * 32 * kSub) as kSub sub-rounds of 32,
+// ranking each by its same-expert lanes on top of the warp's running
+// per-expert count.
+template <int SRC, int EB = 0, bool K8 = false>
 __device__ __forceinline__ void align_chunk(
     int c, const int32_t* idx, const float* wts, long S, int k, int E, int nchunks, int hist_is_prefix,
     const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -208,18 +221,41 @@ __device__ __forceinline__ void align_chunk(
   const int hi = (int)min(S, (long)lo + kChunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // token of slot s: s >> kshift or s / k
+  const int wbase = lo + warp * 32 * kSub;
 
-  // 0. this warp's slots (step 3), loaded first so that their latency overlaps steps 1-2;
+  // 0. this thread's slots (step 3), loaded first so that their latency overlaps steps 1-2;
   //    the barriers of steps 1-2 also order the zeroing of wcnt before step 3
   for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
-  const int wbase = lo + warp * 32 * kSub;
   int eu[kSub], ru[kSub];
   float wu[kSub];
+  auto load_general = [&]() {
 #pragma unroll
-  for (int u = 0; u < kSub; ++u) {
-    const int s = wbase + u * 32 + lane;
-    eu[u] = s < hi ? load_i<SRC>(idx + s) : -1;
-    wu[u] = s < hi ? load_f<SRC>(wts + s) : 0.0f;
+    for (int u = 0; u < kSub; ++u) {
+      const int s = wbase + u * 32 + lane;
+      eu[u] = s < hi ? load_i<SRC>(idx + s) : -1;
+      wu[u] = s < hi ? load_f<SRC>(wts + s) : 0.0f;
+    }
+  };
+  bool masks = K8;
+  if constexpr (K8) {
+    static_assert(kSub == 8 && SRC == kSrcGlobal, "one 8-slot token per thread, read from global memory");
+    const int s0 = lo + 8 * tid;
+    if (s0 + 8 <= hi) {
+      const int4 a = __ldg(reinterpret_cast<const int4*>(idx + s0));
+      const int4 b = __ldg(reinterpret_cast<const int4*>(idx + s0) + 1);
+      const float4 x = __ldg(reinterpret_cast<const float4*>(wts + s0));
+      const float4 y = __ldg(reinterpret_cast<const float4*>(wts + s0) + 1);
+      eu[0] = a.x; eu[1] = a.y; eu[2] = a.z; eu[3] = a.w; eu[4] = b.x; eu[5] = b.y; eu[6] = b.z; eu[7] = b.w;
+      wu[0] = x.x; wu[1] = x.y; wu[2] = x.z; wu[3] = x.w; wu[4] = y.x; wu[5] = y.y; wu[6] = y.z; wu[7] = y.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < kSub; ++u) {
+        eu[u] = s0 + u < hi ? __ldg(idx + s0 + u) : -1;
+        wu[u] = s0 + u < hi ? __ldg(wts + s0 + u) : 0.0f;
+      }
+    }
+  } else {
+    load_general();
   }
 
   // 1. per-expert totals (off[]), slots of earlier chunks (cb[]) and this chunk's counts (cpre[])
@@ -278,30 +314,51 @@ __device__ __forceinline__ void align_chunk(
   if (c == 0)
     for (int e = tid; e < E; e += kThreads) offsets[e] = off[e];
 
-  // 3. ranking, one round: warp w takes the chunk's slots [w * 32 * kSub, (w + 1) * 32 * kSub)
-  //    as kSub sub-rounds of 32, ranking each by its same-expert lanes on top of the warp's
-  //    running per-expert count; a per-expert prefix over the warps then places them.
-  const int ebits = 32 - __clz(max(E - 1, 1));
+  // 3. ranking within the warp, then a per-expert prefix over the warps
+  if constexpr (K8) {
+    unsigned* msk = reinterpret_cast<unsigned*>(wcnt) + warp * E;
+    const unsigned bit = 1u << lane;
+    bool dup = false;
 #pragma unroll
-  for (int u = 0; u < kSub; ++u) {
-    const int e = valid_expert(eu[u], E);
-    const unsigned peers = EB > 0 ? same_expert_lanes_t<EB>(e)
-                           : SRC == kSrcGlobal && ebits > 4 ? same_expert_lanes(e, ebits)
-                                                            : __match_any_sync(0xffffffffu, e);
-    const int below = __popc(peers & ((1u << lane) - 1u));
-    const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
+    for (int u = 0; u < kSub; ++u) {
+      const int e = valid_expert(eu[u], E);
+      eu[u] = e;
+      if (e >= 0) dup |= (atomicOr(msk + e, bit) & bit) != 0u;
+    }
     __syncwarp();
-    if (e >= 0 && below == 0) wcnt[warp * E + e] = prior + __popc(peers);
-    __syncwarp();
-    eu[u] = e;
-    ru[u] = prior + below;
+#pragma unroll
+    for (int u = 0; u < kSub; ++u) ru[u] = eu[u] >= 0 ? __popc(msk[eu[u]] & (bit - 1u)) : 0;
+    if (__syncthreads_or(dup)) {   // a repeated expert in some row: general ranking for this chunk
+      masks = false;
+      for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+      load_general();
+      __syncthreads();
+    }
+  }
+  if (!masks) {
+    const int ebits = 32 - __clz(max(E - 1, 1));
+#pragma unroll
+    for (int u = 0; u < kSub; ++u) {
+      const int e = valid_expert(eu[u], E);
+      const unsigned peers = EB > 0 ? same_expert_lanes_t<EB>(e)
+                             : SRC == kSrcGlobal && ebits > 4 ? same_expert_lanes(e, ebits)
+                                                              : __match_any_sync(0xffffffffu, e);
+      const int below = __popc(peers & ((1u << lane) - 1u));
+      const int prior = e >= 0 ? wcnt[warp * E + e] : 0;
+      __syncwarp();
+      if (e >= 0 && below == 0) wcnt[warp * E + e] = prior + __popc(peers);
+      __syncwarp();
+      eu[u] = e;
+      ru[u] = prior + below;
+    }
   }
   __syncthreads();
   for (int x = tid; x < E; x += kThreads) {
     int run = 0;
 #pragma unroll 4
     for (int w = 0; w < kWarps; ++w) {
-      const int cnt = wcnt[w * E + x];
+      const int v = wcnt[w * E + x];
+      const int cnt = masks ? __popc((unsigned)v) : v;
       wcnt[w * E + x] = run;
       run += cnt;
     }
@@ -311,10 +368,10 @@ __device__ __forceinline__ void align_chunk(
   for (int u = 0; u < kSub; ++u) {
     const int e = eu[u];
     if (e >= 0) {
-      const int s = wbase + u * 32 + lane;
+      const int s = masks ? lo + 8 * tid + u : wbase + u * 32 + lane;
       const int base = cpre[e];
       const int q = base + wcnt[warp * E + e] + ru[u];   // chunk-local, expert-sorted
-      s_tok[q] = kshift >= 0 ? s >> kshift : (int)((uint32_t)s / (uint32_t)k);
+      if (kshift < 0) s_tok[q] = (int)((uint32_t)s / (uint32_t)k);
       s_rev[q] = s;
       s_w[q] = wu[u];
       s_dst[q] = off[e] + cb[e] + (q - base);
@@ -326,21 +383,22 @@ __device__ __forceinline__ void align_chunk(
   const int n = cpre[E];
   for (int q = tid; q < n; q += kThreads) {
     const int p = s_dst[q];
-    sorted_ids[p] = s_tok[q];
-    reverse[p] = s_rev[q];
+    const int sl = s_rev[q];
+    sorted_ids[p] = kshift >= 0 ? sl >> kshift : s_tok[q];
+    reverse[p] = sl;
     sorted_w[p] = s_w[q];
   }
 }
 
 // EB: bits of E - 1 (5..10, the per-bit ballots unrolled), or 0 (E <= 16: __match_any_sync).
-template <int EB>
+template <int EB, bool K8 = false>
 __global__ void __launch_bounds__(kThreads) align_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ wts, long S, int k, int E,
     int nchunks, int hist_is_prefix, const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status) {
   extern __shared__ int sm[];
-  align_chunk<kSrcGlobal, EB>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
+  align_chunk<kSrcGlobal, EB, K8>(blockIdx.x, idx, wts, S, k, E, nchunks, hist_is_prefix, chunk_hist, counts, offsets,
                      sorted_ids, sorted_w, reverse, status, sm);
 }
 
@@ -478,6 +536,17 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
                                                               offsets, sorted_ids, sorted_w, reverse, status);
     return check_launch("align_scatter");
   };
+  if (k == 8) {   // one token per thread, ranked by per-warp expert masks
+    switch (ebits) {
+      case 5: return scatter(align_scatter_kernel<5, true>);
+      case 6: return scatter(align_scatter_kernel<6, true>);
+      case 7: return scatter(align_scatter_kernel<7, true>);
+      case 8: return scatter(align_scatter_kernel<8, true>);
+      case 9: return scatter(align_scatter_kernel<9, true>);
+      case 10: return scatter(align_scatter_kernel<10, true>);
+      default: return scatter(align_scatter_kernel<0, true>);
+    }
+  }
   switch (ebits) {
     case 5: return scatter(align_scatter_kernel<5>);
     case 6: return scatter(align_scatter_kernel<6>);

@@ -198,6 +198,29 @@ def test_align_all_to_one_expert_and_page_example(gold):
     assert _align_case(moe, i, np.ones(i.shape, np.float32), g["E"]) == 0
 
 
+def test_align_repeated_expert_in_a_row_k8():
+    """Rows naming an expert twice are outside what top-k routing produces (the
+    oracle's reading); the k = 8 ranking detects them and falls back to the
+    general ranking, so the result is still the stable sort of the slots by
+    expert: checked against numpy's stable argsort on chunks with and without
+    repeats."""
+    moe = need_gpu()
+    T, E, k = 3000, 64, 8
+    rng = np.random.default_rng(5)
+    i = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    i[700, 3] = i[700, 1]          # a repeat in chunk 1 (tokens 512..1023)
+    i[10, 7] = i[10, 0]            # and one in chunk 0; chunks 2.. have none
+    w = rng.random((T, k)).astype(np.float32)
+    got = moe.moe_align_by_expert(torch.from_numpy(i).to(DEV), torch.from_numpy(w).to(DEV), E)
+    torch.cuda.synchronize()
+    flat = i.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    np.testing.assert_array_equal(got["counts"].cpu().numpy(), np.bincount(flat, minlength=E))
+    np.testing.assert_array_equal(got["reverse_indices"].cpu().numpy(), order)
+    np.testing.assert_array_equal(got["sorted_token_ids"].cpu().numpy(), order // k)
+    np.testing.assert_array_equal(got["sorted_weights"].cpu().numpy(), w.reshape(-1)[order])
+
+
 def test_align_invalid_index_sets_status_and_drops_slot():
     moe = need_gpu()
     for T in (3, 6000):    # single-chunk and multi-chunk launches
