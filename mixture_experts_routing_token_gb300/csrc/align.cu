@@ -78,15 +78,25 @@ __global__ void __launch_bounds__(kThreads) align_hist_kernel(const int32_t* __r
                                                               int32_t* __restrict__ chunk_hist,
                                                               int32_t* status) {
   extern __shared__ int hist[];
+  pdl_wait();      // the routing was written by the previous kernel
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
   __syncthreads();
   const long lo = (long)blockIdx.x * kChunk;
   const long hi = min(S, lo + kChunk);
   bool bad = false;
-  for (long s = lo + threadIdx.x; s < hi; s += kThreads) {
-    const int e = __ldg(idx + s);
+  auto count = [&](int e) {
     if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
     else bad = true;
+  };
+  if (hi - lo == kChunk) {   // a whole chunk: two 16-byte loads per thread, both in flight
+    static_assert(kChunk == 8 * kThreads, "eight slots per thread");
+    const int4 a = __ldg(reinterpret_cast<const int4*>(idx + lo) + threadIdx.x);
+    const int4 b = __ldg(reinterpret_cast<const int4*>(idx + lo) + kThreads + threadIdx.x);
+    count(a.x); count(a.y); count(a.z); count(a.w);
+    count(b.x); count(b.y); count(b.z); count(b.w);
+  } else {
+    for (long s = lo + threadIdx.x; s < hi; s += kThreads) count(__ldg(idx + s));
   }
   if (bad && status) atomicOr(status, MOE_STATUS_BAD_INDEX);
   __syncthreads();
@@ -97,6 +107,8 @@ __global__ void __launch_bounds__(kThreads) align_hist_kernel(const int32_t* __r
 // each thread a contiguous run of chunks, block scan of the run totals.
 __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E) {
   __shared__ int wsum[32];
+  pdl_wait();      // the histograms of align_hist_kernel
+  pdl_trigger();
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (nchunks + 1023) / 1024;
   const int c0 = min(nchunks, tid * per), c1 = min(nchunks, c0 + per);
@@ -224,7 +236,12 @@ __device__ __forceinline__ void align_chunk(
   const int wbase = lo + warp * 32 * kSub;
 
   // 0. this thread's slots (step 3), loaded first so that their latency overlaps steps 1-2;
-  //    the barriers of steps 1-2 also order the zeroing of wcnt before step 3
+  //    the barriers of steps 1-2 also order the zeroing of wcnt before step 3.
+  //    Launched behind the histogram / scan kernels (programmatic serialization), the
+  //    routing is two or more launches back and may be read before pdl_wait(); as the
+  //    only align kernel (one chunk) it comes straight after the routing's producer.
+  if constexpr (SRC == kSrcGlobal)
+    if (!chunk_hist) pdl_wait();
   for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
   int eu[kSub], ru[kSub];
   float wu[kSub];
@@ -256,6 +273,10 @@ __device__ __forceinline__ void align_chunk(
     }
   } else {
     load_general();
+  }
+  if constexpr (SRC == kSrcGlobal) {   // the histograms come from the launch just before
+    if (chunk_hist) pdl_wait();
+    pdl_trigger();
   }
 
   // 1. per-expert totals (off[]), slots of earlier chunks (cb[]) and this chunk's counts (cpre[])
@@ -518,22 +539,25 @@ int launch_align(const int32_t* idx, const float* w, int T, int k, int E, int32_
   if (nchunks > 1) {
     hist = static_cast<int32_t*>(scratch);
     ProfScope ps("align_hist", s);
-    align_hist_kernel<<<nchunks, kThreads, E * sizeof(int), s>>>(idx, S, E, hist, status);
+    const cudaError_t e = launch_pdl(align_hist_kernel, nchunks, kThreads, E * sizeof(int), s, idx, S, E, hist, status);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "align_hist: %s", cudaGetErrorString(e));
     int rc = check_launch("align_hist");
     if (rc) return rc;
   }
   const int prefix = nchunks > kScanAbove;
   if (prefix) {
     ProfScope ps("align_scan", s);
-    align_scan_kernel<<<E, 1024, 0, s>>>(hist, nchunks, E);
+    const cudaError_t e = launch_pdl(align_scan_kernel, E, 1024, 0, s, hist, nchunks, E);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "align_scan: %s", cudaGetErrorString(e));
     int rc = check_launch("align_scan");
     if (rc) return rc;
   }
   auto scatter = [&](auto kernel) -> int {
     if (int rc = ensure_smem_limit(kernel, align_smem_bytes(MOE_MAX_EXPERTS), "align_scatter")) return rc;
     ProfScope ps("align_scatter", s);
-    kernel<<<nchunks > 0 ? nchunks : 1, kThreads, smem, s>>>(idx, w, S, k, E, nchunks, prefix, hist, counts,
-                                                              offsets, sorted_ids, sorted_w, reverse, status);
+    const cudaError_t e = launch_pdl(kernel, nchunks > 0 ? nchunks : 1, kThreads, smem, s, idx, w, S, k, E, nchunks,
+                                     prefix, hist, counts, offsets, sorted_ids, sorted_w, reverse, status);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "align_scatter: %s", cudaGetErrorString(e));
     return check_launch("align_scatter");
   };
   if (k == 8) {   // one token per thread, ranked by per-warp expert masks
