@@ -128,6 +128,11 @@ struct FfnArgs {
 // bf16 matrix [rows, cols] row-major as a TMA tensor map: box = box_rows x 64
 // columns, 128-byte swizzle, zero fill out of bounds.
 int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// Row-major [rows, cols] matrix of 4- or 2-byte elements as a TMA tensor map whose
+// box is box_rows rows x 128 bytes, 128-byte swizzle, zero fill out of bounds
+// (cols * elem_bytes a multiple of 16, base 16-byte aligned).
+int make_tmap_rows128(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, int elem_bytes,
+                      uint32_t box_rows);
 // x_sorted[p] = hidden[sorted_ids[p]] for p < offsets[E] (rows of row_bytes, a multiple of 16).
 int launch_gather_rows(const void* hidden, const int32_t* sorted_ids, const int32_t* offsets, int E, int row_bytes,
                        void* xs, int32_t* status, cudaStream_t s);

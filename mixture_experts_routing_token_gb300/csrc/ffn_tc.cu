@@ -270,6 +270,23 @@ int make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return MOE_OK;
 }
 
+int make_tmap_rows128(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, int elem_bytes,
+                      uint32_t box_rows) {
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(MOE_ERR_UNSUPPORTED, "make_tmap_rows128: %d-byte elements", elem_bytes);
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (cuuint64_t)elem_bytes};
+  const cuuint32_t box[2] = {128u / (cuuint32_t)elem_bytes, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 bool ffn_uses_tensor_cores(int dtype, int H, int I) {
   return dtype == MOE_BF16 && H % 64 == 0 && I % 64 == 0 && H > 0 && I > 0;
 }

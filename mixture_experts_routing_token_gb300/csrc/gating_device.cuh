@@ -242,10 +242,30 @@ constexpr int kStageLd = kStageRows + 1;
 template <typename St>
 __host__ __device__ constexpr int chunk_elems() { return 16 / (int)sizeof(St); }
 
+// Stage layouts: the index (in 16-byte units) of chunk q of staged row r.
+// StagePadded: chunk columns of kStageLd chunks, the form filled by cp.async
+// and thread stores (above). StageSwz128: the form a TMA load of 128-row x
+// 128-byte boxes writes with the 128-byte swizzle (box b = chunks 8b .. 8b+7 of
+// every row; in each 1 KB block of 8 rows, chunk u of row i sits at u ^ i): the
+// 8 lanes of a quarter warp reading one chunk of 8 consecutive rows hit 8
+// distinct bank groups whatever the chunk, so the rounds' reads of different
+// groups by different rows are conflict-free too; the stage must start on a
+// 1024-byte boundary.
+struct StagePadded {
+  static constexpr int kRowsLd = kStageLd;
+  __host__ __device__ static constexpr int chunk(int q, int r) { return q * kStageLd + r; }
+};
+struct StageSwz128 {
+  static constexpr int kRowsLd = kStageRows;
+  __host__ __device__ static constexpr int chunk(int q, int r) {
+    return (q >> 3) * (kStageRows * 8) + r * 8 + ((q & 7) ^ (r & 7));
+  }
+};
+
 // Element e of staged row r.
-template <typename St>
+template <typename St, typename Lay = StagePadded>
 __host__ __device__ constexpr int sofs(int e, int r) {
-  return ((e / chunk_elems<St>()) * kStageLd + r) * chunk_elems<St>() + e % chunk_elems<St>();
+  return Lay::chunk(e / chunk_elems<St>(), r) * chunk_elems<St>() + e % chunk_elems<St>();
 }
 
 // Staged logits are kept as float32, or for bf16 logits as their 16-bit
@@ -342,24 +362,28 @@ __device__ __forceinline__ void stage_rows(const In* __restrict__ logits, long t
 
 // The 8 staged values of group g (experts 8g .. 8g + 7) of row r: two float32
 // chunks, or one chunk of 16-bit patterns.
+template <typename Lay = StagePadded>
 __device__ __forceinline__ void load_group8(const float* col, int g, int r, float (&x)[8]) {
   const float4* c4 = reinterpret_cast<const float4*>(col);
-  const float4 a = c4[(2 * g) * kStageLd + r], b = c4[(2 * g + 1) * kStageLd + r];
+  const float4 a = c4[Lay::chunk(2 * g, r)], b = c4[Lay::chunk(2 * g + 1, r)];
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
+template <typename Lay = StagePadded>
 __device__ __forceinline__ void load_group8(const uint16_t* col, int g, int r, float (&x)[8]) {
-  const uint4 q = reinterpret_cast<const uint4*>(col)[g * kStageLd + r];
+  const uint4 q = reinterpret_cast<const uint4*>(col)[Lay::chunk(g, r)];
   x[0] = lo_bf16(q.x); x[1] = hi_bf16(q.x); x[2] = lo_bf16(q.y); x[3] = hi_bf16(q.y);
   x[4] = lo_bf16(q.z); x[5] = hi_bf16(q.z); x[6] = lo_bf16(q.w); x[7] = hi_bf16(q.w);
 }
 
 // Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: EP / VE
-// chunk columns of kStageLd 16-byte chunks, then (RM false) the float maxima of
-// the rows' groups of 8 [EP / 8][kStageLd].
-template <int EP, typename St = float>
-__host__ __device__ constexpr int stage_rows_bytes() { return EP * kStageLd * (int)sizeof(St); }
-template <int EP, typename St = float, bool RM = false>
-__host__ __device__ constexpr int stage_bytes() { return stage_rows_bytes<EP, St>() + (RM ? 0 : EP / 8 * kStageLd * 4); }
+// chunk columns of Lay::kRowsLd 16-byte chunks, then (RM false) the float maxima
+// of the rows' groups of 8 [EP / 8][kStageLd].
+template <int EP, typename St = float, typename Lay = StagePadded>
+__host__ __device__ constexpr int stage_rows_bytes() { return EP * Lay::kRowsLd * (int)sizeof(St); }
+template <int EP, typename St = float, bool RM = false, typename Lay = StagePadded>
+__host__ __device__ constexpr int stage_bytes() {
+  return stage_rows_bytes<EP, St, Lay>() + (RM ? 0 : EP / 8 * kStageLd * 4);
+}
 template <int EP>
 __host__ __device__ constexpr int stage_floats() { return stage_bytes<EP, float>() / 4; }
 
@@ -386,7 +410,7 @@ __host__ __device__ constexpr int stage_floats() { return stage_bytes<EP, float>
 // own first four chunks (its logits are no longer needed): weight j and index j
 // (bits) as the 32-bit words j and kRegSel + j, word s being word s % 4 of chunk
 // s / 4 for either element type.
-template <int EP, bool TO_COL = false, typename St = float, bool RM = false>
+template <int EP, bool TO_COL = false, typename St = float, bool RM = false, typename Lay = StagePadded>
 __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, int k, int norm,
                                                 float* __restrict__ w_out, int32_t* __restrict__ idx_out,
                                                 float* s_w = nullptr, int32_t* s_idx = nullptr) {
@@ -395,8 +419,8 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
   constexpr int G = EP / 8;          // groups of 8 experts
   static_assert((G & (G - 1)) == 0, "a power-of-two number of groups");
   constexpr int S = (G + 3) / 4;     // supers of 4 groups (RM false)
-  auto at = [&](int i) -> float { return st_get(col + sofs<St>(i, r)); };
-  float* gcol = reinterpret_cast<float*>(reinterpret_cast<char*>(col) + stage_rows_bytes<EP, St>());
+  auto at = [&](int i) -> float { return st_get(col + sofs<St, Lay>(i, r)); };
+  float* gcol = reinterpret_cast<float*>(reinterpret_cast<char*>(col) + stage_rows_bytes<EP, St, Lay>());
   auto gat = [&](int g) -> float& { return gcol[g * kStageLd + r]; };
   float gmx[RM ? G : 1];
   float sm[S];
@@ -405,10 +429,8 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float y[8];
-    load_group8(col, g, r, y);
-    float x = y[0];
-#pragma unroll
-    for (int c = 1; c < 8; ++c) x = fmaxf(x, y[c]);
+    load_group8<Lay>(col, g, r, y);
+    const float x = fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])), fmaxf(fmaxf(y[4], y[5]), fmaxf(y[6], y[7])));
     if constexpr (RM) gmx[g] = x;
     else gat(g) = x;
     sm[g / 4] = fmaxf(sm[g / 4], x);
@@ -422,7 +444,7 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
     int i = 0;
     for (; i + 8 <= E; i += 8) {   // whole groups: one or two 16-byte reads
       float y[8];
-      load_group8(col, i / 8, r, y);
+      load_group8<Lay>(col, i / 8, r, y);
 #pragma unroll
       for (int a = 0; a < 8; ++a) two_sum_add(h[a & 3], l[a & 3], exp_diff_fast(y[a], m));
     }
@@ -469,15 +491,23 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
       bg = 4 * bs + bi;
     }
     float x[8];
-    load_group8(col, bg, r, x);
-    int bc = 0;
+    load_group8<Lay>(col, bg, r, x);
+    // the group's first expert holding v, and its maximum without that expert
+    // (v again when v occurs twice), both as trees rather than 8-step chains
+    unsigned eqm[8];
+    float ne[8];
 #pragma unroll
-    for (int c = 7; c >= 0; --c) bc = x[c] == v ? c : bc;
+    for (int c = 0; c < 8; ++c) {
+      eqm[c] = x[c] == v ? 1u << c : 0u;
+      ne[c] = x[c] == v ? -INFINITY : x[c];
+    }
+    const unsigned eq = ((eqm[0] | eqm[1]) | (eqm[2] | eqm[3])) | ((eqm[4] | eqm[5]) | (eqm[6] | eqm[7]));
+    const int bc = __ffs(eq) - 1;
     e = 8 * bg + bc;
-    st_neg_inf(col + sofs<St>(e, r));
-    float nm = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) nm = fmaxf(nm, c == bc ? -INFINITY : x[c]);
+    st_neg_inf(col + sofs<St, Lay>(e, r));
+    const float nm = (eq & (eq - 1u)) ? v
+                     : fmaxf(fmaxf(fmaxf(ne[0], ne[1]), fmaxf(ne[2], ne[3])),
+                             fmaxf(fmaxf(ne[4], ne[5]), fmaxf(ne[6], ne[7])));
     if constexpr (RM) {
 #pragma unroll
       for (int g = 0; g < G; ++g) gmx[g] = g == bg ? nm : gmx[g];
@@ -512,7 +542,7 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
       uint4* c4 = reinterpret_cast<uint4*>(col);
 #pragma unroll
       for (int h = 0; h < 2 * kRegSel / 4; ++h)
-        c4[h * kStageLd + r] = make_uint4(pw[4 * h], pw[4 * h + 1], pw[4 * h + 2], pw[4 * h + 3]);
+        c4[Lay::chunk(h, r)] = make_uint4(pw[4 * h], pw[4 * h + 1], pw[4 * h + 2], pw[4 * h + 3]);
     } else {
 #pragma unroll
       for (int j = 0; j < kRegSel; ++j)

@@ -13,6 +13,7 @@
 
 #include "common.cuh"
 #include "gating_device.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -46,7 +47,7 @@ constexpr bool kRegMax = std::is_same<StageT<EP, In>, float>::value && EP == 128
 // The parked results of the block's rows (gate::topk_staged_row<TO_COL>: weights
 // as words 0..k-1, indices as words 8..8+k-1 of each row's first chunks) written
 // out contiguously.
-template <typename St>
+template <typename St, typename Lay = gate::StagePadded>
 __device__ __forceinline__ void copy_out_parked(const St* col, long t0, int nt, int k, float* __restrict__ w_out,
                                                 int32_t* __restrict__ idx_out, int tid, int nthr) {
   if (k == 8 || k == 4) {   // whole 16-byte chunks
@@ -54,13 +55,13 @@ __device__ __forceinline__ void copy_out_parked(const St* col, long t0, int nt, 
     const int hs = k >> 3;   // chunks per row's weights, minus one
     for (int f = tid; f < (nt << hs); f += nthr) {
       const int r = f >> hs, h = f & hs;
-      reinterpret_cast<uint4*>(w_out + (t0 + r) * k)[h] = c4[h * gate::kStageLd + r];
-      reinterpret_cast<uint4*>(idx_out + (t0 + r) * k)[h] = c4[(2 + h) * gate::kStageLd + r];
+      reinterpret_cast<uint4*>(w_out + (t0 + r) * k)[h] = c4[Lay::chunk(h, r)];
+      reinterpret_cast<uint4*>(idx_out + (t0 + r) * k)[h] = c4[Lay::chunk(2 + h, r)];
     }
     return;
   }
   auto get32 = [&](int slot, int r) -> uint32_t {   // word `slot` of the row's parking chunks
-    return reinterpret_cast<const uint32_t*>(col)[((slot >> 2) * gate::kStageLd + r) * 4 + (slot & 3)];
+    return reinterpret_cast<const uint32_t*>(col)[Lay::chunk(slot >> 2, r) * 4 + (slot & 3)];
   };
   const int n = nt * k;
   const int kshift = (k & (k - 1)) == 0 ? __ffs(k) - 1 : -1;   // row of output f: f >> kshift, or f / k
@@ -96,9 +97,70 @@ __global__ void __launch_bounds__(kSmemGateThreads) gating_smem_kernel(
   copy_out_parked(col, t0, nt, k, w_out, idx_out, tid, kSmemGateThreads);
 }
 
+// The same with the block's rows brought in by TMA (k <= kRegSel, rows a whole
+// number of 128-byte boxes): one thread issues E * sizeof(In) / 128 tensor-map
+// copies of 128 rows x 128 bytes each (128-byte swizzle, gate::StageSwz128) on
+// one mbarrier, so the 128 threads spend no instructions on staging (measured
+// without the selection, the cp.async staging alone ran at 0.58-0.64 of the
+// copy peak), and every 16-byte read of the selection is conflict-free. The wait
+// is bounded (kGateWaitNs); a block whose rows never arrive writes nothing.
+constexpr uint64_t kGateWaitNs = 2000000000ull;
+
+template <int EP, typename In>
+__global__ void __launch_bounds__(kSmemGateThreads) gating_tma_kernel(
+    const __grid_constant__ CUtensorMap tm, int T, int E, int k, int norm, float* __restrict__ w_out,
+    int32_t* __restrict__ idx_out) {
+  using St = StageT<EP, In>;
+  using Lay = gate::StageSwz128;
+  constexpr bool RM = kRegMax<EP, In>;
+  extern __shared__ __align__(16) uint8_t stage_raw[];   // gate::stage_bytes<EP, St, RM, Lay>() + 1024
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  St* col = reinterpret_cast<St*>(stage_raw + ((1024u - (ptx::smem_u32(stage_raw) & 1023u)) & 1023u));
+  const int tid = threadIdx.x;
+  const long t0 = (long)blockIdx.x * kSmemGateThreads;
+  const int nt = (int)min((long)kSmemGateThreads, (long)T - t0);
+  const uint32_t b = ptx::smem_u32(&bar);
+  if (tid == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(b, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const int nbox = E * (int)sizeof(In) / 128;
+  if (tid == 0) {
+    ptx::mbar_arrive_expect_tx(b, (uint32_t)nbox * kSmemGateThreads * 128u);
+    for (int i = 0; i < nbox; ++i)
+      ptx::tma_load_2d(ptx::smem_u32(col) + (uint32_t)i * kSmemGateThreads * 128u, &tm, i * (128 / (int)sizeof(In)),
+                       (int)t0, b);
+  }
+  ptx::mbar_wait(b, 0, &abort_flag, kGateWaitNs);
+  for (int e = E; e < EP; ++e) gate::st_neg_inf(col + gate::sofs<St, Lay>(e, tid));   // experts past E: -inf
+  __syncthreads();
+  if (abort_flag) return;
+  if (tid < nt) gate::topk_staged_row<EP, true, St, RM, Lay>(col, tid, tid, E, k, norm, nullptr, nullptr);
+  __syncthreads();
+  copy_out_parked<St, Lay>(col, t0, nt, k, w_out, idx_out, tid, kSmemGateThreads);
+}
+
+template <int EP, typename In>
+int launch_gating_tma(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx, cudaStream_t s) {
+  using St = StageT<EP, In>;
+  CUtensorMap tm;
+  if (int rc = make_tmap_rows128(&tm, logits, (uint64_t)T, (uint64_t)E, (int)sizeof(In), kSmemGateThreads)) return rc;
+  const size_t smem = (size_t)gate::stage_bytes<EP, St, kRegMax<EP, In>, gate::StageSwz128>() + 1024;
+  if (int rc = ensure_smem_limit(gating_tma_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
+  const unsigned grid = (unsigned)((T + kSmemGateThreads - 1) / kSmemGateThreads);
+  gating_tma_kernel<EP, In><<<grid, kSmemGateThreads, smem, s>>>(tm, T, E, k, norm, w, idx);
+  return check_launch("gating_softmax_topk");
+}
+
 template <int EP, typename In>
 int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        cudaStream_t s) {
+  if constexpr (EP >= 64 && sizeof(StageT<EP, In>) == sizeof(In))
+    if (k <= gate::kRegSel && (E * (int)sizeof(In)) % 128 == 0)
+      return launch_gating_tma<EP, In>(logits, T, E, k, norm, w, idx, s);
   const unsigned grid = (unsigned)((T + kSmemGateThreads - 1) / kSmemGateThreads);
   const size_t smem = (size_t)gate::stage_bytes<EP, StageT<EP, In>, kRegMax<EP, In>>();
   if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
