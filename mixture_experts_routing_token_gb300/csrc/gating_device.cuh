@@ -59,19 +59,6 @@ __device__ __forceinline__ float exp_diff(float a, float b) {
   return fmaf(e, err, e);
 }
 
-// exp_diff with the fast exponential (CUDA's __expf: at most 2 + floor(1.173 |x|)
-// ulp). For the terms of the full-row softmax denominator, all at x = a - b <= 0:
-// a term's error grows with |x| but its weight falls as e^x, so the sum's relative
-// error stays near that of the largest terms (|x| < 1: <= 3 ulp, 1.8e-7); the k
-// selected numerators keep exp_diff.
-__device__ __forceinline__ float exp_diff_fast(float a, float b) {
-  const float s = a - b;
-  const float bb = s - a;
-  const float err = (a - (s - bb)) + (-b - bb);
-  const float e = __expf(s);
-  return fmaf(e, err, e);
-}
-
 // Order-preserving map of a finite float to an unsigned key (larger float ->
 // larger key; -0 and +0 share a key; 0 is below every finite float's key).
 __device__ __forceinline__ unsigned okey(float x) {
@@ -439,25 +426,40 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
 #pragma unroll
   for (int q = 1; q < S; ++q) m = fmaxf(m, sm[q]);
   float hi = 0.0f, lo = 0.0f;
-  if (!norm) {   // four independent compensated sums (a quarter of the dependent chain), then merged
-    float h[4] = {0.0f, 0.0f, 0.0f, 0.0f}, l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int i = 0;
-    for (; i + 8 <= E; i += 8) {   // whole groups: one or two 16-byte reads
+  if (!norm) {
+    // The full-row denominator: each group's 8 terms exp(x - m) (x <= m, fast
+    // exponential, no correction of the subtraction) summed as a tree, the group
+    // sums added with TwoSum into two alternating compensated accumulators. Its
+    // relative error stays below about 10 ulp (6e-7): the subtraction's rounding
+    // perturbs term i by at most |x_i - m| ulp and the fast exponential by 2 +
+    // 1.2 |x_i - m| ulp, and as the terms weigh e^(x_i - m) these average to a few
+    // ulp over any row (the largest terms have the smallest |x_i - m|); a tree of
+    // 8 positive terms adds 3 ulp. The selected numerators keep exp_diff.
+    auto group_sum = [&](int g) {   // one or two 16-byte reads
       float y[8];
-      load_group8<Lay>(col, i / 8, r, y);
+      load_group8<Lay>(col, g, r, y);
+      float t[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) two_sum_add(h[a & 3], l[a & 3], exp_diff_fast(y[a], m));
+      for (int a = 0; a < 8; ++a) t[a] = __expf(y[a] - m);
+      return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+    };
+    float h0 = 0.0f, l0 = 0.0f, h1 = 0.0f, l1 = 0.0f;
+    int i = 0;
+    for (; i + 16 <= E; i += 16) {
+      two_sum_add(h0, l0, group_sum(i / 8));
+      two_sum_add(h1, l1, group_sum(i / 8 + 1));
     }
-    for (; i + 4 <= E; i += 4) {
-#pragma unroll
-      for (int a = 0; a < 4; ++a) two_sum_add(h[a], l[a], exp_diff_fast(at(i + a), m));
+    if (i + 8 <= E) {
+      two_sum_add(h0, l0, group_sum(i / 8));
+      i += 8;
     }
-    for (; i < E; ++i) two_sum_add(h[0], l[0], exp_diff_fast(at(i), m));
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      two_sum_add(hi, lo, h[a]);
-      lo += l[a];
-    }
+    float tail = 0.0f;
+    for (; i < E; ++i) tail += __expf(at(i) - m);
+    two_sum_add(h0, l0, tail);
+    hi = h0;
+    lo = l0;
+    two_sum_add(hi, lo, h1);
+    lo += l1;
   }
   // one round: the largest remaining value and its lowest expert; refreshes the maxima
   auto take = [&](float& v, int& e) {

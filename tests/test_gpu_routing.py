@@ -76,6 +76,18 @@ def test_gating_bf16_logits(E, k, norm):
     assert torch.equal(i, i32) and torch.equal(w.view(torch.int32), w32.view(torch.int32))
 
 
+@pytest.mark.parametrize("E,gap", [(64, 1.0), (64, 2.3), (128, 2.3), (128, 4.0)])
+def test_gating_full_softmax_near_flat_rows(E, gap):
+    """norm_topk_prob = False sums all E exponentials; rows whose other logits sit
+    just below the maximum at a distance `gap` weigh the terms whose rounding
+    grows with the distance (the worst case of the denominator's error bound)."""
+    moe = need_gpu()
+    rng = np.random.default_rng(E + int(gap * 10))
+    x = (-gap + 0.05 * rng.standard_normal((513, E))).astype(np.float32)
+    x[np.arange(513), rng.integers(0, E, 513)] = 0.0
+    _gating_case(moe, x, 8, False)
+
+
 def test_gating_empty_and_single():
     moe = need_gpu()
     w, i = moe.moe_gating_softmax_topk(torch.zeros((0, 8), device=DEV), 2)
