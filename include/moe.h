@@ -264,9 +264,9 @@ MOE_API int moe_grouped_ffn_backward(const void* hidden, const void* w13, const 
  *   ws / ws_bytes: at least moe_layer_workspace_size(...) bytes; calls that may
  *     run at the same time need separate workspaces.
  * For T <= 2 (bf16, E <= 64) the grouped FFN is one kernel whose CTAs wait for
- * one another at a grid barrier (one CTA on every SM but one, all resident
- * together); if that wait runs out (moe_set_wait_limit_ns) the call sets
- * MOE_STATUS_TIMEOUT in *status and its output is not valid.
+ * one another's FC1 work (per-expert counters; one CTA on every SM but one, all
+ * resident together); if such a wait runs out (moe_set_wait_limit_ns) the call
+ * sets MOE_STATUS_TIMEOUT in *status and its output is not valid.
  */
 MOE_API size_t moe_layer_workspace_size(int dtype, int T, int H, int I, int E, int k);
 MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, const void* w13,

@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
   extern __shared__ __align__(16) int sm[];
   pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
-  if (clear && threadIdx.x == 0) *clear = 0;
+  if (clear && threadIdx.x < kDecodeSyncWords) clear[threadIdx.x] = 0;
   float* col = reinterpret_cast<float*>(sm);
   int* asm_ = sm + gate::stage_floats<EP>();                  // align_chunk's shared memory
   int32_t* s_idx = asm_ + align_smem_bytes(E) / sizeof(int);  // shared copies of the routing
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
   extern __shared__ int sm[];
   pdl_trigger();
-  if (clear && threadIdx.x == 0) *clear = 0;
+  if (clear && threadIdx.x < kDecodeSyncWords) clear[threadIdx.x] = 0;
   constexpr int groups = kThreads / L;
   for (long t = threadIdx.x / L; t < T; t += groups)
     gate::gate_one_token<L, V>(logits, t, E, k, norm, w_out, idx_out);

@@ -230,7 +230,7 @@ FfnWs carve_ffn(Carver& c, int dtype, int T, long S, int H, int I) {
   const size_t xs = ffn_uses_tensor_cores(dtype, H, I) ? ffn_tc_extra_bytes(S, H) : 0;
   w.xs = xs ? c.take<char>(xs) : nullptr;
   w.pos = xs ? c.take<int32_t>(ffn_tc_pos_bytes(S) / sizeof(int32_t)) : nullptr;
-  w.sync = c.take<int32_t>(1);
+  w.sync = c.take<int32_t>(kDecodeSyncWords);
   return w;
 }
 
@@ -594,7 +594,7 @@ MOE_API int moe_layer_forward(const void* hidden, const float* router_logits, co
   }
   // the layer's own gating only produces indices in [0, E): no slot is dropped. The
   // logits let the decode kernels start on the experts' weights before routing ends;
-  // the word the small-batch routing kernel zeroes serves the decode FFN's grid barrier.
+  // the words the small-batch routing kernel zeroes are the decode FFN's counters.
   return run_ffn(hidden, w13, w2, dtype, T, H, I, E, k, al.counts, al.offsets, al.sorted_ids,
                  al.sorted_w, al.reverse, out, fw, status, s, /*may_drop=*/false, router_logits,
                  norm_topk_prob != 0, small ? fw.sync : nullptr);

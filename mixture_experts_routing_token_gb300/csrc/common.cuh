@@ -86,8 +86,11 @@ int launch_multihot_to_indices(const float* pm, const int32_t* pos, int T, int E
                                float* probs, int32_t* idx, cudaStream_t s);
 
 size_t align_scratch_bytes(long S, int E);
+// Words of the one-kernel decode FFN's counters (per active expert, and of FC1
+// units taken; a layer workspace region that the small-batch routing kernel zeroes).
+constexpr int kDecodeSyncWords = 65;
 // Gating + align in one single-CTA launch, for at most 128 tokens whose T*k
-// slots fit one align chunk; it also zeroes *clear (when not null).
+// slots fit one align chunk; it also zeroes clear[0, kDecodeSyncWords) (when not null).
 bool route_is_small(int T, int k);
 int launch_route_small(const float* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* sorted_ids, float* sorted_w,
@@ -120,8 +123,8 @@ struct FfnArgs {
   // kernel, whose outputs it then waits for only before FC2 may start).
   const float* logits;
   int norm;
-  // A word zeroed by the routing kernel launched just before (or null): the grid
-  // barrier of the one-kernel decode FFN (ffn_gemv.cu).
+  // kDecodeSyncWords words zeroed by the routing kernel launched just before (or
+  // null): the per-expert FC1 counters of the one-kernel decode FFN (ffn_gemv.cu).
   int32_t* sync;
 };
 

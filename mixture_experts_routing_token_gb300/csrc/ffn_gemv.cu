@@ -24,16 +24,18 @@
 // Every kernel pays a fixed cost before its loads reach full rate and after
 // they drain (measured: a read-only kernel over 46 MB takes 16 us where the copy
 // bandwidth asks 7). Inside the layer call the whole FFN is therefore one
-// kernel (decode_layer_kernel): every CTA routes the batch itself; before its
-// FC1 units it requests the weight rows of its FC2 units (they do not depend on
-// FC1: the first eight units into the buffers of eight warps, the rest into L2),
-// so that DRAM streams FC2's weights together with FC1's; it then meets the other
-// CTAs at a grid barrier (a counter that the routing kernel just before it
-// zeroed, polled with a time limit) and runs FC2 on the tensor cores (mma.sync
-// on pairs of units, the later units copied into the buffers as the first ones
-// are done). Its grid leaves one SM to the routing kernel it overlaps, so that
-// every CTA of the barrier is resident. Elsewhere (routing given by the caller,
-// or E > 64) FC1 and FC2 are two kernels, FC2 on the CUDA cores.
+// kernel (decode_pipe_kernel): every CTA routes the batch itself; its FC1 warps
+// stream FC1 units (after a first unit each, in order from a counter that all
+// CTAs share, so faster SMs take more) and count each finished unit on its
+// expert's counter; its FC2 warps run behind them, one expert at a time as its
+// counter completes, on the CTA's own output columns: the expert's w2 rows for
+// those columns come into shared memory by bulk copies two of the warp's turns
+// ahead and meet the expert's activation rows on the tensor cores (mma.sync),
+// so FC2 streams with FC1 and only the last expert's FC2 and the combine follow
+// it. The counters are a workspace region that the routing kernel launched just
+// before zeroes, every wait on them is bounded, and the grid leaves one SM to
+// that routing kernel, so that every CTA is resident. Elsewhere (routing given
+// by the caller, or E > 64) FC1 and FC2 are two kernels, FC2 on the CUDA cores.
 #include "common.cuh"
 #include "gating_device.cuh"
 #include "sm100_ptx.cuh"   // smem_u32, globaltimer
@@ -42,15 +44,13 @@ namespace moe {
 namespace {
 
 constexpr int kGemvThreads = 256;                        // FC1 kernel: two CTAs per SM
-constexpr int kLayerThreads = 512;                       // layer kernel: one CTA per SM
+constexpr int kLayerThreads = 512;                       // one-kernel FFN: one CTA per SM
 constexpr int kPieces = 8;                               // FC1: 16-byte pieces per lane per row in flight
 constexpr int kMaxSlots = kGemvMaxTokens * MOE_MAX_TOPK;
 constexpr int kRouteExperts = 64;                        // in-CTA routing (gate::route_block): E <= 64
 constexpr int kFc2Buffers = 8;                           // FC2 warps with a row buffer each, at most
 constexpr int kFc2Threads = kFc2Buffers * 32;            // FC2 kernel
 constexpr size_t kFc2SmemMax = 200 * 1024;               // FC2 kernel: buffers + activation rows
-constexpr size_t kLayerSmemMax = 216 * 1024;             // layer kernel: buffers + activations + token rows
-constexpr int kMaxPairs = 4;                             // layer kernel: FC2 unit pairs per round (four warps each)
 
 struct GemvParams {
   const uint4* hidden;   // [T, H] bf16
@@ -64,9 +64,9 @@ struct GemvParams {
   __nv_bfloat16* act;    // [S, I], sorted slot order
   __nv_bfloat16* out;    // [T, H]
   const float* logits;   // route the batch inside every CTA (E <= 64), or null
-  int32_t* sync;         // layer kernel: grid barrier counter, zero at launch
+  int32_t* sync;         // one-kernel FFN: kDecodeSyncWords counters, zero at launch
   int32_t* status;
-  uint64_t wait_ns;      // limit of the grid barrier wait (moe_set_wait_limit_ns)
+  uint64_t wait_ns;      // limit of the waits on those counters and copies (moe_set_wait_limit_ns)
   int T, H, I, E, k;
 };
 
@@ -77,16 +77,13 @@ struct Fc2Layout {
   size_t slot, ring, act, x, total;
 };
 
-__host__ __device__ inline Fc2Layout fc2_layout(int T, int k, int H, int I, bool with_x) {
+__host__ __device__ inline Fc2Layout fc2_layout(int T, int k, int H, int I) {
   Fc2Layout L;
-  // the layer kernel's rows are one 16-byte piece longer: a row of I bf16 is a
-  // multiple of 128 bytes, so without it the eight rows an ldmatrix reads would
-  // all start on the same banks
-  const size_t row = (size_t)I * 2 + (with_x ? 16 : 0);
+  const size_t row = (size_t)I * 2;
   L.slot = ((size_t)k * row + 127) & ~(size_t)127;
   L.act = ((size_t)T * k * row + 127) & ~(size_t)127;
-  L.x = with_x ? (size_t)T * H * 4 : 0;
-  const size_t cap = with_x ? kLayerSmemMax : kFc2SmemMax;
+  L.x = 0;
+  const size_t cap = kFc2SmemMax;
   const size_t room = cap > L.act + L.x ? cap - L.act - L.x : 0;
   const size_t fit = room / L.slot;
   L.buffers = (int)(fit < (size_t)kFc2Buffers ? fit : (size_t)kFc2Buffers);
@@ -180,69 +177,72 @@ __device__ __forceinline__ void active_experts(const int32_t* counts, int E, int
   if (lane == 0) *a_n = min(n, kMaxSlots);
 }
 
+// FC1 unit (expert e, column i) by the calling warp: gate row i and up row I + i
+// of w13[e] against the expert's token rows (xs, float32), silu_and_mul, act
+// written by lane 0 (slot rows offsets[e] ..).
+// TT: most tokens an expert can have (the batch size bound).
+template <int TT, int PIECES = kPieces>
+__device__ __forceinline__ void fc1_unit(const GemvParams& P, const float4* xs, int e, const int32_t* counts,
+                                         const int32_t* offsets, const int32_t* sorted_ids, int i, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  const int nch = P.H >> 3;
+  const int cnt = min(counts[e], TT);
+  const int p0 = offsets[e];
+  int tok[TT];
+#pragma unroll
+  for (int r = 0; r < TT; ++r) tok[r] = r < cnt ? sorted_ids[p0 + r] : 0;
+  const uint4* g = P.w13 + ((long)e * 2 * P.I + i) * nch;
+  const uint4* up = g + (long)P.I * nch;
+  float ag[TT], au[TT];
+#pragma unroll
+  for (int r = 0; r < TT; ++r) ag[r] = au[r] = 0.0f;
+  for (int c0 = 0; c0 < nch; c0 += 32 * PIECES) {
+    uint4 wg[PIECES], wu[PIECES];
+#pragma unroll
+    for (int b = 0; b < PIECES; ++b) {
+      const int c = c0 + b * 32 + lane;
+      if (c < nch) {
+        wg[b] = ld_stream(g + c, pol);
+        wu[b] = ld_stream(up + c, pol);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < PIECES; ++b) {
+      const int c = c0 + b * 32 + lane;
+      if (c < nch) {
+#pragma unroll
+        for (int r = 0; r < TT; ++r)
+          if (r < cnt) {
+            const float4 x0 = xs[(tok[r] * nch + c) * 2], x1 = xs[(tok[r] * nch + c) * 2 + 1];
+            ag[r] = dot8f(wg[b], x0, x1, ag[r]);
+            au[r] = dot8f(wu[b], x0, x1, au[r]);
+          }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < TT; ++r) {
+    ag[r] = warp_sum(ag[r]);
+    au[r] = warp_sum(au[r]);
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int r = 0; r < TT; ++r)
+      if (r < cnt) P.act[(long)(p0 + r) * P.I + i] = __float2bfloat16_rn(silu(ag[r]) * au[r]);
+}
+
 // FC1 units u0, u0 + ustride, ... < u1 (unit u = a * I + i), taken in turn by the
 // block's warps.
-// TT: most tokens an expert can have (the batch size bound).
 template <int TT, int PIECES = kPieces>
 __device__ __forceinline__ void fc1_units(const GemvParams& P, const float4* xs, const int32_t* a_e,
                                           const int32_t* counts, const int32_t* offsets,
                                           const int32_t* sorted_ids, long u0, long u1, long ustride = 1) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const int nch = P.H >> 3;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const uint64_t pol = evict_first_policy();
   for (long u = u0 + warp * ustride; u < u1; u += nwarps * ustride) {
     const int a = (int)(u / P.I), i = (int)(u - (long)a * P.I);
-    const int e = a_e[a];
-    const int cnt = min(counts[e], TT);
-    const int p0 = offsets[e];
-    int tok[TT];
-#pragma unroll
-    for (int r = 0; r < TT; ++r) tok[r] = r < cnt ? sorted_ids[p0 + r] : 0;
-    const uint4* g = P.w13 + ((long)e * 2 * P.I + i) * nch;
-    const uint4* up = g + (long)P.I * nch;
-    float ag[TT], au[TT];
-#pragma unroll
-    for (int r = 0; r < TT; ++r) ag[r] = au[r] = 0.0f;
-    for (int c0 = 0; c0 < nch; c0 += 32 * PIECES) {
-      uint4 wg[PIECES], wu[PIECES];
-#pragma unroll
-      for (int b = 0; b < PIECES; ++b) {
-        const int c = c0 + b * 32 + lane;
-        if (c < nch) {
-          wg[b] = ld_stream(g + c, pol);
-          wu[b] = ld_stream(up + c, pol);
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < PIECES; ++b) {
-        const int c = c0 + b * 32 + lane;
-        if (c < nch) {
-#pragma unroll
-          for (int r = 0; r < TT; ++r)
-            if (r < cnt) {
-              const float4 x0 = xs[(tok[r] * nch + c) * 2], x1 = xs[(tok[r] * nch + c) * 2 + 1];
-              ag[r] = dot8f(wg[b], x0, x1, ag[r]);
-              au[r] = dot8f(wu[b], x0, x1, au[r]);
-            }
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < TT; ++r) {
-      ag[r] = warp_sum(ag[r]);
-      au[r] = warp_sum(au[r]);
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int r = 0; r < TT; ++r)
-        if (r < cnt) P.act[(long)(p0 + r) * P.I + i] = __float2bfloat16_rn(silu(ag[r]) * au[r]);
+    fc1_unit<TT, PIECES>(P, xs, a_e[a], counts, offsets, sorted_ids, i, pol);
   }
-}
-
-// Row j of FC2 unit u = c * T + t: row c of w2[s_e[t * k + j]] (a valid slot).
-__device__ __forceinline__ const uint4* fc2_row(const GemvParams& P, const int32_t* s_e, long u, int j) {
-  const int c = (int)(u / P.T), t = (int)(u - (long)c * P.T);
-  return P.w2 + ((long)s_e[t * P.k + j] * P.H + c) * (P.I >> 3);
 }
 
 // FC2 unit u = c * T + t: the weight rows of the token's valid slots (s_e[q] >= 0)
@@ -308,44 +308,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Steps [s0, s1) of K of the FC2 products of units ua and ub = ua + T (the same
-// token t), whose k weight rows sit in the shared buffers at sa and sb (rows ld
-// pieces apart; the activation rows in act likewise), for experts jb .. jb + 7,
-// by one warp on the tensor cores: A = rows j of unit ua then of unit ub (16 x K),
-// B = the token's activation rows of the same eight experts (K x 8); the products
-// wanted are D's diagonal, D[8h + j][j] = row j of unit h . act row of expert j.
-// Lane 4j + j/2 returns them: [0] for unit ua, [1] for unit ub (expert jb + j).
-__device__ __forceinline__ float2 fc2_pair_mma(const GemvParams& P, const int32_t* s_pos, uint32_t sa,
-                                               uint32_t sb, uint32_t act, int ld, int t, int jb, int s0,
-                                               int s1) {
-  const int lane = threadIdx.x & 31;
-  // A: lane l gives row (l & 15) (rows 8..15 from unit ub) at k half (l >> 4)
-  const int ja = min(jb + (lane & 7), P.k - 1);   // rows past k: any valid row, unused
-  const uint32_t arow = ((lane & 8) ? sb : sa) + (uint32_t)(ja * ld * 16) + (uint32_t)((lane >> 4) * 16);
-  // B: lane l (0..15) gives the activation row of expert jb + (l & 7) at k half (l >> 3) & 1
-  const uint32_t brow = act + (uint32_t)(s_pos[t * P.k + ja] * ld * 16) + (uint32_t)(((lane >> 3) & 1) * 16);
-  float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // even / odd steps
-  for (int st = s0; st < s1; st += 2) {
-    uint32_t a[4], b0, b1;
-    ldsm_x4(arow + st * 32, a);
-    ldsm_x2(brow + st * 32, b0, b1);
-    mma_16816(d0, a, b0, b1);
-    if (st + 1 < s1) {
-      ldsm_x4(arow + (st + 1) * 32, a);
-      ldsm_x2(brow + (st + 1) * 32, b0, b1);
-      mma_16816(d1, a, b0, b1);
-    }
-  }
-  // D[8h + j][j] sits in lane 4j + j/2, register 2h + (j & 1); in the other lanes: unused
-  const bool odd = (lane >> 2) & 1;   // j & 1 for the lane holding expert j = lane / 4
-  return make_float2(odd ? d0[1] + d1[1] : d0[0] + d1[0], odd ? d0[3] + d1[3] : d0[2] + d1[2]);
-}
-
-// Ask L2 for the 128-byte line holding p.
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p) : "memory");
-}
-
 // Rows [0, n) of the activations (bf16, written by other CTAs or the previous
 // kernel) into shared memory, read through L2.
 __device__ __forceinline__ void stage_act(const GemvParams& P, int n, uint4* act_s, int ld = 0) {
@@ -404,7 +366,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1) fc2_gemv_kernel(const GemvPara
   __shared__ int32_t s_off[MOE_MAX_EXPERTS + 1];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int S = P.T * P.k;
-  const Fc2Layout L = fc2_layout(P.T, P.k, P.H, P.I, false);
+  const Fc2Layout L = fc2_layout(P.T, P.k, P.H, P.I);
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fc2_raw) + 127) & ~uintptr_t(127));
   uint4* act_s = reinterpret_cast<uint4*>(base + L.ring);               // [n][I / 8]
   uint4* buf = reinterpret_cast<uint4*>(base + (size_t)warp * L.slot);   // this warp's rows [k][I / 8]
@@ -445,40 +407,70 @@ __global__ void __launch_bounds__(kFc2Threads, 1) fc2_gemv_kernel(const GemvPara
   if (warp < L.buffers) fc2_units(P, s_pos, s_e, s_w, act_s, buf, u0, nloc, L.buffers);
 }
 
-// Bounded grid barrier (thread 0 of each CTA, between __syncthreads): count this
-// CTA in and wait until all `nblocks` have arrived. False when the limit ran out.
-__device__ __forceinline__ bool grid_barrier(int32_t* ctr, int nblocks, uint64_t limit_ns) {
-  __threadfence();   // this CTA's activations before its arrival
-  atomicAdd(ctr, 1);
-  const uint64_t t0 = ptx::globaltimer();
-  for (;;) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= nblocks) return true;
-    if (ptx::globaltimer() - t0 > limit_ns) return false;
-    __nanosleep(64);
-  }
+// ---- the pipelined one-kernel decode FFN ------------------------------------
+// FC1 warps (the first kPipeFc1Warps) stream FC1 units b, b + G, ... of the flat
+// range [0, a_n * I) (CTA b of G; every CTA finishes expert a's units at about
+// the same time, experts in order) and count each finished unit on its expert's
+// counter (done[a], zeroed by the routing kernel launched just before; the
+// activation is stored and fenced first). The other warps run FC2 behind them:
+// the CTA owns output columns [c0, c1); for each active expert in turn they wait
+// (bounded) until its I units are counted, stage its activation rows, and take
+// the dot products of their columns' w2 rows (asked of L2 at the start) with
+// them into shared memory, so FC2 of expert a overlaps FC1 of the later experts
+// and only the last expert's FC2 and the combine follow the FC1 stream. One
+// warp keeps pace: its products are mma.sync tiles (16 w2 rows x the expert's
+// activation rows) over rows that bulk copies (one per row, two experts ahead)
+// bring into shared memory. The combine: out[t][c] = sum
+// over j of w_j * (row c of w2[e_j] . act_j), float32 in j order, rounded once.
+constexpr int kPipeFc2Warps = 2;    // each takes every other expert
+constexpr int kPipeFc1Warps = kLayerThreads / 32 - kPipeFc2Warps;
+constexpr int kPipeFc2Threads = kPipeFc2Warps * 32;
+constexpr int kPipeCols = 32;   // most output columns per CTA
+static_assert(kMaxSlots + 1 <= kDecodeSyncWords, "one counter per active expert, one of FC1 units taken");
+
+// bytes (a multiple of 16) global -> shared by the TMA engine, completing on bar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
-// The whole FFN of a batch of at most TT tokens inside the layer call (logits
-// given, E <= 64), one CTA on every SM but one. See the file comment.
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Shared memory of decode_pipe_kernel: token rows [T][H] (float32), then per FC2
+// warp its activation rows [TT][I + 8] and nb buffers of the CTA's w2 rows of one
+// expert [ceil(H / G)][I + 8] (bf16, rows padded by 16 bytes); nb = 2 where that
+// fits (the rows of an expert two of the warp's turns ahead in flight), else 1.
+constexpr size_t kPipeSmemMax = 220 * 1024;
+__host__ __device__ inline size_t pipe_smem_nb(int T, int TT, int H, int I, int G, int nb) {
+  return (size_t)T * H * 4 + (size_t)kPipeFc2Warps * ((size_t)TT + (size_t)nb * ((H + G - 1) / G)) * (I + 8) * 2;
+}
+__host__ __device__ inline int pipe_buffers(int T, int TT, int H, int I, int G) {
+  return pipe_smem_nb(T, TT, H, I, G, 2) <= kPipeSmemMax ? 2 : 1;
+}
+__host__ __device__ inline size_t pipe_smem(int T, int TT, int H, int I, int G) {
+  return pipe_smem_nb(T, TT, H, I, G, pipe_buffers(T, TT, H, I, G));
+}
+
 template <int TT>
-__global__ void __launch_bounds__(kLayerThreads, 1) decode_layer_kernel(const GemvParams P) {
-  extern __shared__ uint8_t lay_raw[];
+__global__ void __launch_bounds__(kLayerThreads, 1) decode_pipe_kernel(const GemvParams P) {
+  extern __shared__ float4 pipe_raw[];
   __shared__ int32_t l_idx[kMaxSlots], l_ids[kMaxSlots];
   __shared__ int32_t l_cnt[kRouteExperts], l_off[kRouteExperts + 1], l_run[kRouteExperts];
   __shared__ int32_t a_e[kMaxSlots];
   __shared__ int32_t s_pos[kMaxSlots];
   __shared__ float s_w[kMaxSlots];
-  __shared__ float part[kMaxPairs * 4 * 16];
-  __shared__ int a_n, go;
+  __shared__ float part[kMaxSlots * kPipeCols];   // [sorted slot][column - c0]
+  __shared__ int a_n, abort_flag;
+  __shared__ __align__(8) uint64_t wbar[kPipeFc2Warps * 2];   // each row buffer's copies
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = P.T * P.k;
-  const Fc2Layout L = fc2_layout(P.T, P.k, P.H, P.I, true);
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lay_raw) + 127) & ~uintptr_t(127));
-  uint4* act_s = reinterpret_cast<uint4*>(base + L.ring);
-  float4* xs = reinterpret_cast<float4*>(base + L.ring + L.act);
-  uint4* buf = reinterpret_cast<uint4*>(base + (size_t)warp * L.slot);
+  float4* xs = pipe_raw;                                                   // [T][H / 4]
+  uint4* acts = reinterpret_cast<uint4*>(pipe_raw + (long)P.T * P.H / 4);  // [W][TT][I / 8 + 1]
+  uint4* wbuf = acts + (long)kPipeFc2Warps * TT * ((P.I >> 3) + 1);         // [W][nb][ceil(H / G)][I / 8 + 1]
   // the token rows by the warps that do not route (their loads overlap the logits')
   for (long c = tid - 64; c >= 0 && c < (long)P.T * P.H / 8; c += kLayerThreads - 64) {
     const uint4 v = P.hidden[c];
@@ -487,95 +479,168 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_layer_kernel(const Ge
   }
   gate::route_block(P.logits, P.T, P.E, P.k, l_idx, l_cnt, l_off, l_ids, l_run, s_pos);
   active_experts(l_cnt, P.E, a_e, &a_n);
+  if (tid == 0) abort_flag = 0;
   __syncthreads();
-  const int G = gridDim.x;
-  const long U2 = (long)P.H * P.T;
-  const long u0 = U2 * blockIdx.x / G, u1 = U2 * (blockIdx.x + 1) / G;
-  const int nloc = (int)(u1 - u0);
-  // ---- FC2 weight rows (they do not depend on FC1), requested now so that DRAM
-  // streams them together with FC1's: the first unit of each FC2 warp into its
-  // buffer, the rows of the CTA's later units into L2
-  const int ld = (P.I >> 3) + 1;   // row stride of the buffers and activation rows, 16-byte pieces
-  if (warp < L.buffers && warp < nloc) fc2_fetch(P, l_idx, u0 + warp, buf, ld);
-  {
-    const int lpr = P.I / 64;   // 128-byte lines per row
-    const long nl = (long)max(nloc - L.buffers, 0) * P.k * lpr;
-    for (long x = tid; x < nl; x += kLayerThreads) {
-      const long r = x / lpr;
-      const int i = L.buffers + (int)(r / P.k), j = (int)(r - (long)(r / P.k) * P.k);
-      prefetch_line_l2(reinterpret_cast<const char*>(fc2_row(P, l_idx, u0 + i, j)) + (x - r * lpr) * 128);
-    }
-  }
-  // ---- FC1
-  const long U1 = (long)a_n * P.I;
-  fc1_units<TT>(P, xs, a_e, l_cnt, l_off, l_ids, blockIdx.x, U1, G);   // units b, b + G, ... of CTA b
-  // ---- the routing kernel is complete (barrier counter zeroed, routing weights
-  // written); then every CTA's activations
-  pdl_wait();
-  pdl_trigger();
-  if (tid < S) s_w[tid] = __ldg(P.sorted_w + s_pos[tid]);
-  cp_async_wait_all();   // this warp's buffered rows land before the CTA may leave
-  __syncthreads();
-  if (tid == 0) {
-    go = grid_barrier(P.sync, G, P.wait_ns);
-    if (!go && P.status) atomicOr(P.status, MOE_STATUS_TIMEOUT);
-  }
-  __syncthreads();
-  if (!go) return;
-  stage_act(P, S, act_s, ld);
-  __syncthreads();
-  // ---- FC2 on the tensor cores, in rounds of L.buffers units (unit r0 + b in
-  // buffer b): the pairs of units (b, b + T) of one token, each pair by four warps
-  // (a quarter of K each), which own the pair's two buffers: after a round they
-  // refill them with the pair's units of the next round (rows asked of L2 at the
-  // start) while the other pairs compute.
-  const int B = L.buffers, T2 = 2 * P.T;
-  const int npairs = (B + T2 - 1) / T2 * P.T;
-  const int pr = warp >> 2, qw = warp & 3;       // pair of this warp, its quarter
-  const int ksteps = (P.I >> 3) >> 1;            // 16 bf16 per step
-  if (pr < npairs && pr < kMaxPairs) {
-    const int b0 = pr / P.T * T2 + pr % P.T, b1 = b0 + P.T;
-    uint4* buf0 = reinterpret_cast<uint4*>(base + (size_t)b0 * L.slot);
-    uint4* buf1 = reinterpret_cast<uint4*>(base + (size_t)b1 * L.slot);
-    const int s0 = ksteps * qw / 4, s1 = ksteps * (qw + 1) / 4;
-    float* dg = part + pr * 4 * 16;              // [quarter][h * 8 + j]
-    for (int r0 = 0; r0 < nloc && b0 < B; r0 += B) {
-      const int nr = min(B, nloc - r0);
-      if (b0 >= nr) break;
-      const bool two = b1 < nr;
-      const long ua = u0 + r0 + b0;
-      const int t = (int)(ua % P.T);
-      if (r0 > 0) {   // rows qw, qw + 4, ... of both units
-        fc2_fetch(P, l_idx, ua, buf0, ld, qw, 4);
-        if (two) fc2_fetch(P, l_idx, ua + P.T, buf1, ld, qw, 4);
-        cp_async_wait_all();
-        ptx::named_bar_sync(1 + pr, 128);
+  const int G = gridDim.x, b = blockIdx.x;
+  const int I = P.I, nch = I >> 3;
+  int32_t* done = P.sync;   // [kMaxSlots]: FC1 units finished per active expert
+  if (warp < kPipeFc1Warps) {
+    // every warp's first unit is b + G * warp; later units are taken in order from a
+    // counter shared by all CTAs (the next one requested while the current one
+    // streams), so CTAs that run faster take more of them and the experts still
+    // complete in order
+    const uint64_t pol = evict_first_policy();
+    const long U1 = (long)a_n * I, nfirst = (long)kPipeFc1Warps * G;
+    int32_t* work = P.sync + kMaxSlots;
+    long u = b + (long)G * warp;
+    int next = 0;
+    for (bool first = true; u < U1; first = false) {
+      if (!first && lane == 0) next = atomicAdd(work, 1);
+      const int a = (int)(u / I), i = (int)(u - (long)a * I);
+      fc1_unit<TT>(P, xs, a_e[a], l_cnt, l_off, l_ids, i, pol);
+      if (first) {   // the routing kernel (complete from here on) zeroed the counters
+        pdl_wait();
+        if (lane == 0) next = atomicAdd(work, 1);
       }
-      float acc0 = 0.0f, acc1 = 0.0f;
-      for (int jb = 0; jb < P.k; jb += 8) {
-        const float2 d = fc2_pair_mma(P, s_pos, ptx::smem_u32(buf0), ptx::smem_u32(two ? buf1 : buf0),
-                                      ptx::smem_u32(act_s), ld, t, jb, s0, s1);
-        const int j = lane >> 2;
-        if ((lane & 3) == (j >> 1)) {   // lane 4j + j/2 holds expert j's products
-          dg[qw * 16 + j] = d.x;
-          dg[qw * 16 + 8 + j] = d.y;
+      if (lane == 0)   // the activation (this lane's store) before its count
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(done + a) : "memory");
+      u = nfirst + __shfl_sync(0xffffffffu, next, 0);
+    }
+    return;   // no barrier of the whole CTA follows
+  }
+  // ---- the FC2 warps: warp f takes the active experts a = f, f + kPipeFc2Warps, ...
+  // with its own activation rows and nb row buffers
+  const int f = warp - kPipeFc1Warps, ftid = tid - kPipeFc1Warps * 32;
+  const int S = P.T * P.k;
+  const int c0 = (int)((long)P.H * b / G), c1 = (int)((long)P.H * (b + 1) / G), nc = c1 - c0;
+  const int ld = nch + 1;   // row stride in shared memory, 16-byte pieces (ldmatrix: distinct banks)
+  const long wstride = (long)((P.H + G - 1) / G) * ld;   // one buffer of rows
+  const int nb = pipe_buffers(P.T, TT, P.H, P.I, G);     // row buffers per FC2 warp
+  uint4* my_acts = acts + (long)f * TT * ld;
+  uint4* my_buf = wbuf + (long)f * nb * wstride;
+  uint64_t* my_bar = wbar + f * 2;
+  if (lane == 0) {
+    for (int z = 0; z < nb; ++z) ptx::mbar_init(ptx::smem_u32(&my_bar[z]), 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  // this CTA's w2 rows of expert a (rows c0 .. c1 - 1) into buffer (a / W) % nb: one bulk
+  // copy per row by lane 0 (rows padded in shared memory), completing on its mbarrier;
+  // the n-th use of a buffer completes phase n % 2
+  constexpr int W = kPipeFc2Warps;
+  auto slot = [&](int a) { return (a / W) % nb; };
+  auto phase = [&](int a) { return (uint32_t)((a / W / nb) & 1); };
+  int fetched = f;   // this warp's experts whose rows were requested: f, f + W, ... < fetched
+  auto fetch = [&](int a) {
+    if (a >= a_n) return;
+    fetched = a + W;
+    if (lane == 0) {
+      const uint32_t bar = ptx::smem_u32(&my_bar[slot(a)]);
+      ptx::mbar_arrive_expect_tx(bar, (uint32_t)nc * I * 2);
+      const char* src = reinterpret_cast<const char*>(P.w2 + ((long)a_e[a] * P.H + c0) * nch);
+      const uint32_t dst = ptx::smem_u32(my_buf + slot(a) * wstride);
+      for (int r = 0; r < nc; ++r) bulk_load(dst + (uint32_t)(r * ld * 16), src + (long)r * I * 2, I * 2, bar);
+    }
+  };
+  for (int z = 0; z < nb; ++z) fetch(f + z * W);
+  pdl_wait();   // the routing kernel's weights
+  for (int q = ftid; q < S; q += kPipeFc2Threads) s_w[q] = __ldg(P.sorted_w + s_pos[q]);
+  const uint4* act4 = reinterpret_cast<const uint4*>(P.act);
+  const int ksteps = I >> 4;   // 16 bf16 per mma step
+  bool aborted = false;
+  int a = f;
+  for (; a < a_n; a += W) {
+    const int e = a_e[a], cnt = min(l_cnt[e], TT), p0 = l_off[e];
+    bool ready = true;
+    if (lane == 0) {
+      const uint64_t t0 = ptx::globaltimer();
+      while (ld_acquire(done + a) < I) {
+        if (ptx::globaltimer() - t0 > P.wait_ns || abort_flag) {
+          ready = false;
+          break;
         }
-        ptx::named_bar_sync(1 + pr, 128);
-        if (qw == 0 && lane == 0)
-          for (int jj = 0; jj < 8 && jb + jj < P.k; ++jj) {
-            const float w = s_w[t * P.k + jb + jj];
-            acc0 = fmaf(w, (dg[jj] + dg[16 + jj]) + (dg[32 + jj] + dg[48 + jj]), acc0);
-            acc1 = fmaf(w, (dg[8 + jj] + dg[24 + jj]) + (dg[40 + jj] + dg[56 + jj]), acc1);
-          }
-        ptx::named_bar_sync(1 + pr, 128);   // dg and the buffers are free again
-      }
-      if (qw == 0 && lane == 0) {
-        const int ca = (int)(ua / P.T);
-        P.out[(long)t * P.H + ca] = __float2bfloat16_rn(acc0);
-        if (two) P.out[(long)t * P.H + ca + 1] = __float2bfloat16_rn(acc1);
+        __nanosleep(32);
       }
     }
+    if (!__shfl_sync(0xffffffffu, ready, 0)) {
+      aborted = true;
+      break;
+    }
+    for (int r = 0; r < cnt; ++r)   // the expert's activation rows (bf16)
+      for (int pc = lane; pc < nch; pc += 32) my_acts[r * ld + pc] = __ldcg(act4 + (long)(p0 + r) * nch + pc);
+    const bool rows = ptx::mbar_wait(ptx::smem_u32(&my_bar[slot(a)]), phase(a), &abort_flag, P.wait_ns);
+    if (!__all_sync(0xffffffffu, rows)) {   // the rows (every lane leaves together)
+      aborted = true;
+      break;
+    }
+    __syncwarp();
+    // D (16 columns x 8 slots) = A (16 w2 rows x I) * B (I x the expert's activation rows), on the
+    // tensor cores; rows past nc / cnt repeat a valid row and their products are not kept
+    const uint32_t wb = ptx::smem_u32(my_buf + slot(a) * wstride), ab = ptx::smem_u32(my_acts);
+    const uint32_t brow = ab + (uint32_t)(min(lane & 7, cnt - 1) * ld * 16) + (uint32_t)(((lane >> 3) & 1) * 16);
+    for (int m0 = 0; m0 < nc; m0 += 16) {
+      const uint32_t arow = wb + (uint32_t)(min(m0 + (lane & 15), nc - 1) * ld * 16) + (uint32_t)((lane >> 4) * 16);
+      // four accumulators (steps st mod 4), the four steps' fragments loaded before their mma
+      float d[4][4];
+#pragma unroll
+      for (int z = 0; z < 4; ++z) d[z][0] = d[z][1] = d[z][2] = d[z][3] = 0.0f;
+      int st = 0;
+      for (; st + 4 <= ksteps; st += 4) {
+        uint32_t fa[4][4], fb[4][2];
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+          ldsm_x4(arow + (st + z) * 32, fa[z]);
+          ldsm_x2(brow + (st + z) * 32, fb[z][0], fb[z][1]);
+        }
+#pragma unroll
+        for (int z = 0; z < 4; ++z) mma_16816(d[z], fa[z], fb[z][0], fb[z][1]);
+      }
+#pragma unroll
+      for (int z = 0; z < 3; ++z)   // the last ksteps % 4 steps
+        if (st + z < ksteps) {
+          uint32_t fa[4], b0, b1;
+          ldsm_x4(arow + (st + z) * 32, fa);
+          ldsm_x2(brow + (st + z) * 32, b0, b1);
+          mma_16816(d[z], fa, b0, b1);
+        }
+      // lane l holds D[l / 4 (+ 8)][2 (l % 4) + (0, 1)]
+      const int m = m0 + (lane >> 2), n = 2 * (lane & 3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (m + 8 * h < nc && n + q < cnt)
+            part[(p0 + n + q) * kPipeCols + m + 8 * h] =
+                (d[0][2 * h + q] + d[1][2 * h + q]) + (d[2][2 * h + q] + d[3][2 * h + q]);
+    }
+    __syncwarp();   // this warp's activation rows and buffer are free again
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before the copy engine rewrites the buffer
+    fetch(a + nb * W);
   }
+  if (aborted) {
+    if (lane == 0) {   // no copy in flight when the CTA leaves: experts a, a + W, .. < fetched
+      abort_flag = 1;
+      if (P.status) atomicOr(P.status, MOE_STATUS_TIMEOUT);
+      const uint64_t t0 = ptx::globaltimer();
+      for (int x = a; x < fetched; x += W)
+        while (!ptx::mbar_test_wait(ptx::smem_u32(&my_bar[slot(x)]), phase(x)) && ptx::globaltimer() - t0 < P.wait_ns) {
+        }
+    }
+    __syncwarp();
+  }
+  ptx::named_bar_sync(1, kPipeFc2Threads);   // every FC2 warp's products (and abort_flag) are in
+  if (!abort_flag) {
+    for (int x = ftid; x < P.T * nc; x += kPipeFc2Threads) {
+      const int t = x / nc, cc = x - t * nc;
+      float acc = 0.0f;
+      for (int j = 0; j < P.k; ++j) {
+        const int q = t * P.k + j;
+        acc = fmaf(s_w[q], part[s_pos[q] * kPipeCols + cc], acc);
+      }
+      P.out[(long)t * P.H + c0 + cc] = __float2bfloat16_rn(acc);
+    }
+  }
+  pdl_trigger();   // only now may the next kernel (which zeroes the counters again) start
 }
 
 template <typename K>
@@ -595,14 +660,15 @@ int run_gemv(const FfnArgs& a, cudaStream_t s) {
                      static_cast<const uint4*>(a.w2), a.counts, a.offsets, a.sorted_ids, a.sorted_w, a.reverse,
                      static_cast<__nv_bfloat16*>(a.act), static_cast<__nv_bfloat16*>(a.out),
                      local ? a.logits : nullptr, a.sync, a.status, wait_limit_ns(), a.T, a.H, a.I, a.E, a.k};
-  const Fc2Layout LL = fc2_layout(a.T, a.k, a.H, a.I, true);
   const int G = num_sms() - 1;
-  if (local && a.sync && LL.buffers >= 2 && G >= 1)
-    return launch_one(decode_layer_kernel<TT>, G, kLayerThreads, LL.total, s, p, "ffn_decode_layer");
+  if (local && a.sync && G >= 1 && (a.H + G - 1) / G <= kPipeCols && (a.H * 2) % 128 == 0 && (a.I * 2) % 128 == 0 &&
+      pipe_smem(a.T, TT, a.H, a.I, G) <= kPipeSmemMax)
+    return launch_one(decode_pipe_kernel<TT>, G, kLayerThreads, pipe_smem(a.T, TT, a.H, a.I, G), s, p,
+                      "ffn_decode_layer");
   const int rc = launch_one(fc1_gemv_kernel<TT>, 2 * num_sms(), kGemvThreads, (size_t)a.T * a.H * 4, s, p,
                             "ffn_fc1_gemv");
   if (rc) return rc;
-  return launch_one(fc2_gemv_kernel, num_sms(), kFc2Threads, fc2_layout(a.T, a.k, a.H, a.I, false).total, s, p,
+  return launch_one(fc2_gemv_kernel, num_sms(), kFc2Threads, fc2_layout(a.T, a.k, a.H, a.I).total, s, p,
                     "ffn_fc2_gemv");
 }
 
@@ -610,7 +676,7 @@ int run_gemv(const FfnArgs& a, cudaStream_t s) {
 
 bool ffn_gemv_applies(int dtype, int T, int H, int I, int k) {
   return ffn_uses_tensor_cores(dtype, H, I) && T >= 1 && T <= kGemvMaxTokens &&
-         (size_t)T * H * 4 <= kGemvSmemMax && fc2_layout(T, k, H, I, false).buffers >= 2;
+         (size_t)T * H * 4 <= kGemvSmemMax && fc2_layout(T, k, H, I).buffers >= 2;
 }
 
 int launch_ffn_gemv(const FfnArgs& a, cudaStream_t s) {

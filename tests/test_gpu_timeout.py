@@ -6,8 +6,8 @@ issued finish, free its tensor memory, report MOE_STATUS_TIMEOUT in the call's
 status word and return. The context must stay usable: with the default limit
 restored, the next call matches the oracle and reports nothing.
 No GPU fault is involved: the waits that run out are the kernels' own
-mbarrier waits on their other roles, or (one token) the wait of the
-one-kernel decode FFN's CTAs for each other at its grid barrier.
+mbarrier waits on their other roles, or (one token) the one-kernel decode
+FFN's waits for the other CTAs' FC1 work (its per-expert counters).
 """
 import numpy as np
 import pytest
@@ -20,7 +20,7 @@ from oracle import ffn
 pytestmark = pytest.mark.gpu
 
 
-# prefill pair kernels; decode weight-streaming kernels; the one-kernel decode FFN's grid barrier
+# prefill pair kernels; decode weight-streaming kernels; the one-kernel decode FFN's counter waits
 @pytest.mark.parametrize("T", [600, 8, 1])
 def test_expired_waits_report_timeout_and_leave_the_context_usable(T):
     moe = need_gpu()
