@@ -159,16 +159,39 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
     }
     if (bi / V == g) taken |= 1ull << (bi - base);
   };
-  if (L == 1 && k <= kRegSel) {   // one thread per token: the selected logits stay in registers
-    float sel[kRegSel];
+  if (L == 1 && k <= kRegSel) {
+    // one thread per token, the row in registers: each round an arg-max tree over
+    // the row (a right node wins only when strictly larger: the lower expert among
+    // equal values), the winner then set to -inf; the selected numerators are kept
+    // (the first, exp(m - m), is exactly 1)
+    float w[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) w[i] = base + i < E ? v[i] : -INFINITY;
+    float ex[kRegSel];
+    int sid[kRegSel];
 #pragma unroll
     for (int j = 0; j < kRegSel; ++j) {
+      ex[j] = 0.0f;
+      sid[j] = 0;
       if (j < k) {
-        int bi;
-        take(sel[j], bi);
-        if (j == 0) m = sel[0];
-        if (norm) two_sum_add(hi, lo, exp_diff(sel[j], m));
-        idx_out[t * k + j] = bi;
+        float tv[V];
+        int ti[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) { tv[i] = w[i]; ti[i] = i; }
+#pragma unroll
+        for (int st = 1; st < V; st *= 2)
+#pragma unroll
+          for (int i = 0; i + st < V; i += 2 * st) {
+            const bool right = tv[i + st] > tv[i];
+            tv[i] = right ? tv[i + st] : tv[i];
+            ti[i] = right ? ti[i + st] : ti[i];
+          }
+        if (j == 0) m = tv[0];
+        sid[j] = base + ti[0];
+#pragma unroll
+        for (int i = 0; i < V; ++i) w[i] = i == ti[0] ? -INFINITY : w[i];
+        ex[j] = j == 0 ? 1.0f : exp_diff(tv[0], m);
+        if (norm) two_sum_add(hi, lo, ex[j]);
       }
     }
     if (!norm) {
@@ -177,9 +200,20 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
         if (base + i < E) two_sum_add(hi, lo, exp_diff(v[i], m));
     }
     const float denom = hi + lo;
+    float wj[kRegSel];
+#pragma unroll
+    for (int j = 0; j < kRegSel; ++j) wj[j] = j < k ? __fdiv_rn(ex[j], denom) : 0.0f;
+    if (k == 2) {   // the row's two results as one 8-byte store each (outputs 16-byte aligned)
+      reinterpret_cast<float2*>(w_out)[t] = make_float2(wj[0], wj[1]);
+      reinterpret_cast<int2*>(idx_out)[t] = make_int2(sid[0], sid[1]);
+      return;
+    }
 #pragma unroll
     for (int j = 0; j < kRegSel; ++j)
-      if (j < k) w_out[t * k + j] = __fdiv_rn(exp_diff(sel[j], m), denom);
+      if (j < k) {
+        w_out[t * k + j] = wj[j];
+        idx_out[t * k + j] = sid[j];
+      }
     return;
   }
   for (int j = 0; j < k; ++j) {
