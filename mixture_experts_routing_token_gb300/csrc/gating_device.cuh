@@ -420,11 +420,9 @@ __host__ __device__ constexpr int stage_floats() { return stage_bytes<EP, float>
 // maximum. RM true: the group maxima live in registers and the first group is
 // found by an arg-max tree (a right node wins only when strictly larger); the
 // group read is the round's only shared-memory round trip (measured faster for
-// float32 rows of 128 experts, which are latency-bound at 3 blocks per SM).
-// RM false: the group maxima live in shared memory after the rows and the maxima
-// of 4 consecutive groups ("supers") in registers (fewer instructions: faster
-// where the kernel is issue-bound, the norm = False exponentials and 16-bit
-// stages). Every choice is a select, not a branch: all threads of a warp run the
+// float32 rows of 64-128 experts). RM false: the group maxima live in shared
+// memory after the rows and the maxima of 4 consecutive groups ("supers") in
+// registers (fewer instructions: faster for the 16-bit stages). Every choice is a select, not a branch: all threads of a warp run the
 // same instructions.
 //
 // TO_COL (k <= kRegSel): instead of w_out / idx_out, the results go to the row's

@@ -40,9 +40,10 @@ constexpr int kSmemGateThreads = gate::kStageRows;
 // Staged as 16-bit patterns: bf16 logits with at least 64 experts.
 template <int EP, typename In>
 using StageT = typename std::conditional<!std::is_same<In, float>::value && EP >= 64, uint16_t, float>::type;
-// Group maxima in registers (gate::topk_staged_row): float32 rows of up to 128 experts.
+// Group maxima in registers (gate::topk_staged_row): float32 rows of 64-128 experts
+// (measured faster there; the 16-bit stages keep them in shared memory).
 template <int EP, typename In>
-constexpr bool kRegMax = std::is_same<StageT<EP, In>, float>::value && EP == 128;
+constexpr bool kRegMax = std::is_same<StageT<EP, In>, float>::value && EP >= 64;
 
 // The parked results of the block's rows (gate::topk_staged_row<TO_COL>: weights
 // as words 0..k-1, indices as words 8..8+k-1 of each row's first chunks) written
