@@ -396,6 +396,23 @@ __device__ __forceinline__ void load_group8(const uint16_t* col, int g, int r, f
   x[4] = lo_bf16(q.z); x[5] = hi_bf16(q.z); x[6] = lo_bf16(q.w); x[7] = hi_bf16(q.w);
 }
 
+// The largest of the 8 staged values of group g of row r: float32 as a tree of
+// maxima; 16-bit patterns of bf16 by packed bf16 pair maxima (the value is what
+// matters: equal values, -0 and +0 included, compare equal as float32 later).
+template <typename Lay = StagePadded>
+__device__ __forceinline__ float group_max8(const float* col, int g, int r) {
+  float y[8];
+  load_group8<Lay>(col, g, r, y);
+  return fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])), fmaxf(fmaxf(y[4], y[5]), fmaxf(y[6], y[7])));
+}
+template <typename Lay = StagePadded>
+__device__ __forceinline__ float group_max8(const uint16_t* col, int g, int r) {
+  const uint4 q = reinterpret_cast<const uint4*>(col)[Lay::chunk(g, r)];
+  auto h2 = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); };
+  const __nv_bfloat162 m = __hmax2(__hmax2(h2(q.x), h2(q.y)), __hmax2(h2(q.z), h2(q.w)));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
 // Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: EP / VE
 // chunk columns of Lay::kRowsLd 16-byte chunks, then (RM false) the float maxima
 // of the rows' groups of 8 [EP / 8][kStageLd].
@@ -447,9 +464,7 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
   for (int q = 0; q < S; ++q) sm[q] = -INFINITY;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float y[8];
-    load_group8<Lay>(col, g, r, y);
-    const float x = fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])), fmaxf(fmaxf(y[4], y[5]), fmaxf(y[6], y[7])));
+    const float x = group_max8<Lay>(col, g, r);
     if constexpr (RM) gmx[g] = x;
     else gat(g) = x;
     sm[g / 4] = fmaxf(sm[g / 4], x);
