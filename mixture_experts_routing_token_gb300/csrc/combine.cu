@@ -67,7 +67,9 @@ __device__ __forceinline__ void store_out<__nv_bfloat16, 8>(__nv_bfloat16* o, co
 }
 
 // One thread per N = 16 / sizeof(InT) columns of a token (HV = H / N units per row).
-template <class InT, class OutT>
+// K > 0: k == K known at compile time, and all K loads are issued before the sum
+// (the same j order); K == 0: any k.
+template <class InT, class OutT, int K>
 __global__ void __launch_bounds__(256) combine_vec_kernel(const InT* __restrict__ staging, long T, int k,
                                                           int HV, OutT* __restrict__ out, int sh) {
   constexpr int N = Vec16<InT>::N;
@@ -78,12 +80,25 @@ __global__ void __launch_bounds__(256) combine_vec_kernel(const InT* __restrict_
     const long t = div_idx(i, HV, sh);
     const int c = (int)(i - t * HV);
     const InT* src = staging + (t * k * HV + c) * N;
-    float acc[N], v[N];
-    Vec16<InT>::load(src, acc);
-    for (int j = 1; j < k; ++j) {
-      Vec16<InT>::load(src + (long)j * HV * N, v);
+    float acc[N];
+    if constexpr (K > 0) {
+      float v[K][N];
 #pragma unroll
-      for (int q = 0; q < N; ++q) acc[q] += v[q];
+      for (int j = 0; j < K; ++j) Vec16<InT>::load(src + (long)j * HV * N, v[j]);
+#pragma unroll
+      for (int q = 0; q < N; ++q) acc[q] = v[0][q];
+#pragma unroll
+      for (int j = 1; j < K; ++j)
+#pragma unroll
+        for (int q = 0; q < N; ++q) acc[q] += v[j][q];
+    } else {
+      float v[N];
+      Vec16<InT>::load(src, acc);
+      for (int j = 1; j < k; ++j) {
+        Vec16<InT>::load(src + (long)j * HV * N, v);
+#pragma unroll
+        for (int q = 0; q < N; ++q) acc[q] += v[q];
+      }
     }
     store_out<OutT, N>(out + i * N, acc);
   }
@@ -129,8 +144,14 @@ int launch_t(const InT* staging, int T, int k, int H, OutT* out, cudaStream_t s)
   const long cap = (long)num_sms() * 8;
   const int grid = (int)std::max(1L, std::min(cap, (units + 255) / 256));
   cudaError_t e;
-  if (vec)
-    e = launch_pdl(combine_vec_kernel<InT, OutT>, grid, 256, 0, s, staging, (long)T, k, H / N, out,
+  if (vec && k == 8)
+    e = launch_pdl(combine_vec_kernel<InT, OutT, 8>, grid, 256, 0, s, staging, (long)T, k, H / N, out,
+                   pow2_shift(H / N));
+  else if (vec && k == 2)
+    e = launch_pdl(combine_vec_kernel<InT, OutT, 2>, grid, 256, 0, s, staging, (long)T, k, H / N, out,
+                   pow2_shift(H / N));
+  else if (vec)
+    e = launch_pdl(combine_vec_kernel<InT, OutT, 0>, grid, 256, 0, s, staging, (long)T, k, H / N, out,
                    pow2_shift(H / N));
   else if constexpr (std::is_same<InT, float>::value)
     e = launch_pdl(combine_scalar_kernel<OutT>, grid, 256, 0, s, staging, (long)T, k, H, out, pow2_shift(H));
