@@ -37,8 +37,8 @@ def test_gating_on_workload_logits(name):
 
 
 @pytest.mark.parametrize("E,k", [(1, 1), (2, 1), (3, 2), (5, 5), (7, 3), (8, 8), (16, 4), (31, 1),
-                                 (32, 32), (33, 8), (100, 6), (128, 1), (200, 16), (256, 8),
-                                 (1000, 32), (1024, 2)])
+                                 (32, 32), (33, 8), (64, 4), (96, 8), (100, 6), (128, 1), (128, 8), (200, 16),
+                                 (256, 8), (1000, 32), (1024, 2)])
 @pytest.mark.parametrize("norm", [True, False])
 def test_gating_shapes(E, k, norm):
     moe = need_gpu()
@@ -59,8 +59,8 @@ def test_gating_ties_go_to_lower_index(E, k):
 # bf16 logits: same indices and bit-identical weights as the float32 entry on the widened
 # rows; both within 1e-6 of the oracle. Shapes cover every kernel of the dispatch, vector and
 # scalar row loads (E % 8), and heavy ties (8-bit mantissas).
-@pytest.mark.parametrize("E,k", [(8, 2), (6, 3), (16, 4), (36, 5), (64, 8), (100, 6), (128, 8),
-                                 (256, 8), (520, 16), (1024, 32)])
+@pytest.mark.parametrize("E,k", [(8, 2), (6, 3), (16, 4), (36, 5), (64, 4), (64, 8), (96, 8), (100, 6),
+                                 (128, 8), (256, 8), (520, 16), (1024, 32)])
 @pytest.mark.parametrize("norm", [True, False])
 def test_gating_bf16_logits(E, k, norm):
     moe = need_gpu()
@@ -260,6 +260,7 @@ def _sigmoid_scores(T, E, seed):
 
 @pytest.mark.parametrize("T,E,k,n_group,topk_group", [
     (4096, 256, 8, 8, 4),      # DeepSeek-V3-shaped routing
+    (40000, 256, 8, 8, 4),     # more token groups than resident blocks: the persistent loop
     (3000, 160, 6, 8, 3),      # DeepSeek-V2-shaped routing
     (777, 64, 6, 8, 3), (100, 8, 2, 4, 2), (50, 1024, 32, 32, 7), (1, 256, 8, 8, 4), (0, 256, 8, 8, 4),
     (64, 96, 4, 3, 1), (64, 32, 3, 16, 2),
