@@ -6,8 +6,11 @@
 //
 // Gating dispatch by E: up to 8 experts one thread per token (row in
 // registers); up to 128 one thread per token over a block's rows staged in
-// shared memory; wider rows a group of L lanes per token, lane g holding the
-// V = 64 contiguous experts g*V .. g*V + V - 1 (vector loads of its run).
+// shared memory (by TMA when k <= 8 and a row is a whole number of 128-byte
+// boxes, else by cp.async); wider rows a group of L lanes per token, lane g
+// holding the V = 64 contiguous experts g*V .. g*V + V - 1 (vector loads of its
+// run). Group-limited top-k: one lane per expert group (groups of 32 with
+// coalesced row reads), or a thread / warp per token for larger groups.
 #include <float.h>
 #include <math.h>
 
