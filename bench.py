@@ -551,10 +551,11 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
     torch.cuda.synchronize()
 
     use_graph = graph_mode == "on" or (graph_mode == "auto" and T <= 64)
-    graphs = []
+    graphs, chain = [], None
     if use_graph:
-        # each batch's layer step captured once; the timed region replays them in turn
-        # (what a decode loop does)
+        # each batch's layer step captured once, and the nb steps in turn captured once
+        # more as one graph (what a decode loop does: the steps of a forward pass in one
+        # graph); the timed region replays the chain, single steps only for a remainder
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -567,18 +568,36 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
                 with torch.cuda.graph(gr, stream=side, capture_error_mode="thread_local"):
                     step(side)
                 graphs.append(gr)
+            chain = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(chain, stream=side, capture_error_mode="thread_local"):
+                for r in range(nb):
+                    count[0] = r
+                    step(side)
         torch.cuda.synchronize()
-        for gr in graphs:
+        for gr in graphs + [chain]:
             gr.replay()
         torch.cuda.synchronize()
+        count[0] = 0
+
+    def replay_steps(n, single, whole):
+        """n layer steps from graphs: the chain of all nb batches where a whole turn is left."""
+        i = 0
+        while i < n:
+            if count[0] % nb == 0 and n - i >= nb:
+                whole.replay()
+                count[0] += nb
+                i += nb
+            else:
+                single[count[0] % nb].replay()
+                count[0] += 1
+                i += 1
 
     def run(n):
+        if use_graph:
+            replay_steps(n, graphs, chain)
+            return
         for _ in range(n):
-            if use_graph:
-                graphs[count[0] % nb].replay()
-                count[0] += 1
-            else:
-                step()
+            step()
 
     if min_seconds > 0 or min_steps > 0:   # size the timed region from a short probe
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -629,21 +648,58 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
     # (H2D of step i+1 and D2H of step i-1 overlap step i, as a serving loop would).
     e2e = None
     if with_e2e and use_graph:
-        # decode batches: the whole step (pinned host inputs -> device, the layer call,
-        # the output -> pinned host) captured once per batch and replayed in turn
+        # decode batches: every step copies its inputs from pinned host memory, runs the
+        # layer call and copies its output back. Two device buffer sets: in the captured
+        # chain the H2D of step i+1 and the D2H of step i-1 run on two copy streams while
+        # step i computes; single-step graphs (a remainder) run their copies in line.
         h_hidden = [h.cpu().pin_memory() for h in hiddens]
         h_logits = [x.cpu().pin_memory() for x in logitss]
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_hidden, d_logits, d_out = torch.empty_like(hidden), torch.empty_like(logits), torch.empty_like(out)
-        gs = torch.cuda.Stream(dev)
+        h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        d_hidden = [torch.empty_like(hidden) for _ in range(2)]
+        d_logits = [torch.empty_like(logits) for _ in range(2)]
+        d_out = [torch.empty_like(out) for _ in range(2)]
+        gs, s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         gs.wait_stream(stream)
 
+        def copy_in(r):
+            d_hidden[r % 2].copy_(h_hidden[r], non_blocking=True)
+            d_logits[r % 2].copy_(h_logits[r], non_blocking=True)
+
+        def layer(r):
+            moe.moe_layer_forward(d_hidden[r % 2], d_logits[r % 2], w13, w2, k, wl.norm_topk_prob,
+                                  out=d_out[r % 2], workspace=ws, stream=gs)
+
+        def copy_out(r):
+            h_out[r % 2].copy_(d_out[r % 2], non_blocking=True)
+
         def e2e_once(r):
-            d_hidden.copy_(h_hidden[r], non_blocking=True)
-            d_logits.copy_(h_logits[r], non_blocking=True)
-            moe.moe_layer_forward(d_hidden, d_logits, w13, w2, k, wl.norm_topk_prob, out=d_out, workspace=ws,
-                                  stream=gs)
-            h_out.copy_(d_out, non_blocking=True)
+            copy_in(r)
+            layer(r)
+            copy_out(r)
+
+        def e2e_chain():
+            ev_in = [torch.cuda.Event() for _ in range(nb)]
+            ev_comp = [torch.cuda.Event() for _ in range(nb)]
+            ev_out = [torch.cuda.Event() for _ in range(nb)]
+            s_in.wait_stream(gs)
+            s_out.wait_stream(gs)
+            for r in range(nb):
+                with torch.cuda.stream(s_in):
+                    if r >= 2:
+                        s_in.wait_event(ev_comp[r - 2])   # step r-2 has read buffer set r % 2
+                    copy_in(r)
+                    ev_in[r].record(s_in)
+                gs.wait_event(ev_in[r])
+                if r >= 2:
+                    gs.wait_event(ev_out[r - 2])          # step r-2's output has been read back
+                layer(r)
+                ev_comp[r].record(gs)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_comp[r])
+                    copy_out(r)
+                    ev_out[r].record(s_out)
+            gs.wait_stream(s_in)
+            gs.wait_stream(s_out)
 
         g_e2e = []
         with torch.cuda.stream(gs):
@@ -654,28 +710,32 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
                 with torch.cuda.graph(gr, stream=gs, capture_error_mode="thread_local"):
                     e2e_once(r)
                 g_e2e.append(gr)
+            c_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(c_e2e, stream=gs, capture_error_mode="thread_local"):
+                e2e_chain()
         torch.cuda.synchronize()
-        for gr in g_e2e:
+        for gr in g_e2e + [c_e2e]:
             gr.replay()
         torch.cuda.synchronize()
+        count[0] = 0
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for i in range(steps):
-            g_e2e[i % nb].replay()
+        replay_steps(steps, g_e2e, c_e2e)
         b.record(stream)
         torch.cuda.synchronize()
         last = (steps - 1) % nb                   # the copied-back result is the last step's output
         moe.moe_layer_forward(hiddens[last], logitss[last], w13, w2, k, wl.norm_topk_prob, out=out,
                               workspace=ws, stream=stream)
         torch.cuda.synchronize()
-        assert torch.equal(h_out, out.cpu())
-        h_hidden, h_logits = h_hidden[0], h_logits[0]   # per-step copy sizes below
+        assert torch.equal(h_out[last % 2], out.cpu())
         e_ms = max_over_ranks(a.elapsed_time(b), dev)
         e2e = {"value": whole_job_rate(T, world, steps, e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size() + h_logits.numel() * 4,
-               "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "ms_per_step": e_ms / steps,
-               "copies": "pinned host buffers; each step is one CUDA graph replay of H2D copies of hidden and "
-                         "logits, the layer call and the D2H copy of the output"}
+               "h2d_bytes_per_step": h_hidden[0].numel() * h_hidden[0].element_size() + h_logits[0].numel() * 4,
+               "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(), "ms_per_step": e_ms / steps,
+               "copies": "pinned host buffers; every step does the H2D copies of its hidden and logits, the "
+                         "layer call and the D2H copy of its output, replayed from CUDA graphs as the timed "
+                         "region's steps are; in the chain of %d steps the H2D of step i+1 and the D2H of "
+                         "step i-1 overlap step i on two copy streams (two device buffer sets)" % nb}
     elif with_e2e:
         h_hidden = hidden.cpu().pin_memory()
         h_logits = logits.cpu().pin_memory()
@@ -737,7 +797,9 @@ def measure(moe, wl, dev, steps, warmup, graph_mode="auto", with_e2e=True, seed=
            "roofline": dominant_roofline(moe, wl, kern, logits, peaks, ms, prof_s=n_prof * ms / 1e3),
            "kernels": per_kernel,
            "gpu_launches_per_step": launches, "clocks": clk_rec, "e2e": e2e,
-           "timing": ("CUDA graph replay of one layer step per step" if use_graph else "eager steps") +
+           "timing": ("CUDA graph replay: the %d token batches' layer steps in turn captured as one graph "
+                      "(as a decode loop captures a forward pass), replayed steps // %d times, single-step "
+                      "graphs for the remainder" % (nb, nb) if use_graph else "eager steps") +
                      "; per-kernel CUDA events (roofline, kernels) from a timed pass of %d eager steps just "
                      "before, since events between launches serialise the programmatic dependent launches" % n_prof,
            }

@@ -435,7 +435,11 @@ __global__ void __launch_bounds__(kThreads) route_small_staged_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
   extern __shared__ __align__(16) int sm[];
-  pdl_trigger();   // first kernel of the layer: the FFN kernel may start its prologue
+  // launched while the previous kernel on the stream finishes: its writes (the logits,
+  // or the previous layer step's use of the counters cleared below) are complete after
+  // the wait; only then may the FFN kernel, which reads the logits at once, launch
+  pdl_wait();
+  pdl_trigger();
   if (clear && threadIdx.x < kDecodeSyncWords) clear[threadIdx.x] = 0;
   float* col = reinterpret_cast<float*>(sm);
   int* asm_ = sm + gate::stage_floats<EP>();                  // align_chunk's shared memory
@@ -456,6 +460,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     float* __restrict__ sorted_w, int32_t* __restrict__ reverse, int32_t* status, int32_t* clear) {
   extern __shared__ int sm[];
+  pdl_wait();   // as in route_small_staged_kernel
   pdl_trigger();
   if (clear && threadIdx.x < kDecodeSyncWords) clear[threadIdx.x] = 0;
   constexpr int groups = kThreads / L;
@@ -473,8 +478,9 @@ int launch_route_small_k(Kernel kernel, size_t smem, size_t smem_max, const floa
                          int32_t* clear, cudaStream_t s) {
   if (int rc = ensure_smem_limit(kernel, smem_max, "route_small")) return rc;
   ProfScope ps("route_small", s);
-  kernel<<<1, kThreads, smem, s>>>(logits, T, E, k, norm, w, idx, counts, offsets, sorted_ids, sorted_w,
-                                   reverse, status, clear);
+  const cudaError_t e = launch_pdl(kernel, 1, kThreads, smem, s, logits, T, E, k, norm, w, idx, counts, offsets,
+                                   sorted_ids, sorted_w, reverse, status, clear);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route_small: %s", cudaGetErrorString(e));
   return check_launch("route_small");
 }
 
