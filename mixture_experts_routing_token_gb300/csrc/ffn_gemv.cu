@@ -477,8 +477,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_pipe_kernel(const Gem
     xs[2 * c] = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
     xs[2 * c + 1] = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
   }
-  gate::route_block(P.logits, P.T, P.E, P.k, l_idx, l_cnt, l_off, l_ids, l_run, s_pos);
-  active_experts(l_cnt, P.E, a_e, &a_n);
+  gate::route_block(P.logits, P.T, P.E, P.k, l_idx, l_cnt, l_off, l_ids, l_run, s_pos, a_e, &a_n);
+  if (P.T != 1) active_experts(l_cnt, P.E, a_e, &a_n);   // one token: listed by route_block
   if (tid == 0) abort_flag = 0;
   __syncthreads();
   const int G = gridDim.x, b = blockIdx.x;

@@ -635,12 +635,61 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
 // equal logits, as the routing kernels choose), then every expert's count, its
 // offset and its tokens in slot order (the stable expert order of the align
 // step). All arrays in shared memory: idx[T*k], cnt[E], off[E+1], ids[T*k], run[E],
-// and (when not null) pos[T*k]: the sorted position of every slot.
+// and (when not null) pos[T*k]: the sorted position of every slot. One token (a
+// decode step) takes a shorter path in warp 0 alone: every expert's rank in the
+// row, and from the k best the counts, offsets and slot positions directly; it
+// also writes (when not null) active[0, k): the chosen experts ascending, and
+// *n_active = k (otherwise untouched).
 __device__ __forceinline__ void route_block(const float* __restrict__ logits, int T, int E, int k,
                                             int32_t* idx, int32_t* cnt, int32_t* off, int32_t* ids,
-                                            int32_t* run, int32_t* pos = nullptr) {
+                                            int32_t* run, int32_t* pos = nullptr, int32_t* active = nullptr,
+                                            int* n_active = nullptr) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int S = T * k;
+  if (T == 1) {
+    if (warp == 0) {
+      unsigned key[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) key[i] = lane + 32 * i < E ? okey(__ldg(logits + lane + 32 * i)) : 0u;
+      // rank of expert lane + 32 i: the experts ahead of it (larger logit, or an
+      // equal one at a lower index); experts past E hold key 0 and come last
+      int rk[2] = {0, 0};
+#pragma unroll 8
+      for (int src = 0; src < 32; ++src) {
+        const unsigned o0 = __shfl_sync(0xffffffffu, key[0], src), o1 = __shfl_sync(0xffffffffu, key[1], src);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int me = lane + 32 * i;
+          rk[i] += (o0 > key[i] || (o0 == key[i] && src < me)) + (o1 > key[i] || (o1 == key[i] && src + 32 < me));
+        }
+      }
+      const bool sel0 = lane < E && rk[0] < k, sel1 = lane + 32 < E && rk[1] < k;
+      const unsigned b0 = __ballot_sync(0xffffffffu, sel0), b1 = __ballot_sync(0xffffffffu, sel1);
+      const unsigned below = (1u << lane) - 1u;
+      const int o[2] = {__popc(b0 & below), __popc(b0) + __popc(b1 & below)};
+      const bool sel[2] = {sel0, sel1};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int me = lane + 32 * i;
+        if (me < E) {
+          cnt[me] = sel[i] ? 1 : 0;
+          off[me] = o[i];
+        }
+        if (sel[i]) {
+          idx[rk[i]] = me;
+          ids[o[i]] = 0;
+          if (pos) pos[rk[i]] = o[i];
+          if (active) active[o[i]] = me;
+        }
+      }
+      if (lane == 0) {
+        off[E] = k;
+        if (n_active) *n_active = k;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   for (int t = warp; t < T; t += nwarps) {
     const float* row = logits + (long)t * E;
     unsigned key[2];

@@ -102,6 +102,20 @@ def test_layer_matrix_vector_shapes(T, H, I, E, k, norm):
                                        logits="distinct", seed=T * 11 + E))
 
 
+# one token routed inside each CTA by expert ranks: logits on a coarse grid (ties inside
+# and across the top k), all equal (the k lowest experts win), E below one warp's width
+@pytest.mark.parametrize("E,k,kind,H,I", [(64, 8, "coarse", 2048, 1408), (40, 6, "coarse", 256, 128),
+                                          (64, 8, "flat", 256, 128), (17, 5, "flat", 128, 64),
+                                          (33, 32, "coarse", 128, 64)])
+def test_layer_one_token_tied_logits(E, k, kind, H, I):
+    moe = need_gpu()
+    d = make_layer_inputs(T=1, H=H, I=I, E=E, k=k, norm_topk_prob=True, dtype="bf16", logits="distinct",
+                          seed=E + k)
+    d["logits"] = (np.round(d["logits"] * 2) / 2 if kind == "coarse" else
+                   np.full_like(d["logits"], 0.25)).astype(np.float32)
+    _full_check(moe, d)
+
+
 # CUDA-core path: float32, and bf16 shapes the tensor path does not take
 @pytest.mark.parametrize("T,H,I,E,k,dtype", [
     (64, 128, 256, 8, 2, "f32"),
