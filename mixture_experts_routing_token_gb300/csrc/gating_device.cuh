@@ -96,6 +96,69 @@ __device__ __forceinline__ int warp_argmax_round(const unsigned (&key)[V], unsig
   return (int)__reduce_min_sync(0xffffffffu, cand);
 }
 
+// One thread's token (row v[0, V), experts past E ignored), K = k: each round an
+// arg-max tree over the row (a right node wins only when strictly larger: the
+// lower expert among equal values), the winner then set to -inf; the selected
+// numerators are kept (the first, exp(m - m), is exactly 1). Weights as in
+// gate_one_token.
+template <int V, int K>
+__device__ __forceinline__ void gate_row_regs(const float (&v)[V], int E, int norm, long t,
+                                              float* __restrict__ w_out, int32_t* __restrict__ idx_out) {
+  float w[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) w[i] = i < E ? v[i] : -INFINITY;
+  float ex[K], m = 0.0f, hi = 0.0f, lo = 0.0f;
+  int sid[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    float tv[V];
+    int ti[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) { tv[i] = w[i]; ti[i] = i; }
+#pragma unroll
+    for (int st = 1; st < V; st *= 2)
+#pragma unroll
+      for (int i = 0; i + st < V; i += 2 * st) {
+        const bool right = tv[i + st] > tv[i];
+        tv[i] = right ? tv[i + st] : tv[i];
+        ti[i] = right ? ti[i + st] : ti[i];
+      }
+    if (j == 0) m = tv[0];
+    sid[j] = ti[0];
+    if (j + 1 < K) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) w[i] = i == ti[0] ? -INFINITY : w[i];
+    }
+    ex[j] = j == 0 ? 1.0f : exp_diff(tv[0], m);
+    if (norm) two_sum_add(hi, lo, ex[j]);
+  }
+  if (!norm) {
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (i < E) two_sum_add(hi, lo, exp_diff(v[i], m));
+  }
+  const float denom = hi + lo;
+  float wj[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) wj[j] = __fdiv_rn(ex[j], denom);
+  if constexpr (K == 2) {   // whole rows as one 8-byte store each (outputs 16-byte aligned)
+    reinterpret_cast<float2*>(w_out)[t] = make_float2(wj[0], wj[1]);
+    reinterpret_cast<int2*>(idx_out)[t] = make_int2(sid[0], sid[1]);
+  } else if constexpr (K == 4 || K == 8) {
+#pragma unroll
+    for (int q = 0; q < K / 4; ++q) {
+      reinterpret_cast<float4*>(w_out)[t * (K / 4) + q] = make_float4(wj[4 * q], wj[4 * q + 1], wj[4 * q + 2], wj[4 * q + 3]);
+      reinterpret_cast<int4*>(idx_out)[t * (K / 4) + q] = make_int4(sid[4 * q], sid[4 * q + 1], sid[4 * q + 2], sid[4 * q + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      w_out[t * K + j] = wj[j];
+      idx_out[t * K + j] = sid[j];
+    }
+  }
+}
+
 // Top-k and softmax of one token's logits row by the L lanes of a group (V <= 64); lane
 // g holds the contiguous experts [g*V, g*V + V) (vector loads when E % 4 == 0).
 // Each of the k rounds takes the best remaining value of every lane (strictly
@@ -160,61 +223,18 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
     if (bi / V == g) taken |= 1ull << (bi - base);
   };
   if (L == 1 && k <= kRegSel) {
-    // one thread per token, the row in registers: each round an arg-max tree over
-    // the row (a right node wins only when strictly larger: the lower expert among
-    // equal values), the winner then set to -inf; the selected numerators are kept
-    // (the first, exp(m - m), is exactly 1)
-    float w[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) w[i] = base + i < E ? v[i] : -INFINITY;
-    float ex[kRegSel];
-    int sid[kRegSel];
-#pragma unroll
-    for (int j = 0; j < kRegSel; ++j) {
-      ex[j] = 0.0f;
-      sid[j] = 0;
-      if (j < k) {
-        float tv[V];
-        int ti[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) { tv[i] = w[i]; ti[i] = i; }
-#pragma unroll
-        for (int st = 1; st < V; st *= 2)
-#pragma unroll
-          for (int i = 0; i + st < V; i += 2 * st) {
-            const bool right = tv[i + st] > tv[i];
-            tv[i] = right ? tv[i + st] : tv[i];
-            ti[i] = right ? ti[i + st] : ti[i];
-          }
-        if (j == 0) m = tv[0];
-        sid[j] = base + ti[0];
-#pragma unroll
-        for (int i = 0; i < V; ++i) w[i] = i == ti[0] ? -INFINITY : w[i];
-        ex[j] = j == 0 ? 1.0f : exp_diff(tv[0], m);
-        if (norm) two_sum_add(hi, lo, ex[j]);
-      }
+    // one thread per token, the row in registers, k known at compile time (a loop
+    // over runtime k would issue every round's instructions under predicates)
+    switch (k) {
+      case 1: return gate_row_regs<V, 1>(v, E, norm, t, w_out, idx_out);
+      case 2: return gate_row_regs<V, 2>(v, E, norm, t, w_out, idx_out);
+      case 3: return gate_row_regs<V, 3>(v, E, norm, t, w_out, idx_out);
+      case 4: return gate_row_regs<V, 4>(v, E, norm, t, w_out, idx_out);
+      case 5: return gate_row_regs<V, 5>(v, E, norm, t, w_out, idx_out);
+      case 6: return gate_row_regs<V, 6>(v, E, norm, t, w_out, idx_out);
+      case 7: return gate_row_regs<V, 7>(v, E, norm, t, w_out, idx_out);
+      default: return gate_row_regs<V, 8>(v, E, norm, t, w_out, idx_out);
     }
-    if (!norm) {
-#pragma unroll
-      for (int i = 0; i < V; ++i)
-        if (base + i < E) two_sum_add(hi, lo, exp_diff(v[i], m));
-    }
-    const float denom = hi + lo;
-    float wj[kRegSel];
-#pragma unroll
-    for (int j = 0; j < kRegSel; ++j) wj[j] = j < k ? __fdiv_rn(ex[j], denom) : 0.0f;
-    if (k == 2) {   // the row's two results as one 8-byte store each (outputs 16-byte aligned)
-      reinterpret_cast<float2*>(w_out)[t] = make_float2(wj[0], wj[1]);
-      reinterpret_cast<int2*>(idx_out)[t] = make_int2(sid[0], sid[1]);
-      return;
-    }
-#pragma unroll
-    for (int j = 0; j < kRegSel; ++j)
-      if (j < k) {
-        w_out[t * k + j] = wj[j];
-        idx_out[t * k + j] = sid[j];
-      }
-    return;
   }
   for (int j = 0; j < k; ++j) {
     float bv;

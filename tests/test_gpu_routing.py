@@ -36,7 +36,8 @@ def test_gating_on_workload_logits(name):
     _gating_case(moe, x, wl.k, not wl.norm_topk_prob)
 
 
-@pytest.mark.parametrize("E,k", [(1, 1), (2, 1), (3, 2), (5, 5), (7, 3), (8, 8), (16, 4), (31, 1),
+@pytest.mark.parametrize("E,k", [(1, 1), (2, 1), (3, 2), (4, 4), (5, 5), (7, 3), (7, 7), (8, 4), (8, 6), (8, 8),
+                                 (16, 4), (31, 1),
                                  (32, 32), (33, 8), (64, 4), (96, 8), (100, 6), (128, 1), (128, 8), (200, 16),
                                  (256, 8), (1000, 32), (1024, 2)])
 @pytest.mark.parametrize("norm", [True, False])
