@@ -96,6 +96,37 @@ __device__ __forceinline__ int warp_argmax_round(const unsigned (&key)[V], unsig
   return (int)__reduce_min_sync(0xffffffffu, cand);
 }
 
+// Experts [base, base + V) of one logits row as float32 (0 past E); 16-byte vector
+// loads when E allows them.
+template <int V, typename In>
+__device__ __forceinline__ void load_row_part(const In* __restrict__ row, int base, int E, float (&v)[V]) {
+  if constexpr (!std::is_same<In, float>::value) {
+    if ((V % 8) == 0 && (E & 7) == 0) {
+#pragma unroll
+      for (int q = 0; q < V / 8; ++q) {
+        const int e0 = base + 8 * q;
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (e0 < E) load8_bf16(row + e0, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * q + i] = x[i];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = base + i < E ? load_logit(row + base + i) : 0.0f;
+    }
+  } else if ((V % 4) == 0 && (E & 3) == 0) {
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+      const int e0 = base + 4 * q;
+      const float4 x = e0 < E ? __ldg(reinterpret_cast<const float4*>(row + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) v[i] = base + i < E ? __ldg(row + base + i) : 0.0f;
+  }
+}
+
 // One thread's token (row v[0, V), experts past E ignored), K = k: each round an
 // arg-max tree over the row (a right node wins only when strictly larger: the
 // lower expert among equal values), the winner then set to -inf; the selected
@@ -174,33 +205,8 @@ __device__ __forceinline__ void gate_one_token(const In* __restrict__ logits, lo
   const int g = threadIdx.x & (L - 1);
   const unsigned gm = group_mask<L>();
   const int base = g * V;
-  const In* row = logits + t * (long)E;
   float v[V];
-  if constexpr (!std::is_same<In, float>::value) {
-    if ((V % 8) == 0 && (E & 7) == 0) {
-#pragma unroll
-      for (int q = 0; q < V / 8; ++q) {
-        const int e0 = base + 8 * q;
-        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (e0 < E) load8_bf16(row + e0, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * q + i] = x[i];
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < V; ++i) v[i] = base + i < E ? load_logit(row + base + i) : 0.0f;
-    }
-  } else if ((V % 4) == 0 && (E & 3) == 0) {
-#pragma unroll
-    for (int q = 0; q < V / 4; ++q) {
-      const int e0 = base + 4 * q;
-      const float4 x = e0 < E ? __ldg(reinterpret_cast<const float4*>(row + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < V; ++i) v[i] = base + i < E ? __ldg(row + base + i) : 0.0f;
-  }
+  load_row_part<V>(logits + t * (long)E, base, E, v);
   uint64_t taken = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i)

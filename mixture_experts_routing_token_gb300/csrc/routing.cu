@@ -36,6 +36,30 @@ __global__ void __launch_bounds__(kBlock, L == 1 ? 6 : 1) gating_kernel(const In
   gate::gate_one_token<L, V, In>(logits, t, E, k, norm, w_out, idx_out);
 }
 
+// Gating for E <= 8, K = k: a thread per token over a grid-stride loop, the next
+// token's row loaded before the current one is ranked (one row in flight while
+// the thread computes).
+template <int K, typename In>
+__global__ void __launch_bounds__(kBlock, 6) gating_rows8_kernel(const In* __restrict__ logits, int T, int E,
+                                                                 int norm, float* __restrict__ w_out,
+                                                                 int32_t* __restrict__ idx_out) {
+  const long stride = (long)gridDim.x * kBlock;
+  long t = (long)blockIdx.x * kBlock + threadIdx.x;
+  if (t >= T) return;
+  float v[8];
+  gate::load_row_part<8>(logits + t * (long)E, 0, E, v);
+  for (;;) {
+    const long tn = t + stride;
+    float nv[8];
+    if (tn < T) gate::load_row_part<8>(logits + tn * (long)E, 0, E, nv);
+    gate::gate_row_regs<8, K>(v, E, norm, t, w_out, idx_out);
+    if (tn >= T) break;
+    t = tn;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = nv[i];
+  }
+}
+
 // Gating for E <= 128, one thread per token: each CTA stages its 128 rows in
 // shared memory and runs gate::topk_staged_row on them (gating_device.cuh).
 constexpr int kSmemGateThreads = gate::kStageRows;
@@ -170,6 +194,28 @@ int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w
   if (int rc = ensure_smem_limit(gating_smem_kernel<EP, In>, smem, "gating_softmax_topk")) return rc;
   gating_smem_kernel<EP, In><<<grid, kSmemGateThreads, smem, s>>>(logits, T, E, k, norm, w, idx);
   return check_launch("gating_softmax_topk");
+}
+
+template <int K, typename In>
+int launch_rows8(const In* logits, int T, int E, int norm, float* w, int32_t* idx, cudaStream_t s) {
+  const long blocks = ((long)T + kBlock - 1) / kBlock, cap = (long)num_sms() * 6;
+  gating_rows8_kernel<K, In><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(logits, T, E, norm, w, idx);
+  return check_launch("gating_softmax_topk");
+}
+
+template <typename In>
+int launch_gating_rows8(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
+                        cudaStream_t s) {
+  switch (k) {
+    case 1: return launch_rows8<1, In>(logits, T, E, norm, w, idx, s);
+    case 2: return launch_rows8<2, In>(logits, T, E, norm, w, idx, s);
+    case 3: return launch_rows8<3, In>(logits, T, E, norm, w, idx, s);
+    case 4: return launch_rows8<4, In>(logits, T, E, norm, w, idx, s);
+    case 5: return launch_rows8<5, In>(logits, T, E, norm, w, idx, s);
+    case 6: return launch_rows8<6, In>(logits, T, E, norm, w, idx, s);
+    case 7: return launch_rows8<7, In>(logits, T, E, norm, w, idx, s);
+    default: return launch_rows8<8, In>(logits, T, E, norm, w, idx, s);
+  }
 }
 
 template <int L, int V, typename In>
@@ -987,14 +1033,14 @@ int launch_group_t(const float* scores, const float* bias, int T, int E, int k, 
   return check_launch("group_limited_topk");
 }
 
-// E <= 8: a thread per token, row in registers; E <= 128: the staged thread-per-token
+// E <= 8: a thread per token, row in registers (k <= E <= 8); E <= 128: the staged thread-per-token
 // kernel; wider rows: L lanes of 64 experts per token.
 template <typename In>
 int launch_gating_any(const In* logits, int T, int E, int k, int norm, float* w, int32_t* idx,
                       cudaStream_t s, const char* name) {
   if (T == 0) return MOE_OK;
   ProfScope ps(name, s);
-  if (E <= 8) return launch_gating_t<1, 8, In>(logits, T, E, k, norm, w, idx, s);
+  if (E <= 8) return launch_gating_rows8<In>(logits, T, E, k, norm, w, idx, s);
   if (E <= 16) return launch_gating_smem<16, In>(logits, T, E, k, norm, w, idx, s);
   if (E <= 32) return launch_gating_smem<32, In>(logits, T, E, k, norm, w, idx, s);
   if (E <= 64) return launch_gating_smem<64, In>(logits, T, E, k, norm, w, idx, s);
