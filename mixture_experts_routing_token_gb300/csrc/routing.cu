@@ -38,11 +38,13 @@ __global__ void __launch_bounds__(kBlock, L == 1 ? 6 : 1) gating_kernel(const In
 
 // Gating for E <= 8, K = k: a thread per token over a grid-stride loop, the next
 // token's row loaded before the current one is ranked (one row in flight while
-// the thread computes).
-template <int K, typename In>
-__global__ void __launch_bounds__(kBlock, 6) gating_rows8_kernel(const In* __restrict__ logits, int T, int E,
+// the thread computes). FULL: E == 8, so no expert is masked (the selection is
+// bound by the integer / compare pipe, and the masks cost a sixth of it).
+template <int K, typename In, bool FULL>
+__global__ void __launch_bounds__(kBlock, 6) gating_rows8_kernel(const In* __restrict__ logits, int T, int E_rt,
                                                                  int norm, float* __restrict__ w_out,
                                                                  int32_t* __restrict__ idx_out) {
+  const int E = FULL ? 8 : E_rt;
   const long stride = (long)gridDim.x * kBlock;
   long t = (long)blockIdx.x * kBlock + threadIdx.x;
   if (t >= T) return;
@@ -199,7 +201,9 @@ int launch_gating_smem(const In* logits, int T, int E, int k, int norm, float* w
 template <int K, typename In>
 int launch_rows8(const In* logits, int T, int E, int norm, float* w, int32_t* idx, cudaStream_t s) {
   const long blocks = ((long)T + kBlock - 1) / kBlock, cap = (long)num_sms() * 6;
-  gating_rows8_kernel<K, In><<<(unsigned)(blocks < cap ? blocks : cap), kBlock, 0, s>>>(logits, T, E, norm, w, idx);
+  const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
+  if (E == 8) gating_rows8_kernel<K, In, true><<<grid, kBlock, 0, s>>>(logits, T, E, norm, w, idx);
+  else gating_rows8_kernel<K, In, false><<<grid, kBlock, 0, s>>>(logits, T, E, norm, w, idx);
   return check_launch("gating_softmax_topk");
 }
 
