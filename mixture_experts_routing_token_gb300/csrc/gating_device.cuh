@@ -140,6 +140,45 @@ __device__ __forceinline__ void gate_row_regs(const float (&v)[V], int E, int no
   for (int i = 0; i < V; ++i) w[i] = i < E ? v[i] : -INFINITY;
   float ex[K], m = 0.0f, hi = 0.0f, lo = 0.0f;
   int sid[K];
+  if constexpr (K == 2 && V >= 2) {
+    // the two largest by pairwise merges: every node keeps its range's best and
+    // second (value, expert); a node's left range holds the lower experts, so the
+    // right side wins only when strictly larger, for the best and for the second
+    float bv[V / 2], sv[V / 2];
+    int bi[V / 2], si[V / 2];
+#pragma unroll
+    for (int q = 0; q < V / 2; ++q) {
+      const bool r = w[2 * q + 1] > w[2 * q];
+      bv[q] = r ? w[2 * q + 1] : w[2 * q];
+      bi[q] = r ? 2 * q + 1 : 2 * q;
+      sv[q] = r ? w[2 * q] : w[2 * q + 1];
+      si[q] = r ? 2 * q : 2 * q + 1;
+    }
+#pragma unroll
+    for (int n = V / 2; n > 1; n /= 2)
+#pragma unroll
+      for (int q = 0; q < n / 2; ++q) {
+        const int a = 2 * q, b = 2 * q + 1;
+        const bool r = bv[b] > bv[a];
+        // the second: the losing side's best against the winning side's second
+        const float xv = r ? bv[a] : sv[a], yv = r ? sv[b] : bv[b];
+        const int xi = r ? bi[a] : si[a], yi = r ? si[b] : bi[b];
+        const bool r2 = yv > xv;
+        bv[q] = r ? bv[b] : bv[a];
+        bi[q] = r ? bi[b] : bi[a];
+        sv[q] = r2 ? yv : xv;
+        si[q] = r2 ? yi : xi;
+      }
+    m = bv[0];
+    sid[0] = bi[0];
+    sid[1] = si[0];
+    ex[0] = 1.0f;
+    ex[1] = exp_diff(sv[0], m);
+    if (norm) {
+      two_sum_add(hi, lo, ex[0]);
+      two_sum_add(hi, lo, ex[1]);
+    }
+  } else {
 #pragma unroll
   for (int j = 0; j < K; ++j) {
     float tv[V];
@@ -162,6 +201,7 @@ __device__ __forceinline__ void gate_row_regs(const float (&v)[V], int E, int no
     }
     ex[j] = j == 0 ? 1.0f : exp_diff(tv[0], m);
     if (norm) two_sum_add(hi, lo, ex[j]);
+  }
   }
   if (!norm) {
 #pragma unroll
