@@ -245,6 +245,65 @@ __device__ __forceinline__ void fc1_units(const GemvParams& P, const float4* xs,
   }
 }
 
+// FC1 pair (expert e, columns i and i + 1, i even) by the calling warp: gate rows
+// i, i + 1 and up rows I + i, I + i + 1 of w13[e] (two contiguous row pairs, all
+// four rows' pieces in flight together) against the expert's token rows,
+// silu_and_mul, both activations written by lane 0 as one 4-byte store.
+template <int TT>
+__device__ __forceinline__ void fc1_pair(const GemvParams& P, const float4* xs, int e, const int32_t* counts,
+                                         const int32_t* offsets, const int32_t* sorted_ids, int i, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  const int nch = P.H >> 3;
+  const int cnt = min(counts[e], TT);
+  const int p0 = offsets[e];
+  int tok[TT];
+#pragma unroll
+  for (int r = 0; r < TT; ++r) tok[r] = r < cnt ? sorted_ids[p0 + r] : 0;
+  const uint4* g = P.w13 + ((long)e * 2 * P.I + i) * nch;   // gate rows i, i + 1
+  const uint4* up = g + (long)P.I * nch;                     // up rows I + i, I + i + 1
+  float acc[4][TT];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int r = 0; r < TT; ++r) acc[q][r] = 0.0f;
+  for (int c0 = 0; c0 < nch; c0 += 32 * kPieces) {
+    uint4 wv[4][kPieces];
+#pragma unroll
+    for (int b = 0; b < kPieces; ++b) {
+      const int c = c0 + b * 32 + lane;
+      if (c < nch) {
+        wv[0][b] = ld_stream(g + c, pol);
+        wv[1][b] = ld_stream(g + nch + c, pol);
+        wv[2][b] = ld_stream(up + c, pol);
+        wv[3][b] = ld_stream(up + nch + c, pol);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kPieces; ++b) {
+      const int c = c0 + b * 32 + lane;
+      if (c < nch) {
+#pragma unroll
+        for (int r = 0; r < TT; ++r)
+          if (r < cnt) {
+            const float4 x0 = xs[(tok[r] * nch + c) * 2], x1 = xs[(tok[r] * nch + c) * 2 + 1];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q][r] = dot8f(wv[q][b], x0, x1, acc[q][r]);
+          }
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int r = 0; r < TT; ++r) acc[q][r] = warp_sum(acc[q][r]);
+  if (lane == 0)
+#pragma unroll
+    for (int r = 0; r < TT; ++r)
+      if (r < cnt)
+        *reinterpret_cast<__nv_bfloat162*>(P.act + (long)(p0 + r) * P.I + i) =
+            __floats2bfloat162_rn(silu(acc[0][r]) * acc[2][r], silu(acc[1][r]) * acc[3][r]);
+}
+
 // FC2 unit u = c * T + t: the weight rows of the token's valid slots (s_e[q] >= 0)
 // into buf [k][I / 8], asynchronously, by the calling warp.
 __device__ __forceinline__ void fc2_fetch(const GemvParams& P, const int32_t* s_e, long u, uint4* buf,
@@ -422,8 +481,9 @@ __global__ void __launch_bounds__(kFc2Threads, 1) fc2_gemv_kernel(const GemvPara
 // activation rows) over rows that bulk copies (one per row, two experts ahead)
 // bring into shared memory. The combine: out[t][c] = sum
 // over j of w_j * (row c of w2[e_j] . act_j), float32 in j order, rounded once.
+constexpr int kPipeThreads = 384;   // 12 warps of up to 168 registers: FC1 warps keep 16 KB in flight
 constexpr int kPipeFc2Warps = 2;    // each takes every other expert
-constexpr int kPipeFc1Warps = kLayerThreads / 32 - kPipeFc2Warps;
+constexpr int kPipeFc1Warps = kPipeThreads / 32 - kPipeFc2Warps;
 constexpr int kPipeFc2Threads = kPipeFc2Warps * 32;
 constexpr int kPipeCols = 32;   // most output columns per CTA
 static_assert(kMaxSlots + 1 <= kDecodeSyncWords, "one counter per active expert, one of FC1 units taken");
@@ -457,7 +517,7 @@ __host__ __device__ inline size_t pipe_smem(int T, int TT, int H, int I, int G) 
 }
 
 template <int TT>
-__global__ void __launch_bounds__(kLayerThreads, 1) decode_pipe_kernel(const GemvParams P) {
+__global__ void __launch_bounds__(kPipeThreads, 1) decode_pipe_kernel(const GemvParams P) {
   extern __shared__ float4 pipe_raw[];
   __shared__ int32_t l_idx[kMaxSlots], l_ids[kMaxSlots];
   __shared__ int32_t l_cnt[kRouteExperts], l_off[kRouteExperts + 1], l_run[kRouteExperts];
@@ -472,7 +532,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_pipe_kernel(const Gem
   uint4* acts = reinterpret_cast<uint4*>(pipe_raw + (long)P.T * P.H / 4);  // [W][TT][I / 8 + 1]
   uint4* wbuf = acts + (long)kPipeFc2Warps * TT * ((P.I >> 3) + 1);         // [W][nb][ceil(H / G)][I / 8 + 1]
   // the token rows by the warps that do not route (their loads overlap the logits')
-  for (long c = tid - 64; c >= 0 && c < (long)P.T * P.H / 8; c += kLayerThreads - 64) {
+  for (long c = tid - 64; c >= 0 && c < (long)P.T * P.H / 8; c += kPipeThreads - 64) {
     const uint4 v = P.hidden[c];
     xs[2 * c] = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
     xs[2 * c + 1] = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
@@ -490,20 +550,21 @@ __global__ void __launch_bounds__(kLayerThreads, 1) decode_pipe_kernel(const Gem
     // streams), so CTAs that run faster take more of them and the experts still
     // complete in order
     const uint64_t pol = evict_first_policy();
-    const long U1 = (long)a_n * I, nfirst = (long)kPipeFc1Warps * G;
+    const int Ih = I >> 1;   // column pairs per expert (I is even here)
+    const long U1 = (long)a_n * Ih, nfirst = (long)kPipeFc1Warps * G;
     int32_t* work = P.sync + kMaxSlots;
     long u = b + (long)G * warp;
     int next = 0;
     for (bool first = true; u < U1; first = false) {
       if (!first && lane == 0) next = atomicAdd(work, 1);
-      const int a = (int)(u / I), i = (int)(u - (long)a * I);
-      fc1_unit<TT>(P, xs, a_e[a], l_cnt, l_off, l_ids, i, pol);
+      const int a = (int)(u / Ih), i = 2 * (int)(u - (long)a * Ih);
+      fc1_pair<TT>(P, xs, a_e[a], l_cnt, l_off, l_ids, i, pol);
       if (first) {   // the routing kernel (complete from here on) zeroed the counters
         pdl_wait();
         if (lane == 0) next = atomicAdd(work, 1);
       }
-      if (lane == 0)   // the activation (this lane's store) before its count
-        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(done + a) : "memory");
+      if (lane == 0)   // the activations (this lane's store) before their count
+        asm volatile("red.release.gpu.global.add.s32 [%0], 2;" ::"l"(done + a) : "memory");
       u = nfirst + __shfl_sync(0xffffffffu, next, 0);
     }
     return;   // no barrier of the whole CTA follows
@@ -663,7 +724,7 @@ int run_gemv(const FfnArgs& a, cudaStream_t s) {
   const int G = num_sms() - 1;
   if (local && a.sync && G >= 1 && (a.H + G - 1) / G <= kPipeCols && (a.H * 2) % 128 == 0 && (a.I * 2) % 128 == 0 &&
       pipe_smem(a.T, TT, a.H, a.I, G) <= kPipeSmemMax)
-    return launch_one(decode_pipe_kernel<TT>, G, kLayerThreads, pipe_smem(a.T, TT, a.H, a.I, G), s, p,
+    return launch_one(decode_pipe_kernel<TT>, G, kPipeThreads, pipe_smem(a.T, TT, a.H, a.I, G), s, p,
                       "ffn_decode_layer");
   const int rc = launch_one(fc1_gemv_kernel<TT>, 2 * num_sms(), kGemvThreads, (size_t)a.T * a.H * 4, s, p,
                             "ffn_fc1_gemv");
