@@ -226,30 +226,42 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
     ws = torch.empty(max(1, moe.moe_align_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
     al = moe.moe_align_by_expert(idx, w, E, workspace=ws)
     calls = {
-        "gating_softmax_topk": lambda: moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob, weights=w,
-                                                                   indices=idx, stream=stream),
-        "gating_softmax_topk_bf16": lambda: moe.moe_gating_softmax_topk_bf16(
-            logits_bf16, k, wl.norm_topk_prob, weights=w, indices=idx, stream=stream),
-        "indices_to_multihot": lambda: moe.moe_indices_to_multihot(idx, w, E, multihot=mh, probs_in_multihot=pm,
-                                                                   position_map=pos, stream=stream),
-        "multihot_to_indices": lambda: moe.moe_multihot_to_indices(pm, pos, k, probs=p2, indices=i2, stream=stream),
-        "align_by_expert": lambda: moe.moe_align_by_expert(idx, w, E, out=al, workspace=ws, stream=stream),
+        "gating_softmax_topk": lambda st: moe.moe_gating_softmax_topk(logits, k, wl.norm_topk_prob, weights=w,
+                                                                      indices=idx, stream=st),
+        "gating_softmax_topk_bf16": lambda st: moe.moe_gating_softmax_topk_bf16(
+            logits_bf16, k, wl.norm_topk_prob, weights=w, indices=idx, stream=st),
+        "indices_to_multihot": lambda st: moe.moe_indices_to_multihot(idx, w, E, multihot=mh, probs_in_multihot=pm,
+                                                                      position_map=pos, stream=st),
+        "multihot_to_indices": lambda st: moe.moe_multihot_to_indices(pm, pos, k, probs=p2, indices=i2, stream=st),
+        "align_by_expert": lambda st: moe.moe_align_by_expert(idx, w, E, out=al, workspace=ws, stream=st),
     }
     res = {}
+    inner = 10   # calls per captured graph: the timed launches run back to back, with no host gap
 
-    def timed(fn, nbytes):
+    def timed(fn, nbytes, tokens=T):
         for _ in range(2):
-            fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            fn(stream)
         torch.cuda.synchronize()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(gr, stream=side, capture_error_mode="thread_local"):
+                for _ in range(inner):
+                    fn(side)
+        torch.cuda.synchronize()
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(reps):
-            fn()
+            gr.replay()
         b.record(stream)
         torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
+        ms = a.elapsed_time(b) / (reps * inner)
         gbs = nbytes / (ms / 1e3) / 1e9
-        return {"tokens": T, "us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+        return {"tokens": tokens, "us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "bytes": nbytes,
+                "timing": "CUDA graph of %d calls replayed %d times" % (inner, reps)}
 
     for name, fn in calls.items():
         res[name] = timed(fn, per_tok[name] * T)
@@ -261,8 +273,8 @@ def routing_bandwidth(moe, wl, dev, peaks, reps=10, target_bytes=768 << 20):
     bias = 0.05 * torch.randn((Eg,), generator=g, device=dev)
     gw, gi = moe.moe_group_limited_topk(sc, kg, 8, 4, "noaux_tc", bias=bias)
     res["group_limited_topk"] = timed(
-        lambda: moe.moe_group_limited_topk(sc, kg, 8, 4, "noaux_tc", bias=bias, weights=gw, indices=gi, stream=stream),
-        (4 * Eg + 8 * kg) * Tg)
+        lambda st: moe.moe_group_limited_topk(sc, kg, 8, 4, "noaux_tc", bias=bias, weights=gw, indices=gi, stream=st),
+        (4 * Eg + 8 * kg) * Tg, Tg)
     res["group_limited_topk"]["shape"] = "E=256, n_group=8, topk_group=4, k=8, noaux_tc"
     return res
 
