@@ -77,6 +77,26 @@ def test_gating_bf16_logits(E, k, norm):
     assert torch.equal(i, i32) and torch.equal(w.view(torch.int32), w32.view(torch.int32))
 
 
+# rows of at most 8 experts on enough tokens that the grid-stride kernel loops (more
+# rows than 6 blocks of 256 threads per SM) with a ragged last pass; float32 and bf16
+# (bit-identical to the float32 entry on the widened rows), full (E = 8) and partial rows
+@pytest.mark.parametrize("E,k,norm", [(8, 2, True), (8, 3, False), (6, 2, True), (8, 8, True)])
+def test_gating_small_rows_over_many_tokens(E, k, norm):
+    moe = need_gpu()
+    T = 400_003
+    x = gen_logits(np.random.SeedSequence(E * 131 + k), T, E, "plain")
+    _gating_case(moe, x, k, norm)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    w_ref, i_ref = gating.softmax_topk_bf16(bits, k, norm)
+    w, i = moe.moe_gating_softmax_topk_bf16(xb, k, norm)
+    w32, i32 = moe.moe_gating_softmax_topk(xb.float(), k, norm)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(i.cpu().numpy(), i_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=W_RTOL, atol=0)
+    assert torch.equal(i, i32) and torch.equal(w.view(torch.int32), w32.view(torch.int32))
+
+
 @pytest.mark.parametrize("E,gap", [(64, 1.0), (64, 2.3), (128, 2.3), (128, 4.0)])
 def test_gating_full_softmax_near_flat_rows(E, gap):
     """norm_topk_prob = False sums all E exponentials; rows whose other logits sit
