@@ -675,8 +675,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1) decode_pipe_kernel(const Gemv
                 (d[0][2 * h + q] + d[1][2 * h + q]) + (d[2][2 * h + q] + d[3][2 * h + q]);
     }
     __syncwarp();   // this warp's activation rows and buffer are free again
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before the copy engine rewrites the buffer
-    fetch(a + nb * W);
+    if (a + nb * W < a_n) {   // a copy will rewrite the buffer: order the reads above before it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      fetch(a + nb * W);
+    }
   }
   if (aborted) {
     if (lane == 0) {   // no copy in flight when the CTA leaves: experts a, a + W, .. < fetched
