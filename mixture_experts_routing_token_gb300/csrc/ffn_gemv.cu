@@ -505,7 +505,7 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 // warp its activation rows [TT][I + 8] and nb buffers of the CTA's w2 rows of one
 // expert [ceil(H / G)][I + 8] (bf16, rows padded by 16 bytes); nb = 2 where that
 // fits (the rows of an expert two of the warp's turns ahead in flight), else 1.
-constexpr size_t kPipeSmemMax = 220 * 1024;
+constexpr size_t kPipeSmemMax = 216 * 1024;   // + the kernel's ~10 KB of static shared memory <= 227 KB
 __host__ __device__ inline size_t pipe_smem_nb(int T, int TT, int H, int I, int G, int nb) {
   return (size_t)T * H * 4 + (size_t)kPipeFc2Warps * ((size_t)TT + (size_t)nb * ((H + G - 1) / G)) * (I + 8) * 2;
 }
