@@ -479,6 +479,44 @@ __device__ __forceinline__ float group_max8(const uint16_t* col, int g, int r) {
   return fmaxf(__low2float(m), __high2float(m));
 }
 
+// Of the 8 staged values of group g of row r: eq, bit c set where value c equals v
+// (as float32: -0 and +0 equal), and rest, the largest of the others (-inf if none).
+// float32 stages as trees over the values; 16-bit stages on packed bf16 pairs (v is
+// itself a staged value, so exact as bf16): pair comparisons give the mask, the
+// matching halves become -inf by a bitwise select, and pair maxima give the rest.
+template <typename Lay = StagePadded>
+__device__ __forceinline__ void group_match8(const float* col, int g, int r, float v, unsigned& eq, float& rest) {
+  float x[8];
+  load_group8<Lay>(col, g, r, x);
+  unsigned eqm[8];
+  float ne[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    eqm[c] = x[c] == v ? 1u << c : 0u;
+    ne[c] = x[c] == v ? -INFINITY : x[c];
+  }
+  eq = ((eqm[0] | eqm[1]) | (eqm[2] | eqm[3])) | ((eqm[4] | eqm[5]) | (eqm[6] | eqm[7]));
+  rest = fmaxf(fmaxf(fmaxf(ne[0], ne[1]), fmaxf(ne[2], ne[3])), fmaxf(fmaxf(ne[4], ne[5]), fmaxf(ne[6], ne[7])));
+}
+template <typename Lay = StagePadded>
+__device__ __forceinline__ void group_match8(const uint16_t* col, int g, int r, float v, unsigned& eq, float& rest) {
+  const uint4 q = reinterpret_cast<const uint4*>(col)[Lay::chunk(g, r)];
+  auto h2 = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); };
+  const __nv_bfloat162 vv = __float2bfloat162_rn(v);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t m[4], k[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m[i] = __heq2_mask(h2(w[i]), vv);                   // 0xffff per equal half
+    k[i] = (w[i] & ~m[i]) | (0xff80ff80u & m[i]);      // equal halves -> bf16 -inf
+  }
+  eq = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) eq |= ((m[i] & 1u) | ((m[i] >> 15) & 2u)) << (2 * i);
+  const __nv_bfloat162 mx = __hmax2(__hmax2(h2(k[0]), h2(k[1])), __hmax2(h2(k[2]), h2(k[3])));
+  rest = fmaxf(__low2float(mx), __high2float(mx));
+}
+
 // Shared memory (bytes) of a stage of kStageRows rows padded to EP experts: EP / VE
 // chunk columns of Lay::kRowsLd 16-byte chunks, then (RM false) the float maxima
 // of the rows' groups of 8 [EP / 8][kStageLd].
@@ -605,24 +643,15 @@ __device__ __forceinline__ void topk_staged_row(St* col, int r, long t, int E, i
       for (int i = 3; i >= 0; --i) bi = gv[i] == v ? i : bi;
       bg = 4 * bs + bi;
     }
-    float x[8];
-    load_group8<Lay>(col, bg, r, x);
     // the group's first expert holding v, and its maximum without that expert
-    // (v again when v occurs twice), both as trees rather than 8-step chains
-    unsigned eqm[8];
-    float ne[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      eqm[c] = x[c] == v ? 1u << c : 0u;
-      ne[c] = x[c] == v ? -INFINITY : x[c];
-    }
-    const unsigned eq = ((eqm[0] | eqm[1]) | (eqm[2] | eqm[3])) | ((eqm[4] | eqm[5]) | (eqm[6] | eqm[7]));
+    // (v again when v occurs twice)
+    unsigned eq;
+    float rest;
+    group_match8<Lay>(col, bg, r, v, eq, rest);
     const int bc = __ffs(eq) - 1;
     e = 8 * bg + bc;
     st_neg_inf(col + sofs<St, Lay>(e, r));
-    const float nm = (eq & (eq - 1u)) ? v
-                     : fmaxf(fmaxf(fmaxf(ne[0], ne[1]), fmaxf(ne[2], ne[3])),
-                             fmaxf(fmaxf(ne[4], ne[5]), fmaxf(ne[6], ne[7])));
+    const float nm = (eq & (eq - 1u)) ? v : rest;
     if constexpr (RM) {
 #pragma unroll
       for (int g = 0; g < G; ++g) gmx[g] = g == bg ? nm : gmx[g];
