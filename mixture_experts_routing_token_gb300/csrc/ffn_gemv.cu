@@ -467,11 +467,15 @@ __global__ void __launch_bounds__(kFc2Threads, 1) fc2_gemv_kernel(const GemvPara
 }
 
 // ---- the pipelined one-kernel decode FFN ------------------------------------
-// FC1 warps (the first kPipeFc1Warps) stream FC1 units b, b + G, ... of the flat
-// range [0, a_n * I) (CTA b of G; every CTA finishes expert a's units at about
-// the same time, experts in order) and count each finished unit on its expert's
-// counter (done[a], zeroed by the routing kernel launched just before; the
-// activation is stored and fenced first). The other warps run FC2 behind them:
+// FC1 warps (the first kPipeFc1Warps) stream FC1 column pairs (units of two
+// columns: both gate rows and both up rows in flight together) over the flat
+// range [0, a_n * I / 2), each warp's first pair fixed and the rest taken in
+// order from a counter all CTAs share (every CTA finishes expert a's pairs at
+// about the same time, experts in order), and count each finished pair on its
+// expert's counter (done[a] += 2, zeroed by the routing kernel launched just
+// before; the activations are stored first, the add releases them). FC1 is bound
+// by the bytes each SM keeps in flight, which registers hold: 10 warps of 168
+// registers with 16 KB each. The other warps run FC2 behind them:
 // the CTA owns output columns [c0, c1); for each active expert in turn they wait
 // (bounded) until its I units are counted, stage its activation rows, and take
 // the dot products of their columns' w2 rows (asked of L2 at the start) with
