@@ -27,7 +27,7 @@ using gate::kNone;
 
 constexpr int kBlock = 256;
 template <int L, int V, typename In>
-__global__ void __launch_bounds__(kBlock, L == 1 ? 6 : 1) gating_kernel(const In* __restrict__ logits, int T,
+__global__ void __launch_bounds__(kBlock) gating_kernel(const In* __restrict__ logits, int T,
                                                         int E, int k, int norm,
                                                         float* __restrict__ w_out,
                                                         int32_t* __restrict__ idx_out) {
