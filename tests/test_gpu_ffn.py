@@ -116,6 +116,32 @@ def test_layer_one_token_tied_logits(E, k, kind, H, I):
     _full_check(moe, d)
 
 
+# the small-batch routing kernel waits for the kernel before it on the stream (which
+# here writes the logits) before the FFN kernel, which reads the logits at once, may
+# start: logits produced on the GPU just before each call, no synchronisation between
+@pytest.mark.parametrize("T,E,k", [(1, 64, 8), (2, 32, 4), (5, 16, 2)])
+def test_layer_logits_written_by_the_previous_kernel(T, E, k):
+    moe = need_gpu()
+    H, I = 256, 128
+    d = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, norm_topk_prob=True, dtype="bf16", logits="distinct",
+                          seed=T * 7 + E)
+    hid, w13, w2 = to_dev(d["hidden"], "bf16"), to_dev(d["w13"], "bf16"), to_dev(d["w2"], "bf16")
+    g = torch.Generator(device=DEV)
+    g.manual_seed(T + E)
+    outs, logits_all = [], []
+    for r in range(4):
+        # a chain of device ops ending in the logits: the last one runs right before the call
+        base = torch.randn((T, E), generator=g, device=DEV, dtype=torch.float64)
+        logits = (base * 1.5 + 0.25 * r).to(torch.float32)
+        outs.append(moe.moe_layer_forward(hid, logits, w13, w2, k, True))
+        logits_all.append(logits)
+    torch.cuda.synchronize()
+    for out, logits in zip(outs, logits_all):
+        lg = logits.cpu().numpy()
+        ref = ffn.layer_forward(lg, d["hidden"], d["w13"], d["w2"], k, True, "bf16")["out"]
+        assert_close_rel_max(to_np64(out), ref, layer_tolerance("bf16"), "layer out")
+
+
 # CUDA-core path: float32, and bf16 shapes the tensor path does not take
 @pytest.mark.parametrize("T,H,I,E,k,dtype", [
     (64, 128, 256, 8, 2, "f32"),
