@@ -44,7 +44,6 @@ namespace moe {
 namespace {
 
 constexpr int kGemvThreads = 256;                        // FC1 kernel: two CTAs per SM
-constexpr int kLayerThreads = 512;                       // one-kernel FFN: one CTA per SM
 constexpr int kPieces = 8;                               // FC1: 16-byte pieces per lane per row in flight
 constexpr int kMaxSlots = kGemvMaxTokens * MOE_MAX_TOPK;
 constexpr int kRouteExperts = 64;                        // in-CTA routing (gate::route_block): E <= 64
@@ -482,7 +481,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1) fc2_gemv_kernel(const GemvPara
 // them into shared memory, so FC2 of expert a overlaps FC1 of the later experts
 // and only the last expert's FC2 and the combine follow the FC1 stream. One
 // warp keeps pace: its products are mma.sync tiles (16 w2 rows x the expert's
-// activation rows) over rows that bulk copies (one per row, two experts ahead)
+// activation rows) over rows that bulk copies (one per row, one expert ahead)
 // bring into shared memory. The combine: out[t][c] = sum
 // over j of w_j * (row c of w2[e_j] . act_j), float32 in j order, rounded once.
 constexpr int kPipeThreads = 384;   // 12 warps of up to 168 registers: FC1 warps keep 16 KB in flight
@@ -507,15 +506,15 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 
 // Shared memory of decode_pipe_kernel: token rows [T][H] (float32), then per FC2
 // warp its activation rows [TT][I + 8] and nb buffers of the CTA's w2 rows of one
-// expert [ceil(H / G)][I + 8] (bf16, rows padded by 16 bytes); nb = 2 where that
-// fits (the rows of an expert two of the warp's turns ahead in flight), else 1.
+// expert [ceil(H / G)][I + 8] (bf16, rows padded by 16 bytes). nb = 1: the rows of
+// the warp's next expert are requested once the current one is multiplied (two
+// buffers, the next two experts' rows in flight, measured 0.5% slower at T = 1:
+// their opening requests compete with FC1's first column pairs).
 constexpr size_t kPipeSmemMax = 216 * 1024;   // + the kernel's ~10 KB of static shared memory <= 227 KB
 __host__ __device__ inline size_t pipe_smem_nb(int T, int TT, int H, int I, int G, int nb) {
   return (size_t)T * H * 4 + (size_t)kPipeFc2Warps * ((size_t)TT + (size_t)nb * ((H + G - 1) / G)) * (I + 8) * 2;
 }
-__host__ __device__ inline int pipe_buffers(int T, int TT, int H, int I, int G) {
-  return pipe_smem_nb(T, TT, H, I, G, 2) <= kPipeSmemMax ? 2 : 1;
-}
+__host__ __device__ inline int pipe_buffers(int, int, int, int, int) { return 1; }
 __host__ __device__ inline size_t pipe_smem(int T, int TT, int H, int I, int G) {
   return pipe_smem_nb(T, TT, H, I, G, pipe_buffers(T, TT, H, I, G));
 }
